@@ -1,0 +1,48 @@
+"""Work and traffic accounting for the attention forward pass.
+
+FLOPs: each head does two contractions, S = Q K^T (2 N^2 d) and O = P V (2 N^2 d_v),
+so 2 N^2 (d + d_v) per head; a causal mask keeps half of the score matrix, so the
+count is halved. The method stays quadratic in work; only the N x N intermediates
+leave HBM ("Compilers and kernels", section "FlashAttention rewrites the algorithm
+around IO": exactness and the remark that the arithmetic is still quadratic).
+
+Algorithmic bytes (the traffic a kernel that reads every input once and writes every
+output once must move): Q, K, V in bf16, O in its output dtype, LSE in fp32, and the
+dense fp32 bias C when there is one. S and P count zero bytes: keeping them on chip
+is the method. The materialised alternative writes S and reads it, writes P and reads
+it ("AI Infra ch. 5", section 5.3 "FlashAttention", the L = 8192, d = 128 example).
+"""
+from __future__ import annotations
+
+BF16 = 2
+F32 = 4
+MiB = 1 << 20
+GiB = 1 << 30
+
+
+def flops(BH: int, N: int, d: int, dv: int, causal: bool) -> float:
+    """Algorithmic FLOPs of one forward pass: 2 * BH * N^2 * (d + dv), halved when causal."""
+    f = 2.0 * BH * N * N * (d + dv)
+    return f / 2.0 if causal else f
+
+
+def required_bytes(BH: int, N: int, d: int, dv: int, out_bytes: int, lse: bool = True,
+                   dense_bias: bool = False) -> int:
+    """Bytes of reading Q, K, V (bf16) and C (fp32, dense mode) once and writing O and LSE once."""
+    b = BH * N * (d + d + dv) * BF16 + BH * N * dv * out_bytes
+    if lse:
+        b += BH * N * F32
+    if dense_bias:
+        b += BH * N * N * F32
+    return b
+
+
+def materialized_intermediate_bytes(N: int, elem_bytes: int = F32) -> dict:
+    """Sizes of S and P for one head and the traffic of writing and re-reading both."""
+    s = N * N * elem_bytes
+    return {"S": s, "P": s, "roundtrip": 4 * s}
+
+
+def roofline_time_s(F: float, Q_bytes: float, peak_flops: float, peak_bytes_per_s: float) -> float:
+    """Lower bound T >= max(F / P_max, Q / B_max) ("Compilers and kernels", roofline section)."""
+    return max(F / peak_flops, Q_bytes / peak_bytes_per_s)

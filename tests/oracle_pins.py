@@ -1,0 +1,432 @@
+"""Pins for the CPU oracle: facts fixed by the attention pages and by mathematics.
+
+Each pin takes an ``oracle.Oracle`` and raises AssertionError when the oracle
+breaks the fact it checks. tests/test_oracle_pins.py runs them on the committed
+oracle; tests/test_oracle_mutants.py runs them on copies of the oracle source with
+a planted mistake and requires that some pin fails for every mistake.
+
+Sources of the facts:
+  * "Compilers and kernels" (aaai.latere.ai/zh/infrastructure/compilers-kernels),
+    section "FlashAttention rewrites the algorithm around IO": the definition of
+    S, P, O, m, l; the assumption of at least one allowed key per row; the blockwise
+    recurrence over blocks that partition the allowed keys and its exactness.
+  * "AI Infra ch. 5" (pre.everytik.com/books/ai-infra/05), section 5.3, Example 5-6
+    and Exercise 5-3 (the (m, l, u) update), and section 5.4 (two blocks holding 1
+    and 3 cannot be merged without their statistics).
+  * Closed forms and invariants of softmax attention (rows of P sum to 1, constant V,
+    uniform weights, shift invariance, key permutation), and brute force in 50-digit
+    arithmetic on tiny inputs.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+
+import synth
+
+NONE, CAUSAL, DENSE = synth.MODE_NONE, synth.MODE_CAUSAL, synth.MODE_DENSE
+EPS = np.finfo(np.float64).eps
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _vals(bits):
+    return synth.bf16_to_f32(bits).astype(np.float64)
+
+
+def _case(seed, N, d, dv, mode, p_mask=0.0, qk_mult=1.0, BH=1):
+    return synth.random_case(seed, BH, N, d, dv, mode, qk_mult, p_mask)
+
+
+def _head(c, h=0):
+    C = None if c["C"] is None else c["C"][h]
+    return c["Q"][h], c["K"][h], c["V"][h], C
+
+
+def _scores_numpy(Q, K, C, mode, scale):
+    """S recomputed with a numpy matmul (used only where a pin needs a single score)."""
+    S = scale * (_vals(Q) @ _vals(K).T)
+    N = S.shape[0]
+    if mode == CAUSAL:
+        S = S + np.where(np.arange(N)[None, :] > np.arange(N)[:, None], -np.inf, 0.0)
+    elif mode == DENSE:
+        S = S + C.astype(np.float64)
+    return S
+
+
+def _set_partitions(items):
+    """Every partition of the list `items` into non-empty blocks."""
+    if not items:
+        yield []
+        return
+    first, rest = items[0], items[1:]
+    for part in _set_partitions(rest):
+        for k in range(len(part)):
+            yield part[:k] + [[first] + part[k]] + part[k + 1:]
+        yield [[first]] + part
+
+
+def pin_p_rows_sum_to_one(orc):
+    """Rows of P are probability vectors: P >= 0 and sum_j P_ij = 1 within 4 N eps."""
+    for seed, N, mode in [(11, 1, NONE), (12, 7, CAUSAL), (13, 33, DENSE), (14, 50, NONE),
+                          (15, 40, CAUSAL)]:
+        c = _case(seed, N, 16, 8, mode, p_mask=0.3)
+        Q, K, V, C = _head(c)
+        S, P, O, L = orc.attention_head(Q, K, V, mode, C, c["scale"])
+        assert np.all(P >= 0.0)
+        assert np.all(np.abs(P.sum(axis=1) - 1.0) <= 4 * N * EPS), (seed, P.sum(axis=1))
+        # O is the P-weighted combination of the rows of V.
+        assert np.allclose(O, P @ _vals(V), rtol=0, atol=64 * N * EPS)
+
+
+def pin_constant_v(orc):
+    """If every v_j equals the same vector c, then O_i = c for any Q, K and C."""
+    for seed, N, mode, cval in [(21, 13, NONE, 1.5), (22, 29, CAUSAL, -0.375), (23, 17, DENSE, 3.0)]:
+        c = _case(seed, N, 32, 5, mode, p_mask=0.4)
+        Q, K, _, C = _head(c)
+        row = synth.bf16_bits(np.array([cval, -2.0 * cval, 0.5, 7.0, -1.25], dtype=np.float32))
+        V = np.tile(row, (N, 1))
+        _, _, O, _ = orc.attention_head(Q, K, V, mode, C, c["scale"])
+        expect = _vals(row)
+        assert np.allclose(O, expect[None, :], rtol=8 * N * EPS, atol=0), (seed, O[:2])
+
+
+def pin_single_allowed_key(orc):
+    """A row with exactly one allowed key j returns O_i = v_j exactly and LSE_i = S_ij."""
+    N, d, dv = 9, 16, 6
+    c = _case(31, N, d, dv, DENSE)
+    Q, K, V, C = _head(c)
+    C = C.copy()
+    rng = np.random.default_rng(31)
+    keep = rng.integers(0, N, size=N)
+    mask = np.full((N, N), -np.inf, dtype=np.float32)
+    mask[np.arange(N), keep] = C[np.arange(N), keep]
+    _, _, O, L = orc.attention_head(Q, K, V, DENSE, mask, c["scale"])
+    Vv = _vals(V)
+    assert np.array_equal(O, Vv[keep]), "O_i must equal v_j of the only allowed key"
+    S = _scores_numpy(Q, K, mask, DENSE, c["scale"])
+    assert np.allclose(L, S[np.arange(N), keep], rtol=0, atol=1e-12)
+    # Causal row 0 may only see key 0.
+    c2 = _case(32, 5, d, dv, CAUSAL)
+    Q2, K2, V2, _ = _head(c2)
+    _, _, O2, L2 = orc.attention_head(Q2, K2, V2, CAUSAL, None, c2["scale"])
+    assert np.array_equal(O2[0], _vals(V2)[0])
+    assert math.isclose(L2[0], c2["scale"] * float(_vals(Q2)[0] @ _vals(K2)[0]), rel_tol=0,
+                        abs_tol=1e-12)
+
+
+def pin_uniform_weights(orc):
+    """Q = 0 and C = 0 give uniform weights: O_i = mean_j v_j, LSE_i = ln N (causal: ln(i+1))."""
+    N, d, dv = 23, 8, 7
+    c = _case(41, N, d, dv, NONE)
+    _, K, V, _ = _head(c)
+    Q0 = np.zeros((N, d), dtype=np.uint16)
+    Vv = _vals(V)
+    _, _, O, L = orc.attention_head(Q0, K, V, NONE, None, c["scale"])
+    assert np.allclose(O, Vv.mean(axis=0)[None, :], rtol=0, atol=16 * N * EPS)
+    assert np.allclose(L, math.log(N), rtol=0, atol=4 * EPS)
+    _, _, Oc, Lc = orc.attention_head(Q0, K, V, CAUSAL, None, c["scale"])
+    for i in range(N):
+        assert np.allclose(Oc[i], Vv[: i + 1].mean(axis=0), rtol=0, atol=16 * N * EPS), i
+        assert math.isclose(Lc[i], math.log(i + 1), rel_tol=0, abs_tol=4 * EPS), i
+
+
+def pin_shift_invariance(orc):
+    """Adding kappa_i to row i of C leaves O_i unchanged and adds kappa_i to LSE_i."""
+    N, d, dv = 19, 16, 4
+    c = _case(51, N, d, dv, DENSE)
+    Q, K, V, _ = _head(c)
+    rng = np.random.default_rng(51)
+    # Multiples of 1/64 below 8 in magnitude and shifts in quarters stay exact in fp32.
+    C = (np.round(rng.standard_normal((N, N)) * 64.0) / 64.0).astype(np.float32)
+    C[rng.random((N, N)) < 0.25] = -np.inf
+    C[:, 0] = 0.5
+    kappa = (rng.integers(-12, 13, size=N) / 4.0).astype(np.float32)
+    C2 = (C + kappa[:, None]).astype(np.float32)
+    _, _, O1, L1 = orc.attention_head(Q, K, V, DENSE, C, c["scale"])
+    _, _, O2, L2 = orc.attention_head(Q, K, V, DENSE, C2, c["scale"])
+    assert np.allclose(O1, O2, rtol=0, atol=64 * EPS * np.abs(O1).max())
+    assert np.allclose(L2 - L1, kappa.astype(np.float64), rtol=0, atol=1e-13)
+
+
+def pin_blockwise_equals_full(orc):
+    """The recurrence over any partition of the allowed keys into blocks, in any block
+    order, gives the full-softmax O_i and m_T + ln l_T = LSE_i."""
+    rng = np.random.default_rng(61)
+    for N in range(1, 7):
+        for rep in range(2):
+            c = _case(600 + 10 * N + rep, N, 8, 3, DENSE, p_mask=0.0)
+            Q, K, V, C = _head(c)
+            C = C.copy()
+            forbidden = rng.random(N) < 0.3
+            forbidden[rng.integers(0, N)] = False
+            C[:, forbidden] = -np.inf
+            S, _, O, L = orc.attention_head(Q, K, V, DENSE, C, c["scale"])
+            Vv = _vals(V)
+            i = int(rng.integers(0, N))
+            allowed = [j for j in range(N) if not forbidden[j]]
+            for part in _set_partitions(allowed):
+                T = len(part)
+                blk = np.full(N, -1, dtype=np.int32)
+                for t, block in enumerate(part):
+                    blk[block] = t
+                orders = [list(range(T)), list(reversed(range(T)))]
+                orders.append(list(rng.permutation(T)))
+                for order in orders:
+                    Ob, m, l = orc.online_blocks(S[i], Vv, blk, T, order)
+                    assert np.allclose(Ob, O[i], rtol=0, atol=32 * N * EPS), (N, part, order)
+                    assert math.isclose(m + math.log(l), L[i], rel_tol=0, abs_tol=1e-14)
+                    # m_T is the running maximum, so it ends at the row maximum m_i.
+                    assert m == S[i].max(), (m, S[i].max())
+    # Random contiguous partitions (tiles) of longer rows, scores of large magnitude.
+    for N in (8, 17, 64):
+        c = _case(700 + N, N, 32, 4, NONE, qk_mult=4.0)
+        Q, K, V, C = _head(c)
+        S, _, O, L = orc.attention_head(Q, K, V, NONE, None, c["scale"])
+        Vv = _vals(V)
+        for rep in range(8):
+            cuts = sorted(set(rng.integers(1, N, size=int(rng.integers(0, min(N - 1, 8) + 1)))))
+            bounds = [0] + list(cuts) + [N]
+            blk = np.empty(N, dtype=np.int32)
+            for t in range(len(bounds) - 1):
+                blk[bounds[t]:bounds[t + 1]] = t
+            i = int(rng.integers(0, N))
+            Ob, m, l = orc.online_blocks(S[i], Vv, blk, len(bounds) - 1)
+            assert np.allclose(Ob, O[i], rtol=0, atol=64 * N * EPS * max(1.0, np.abs(O[i]).max()))
+            assert math.isclose(m + math.log(l), L[i], rel_tol=0, abs_tol=1e-12)
+            assert m == S[i].max()
+    # Tiles whose maxima differ by thousands (scores ~1e4): alpha must stay <= 1, so the
+    # recurrence cannot overflow whatever the order of the tiles.
+    c = _case(777, 48, 64, 4, NONE, qk_mult=32.0)
+    Q, K, V, _ = _head(c)
+    S, _, O, L = orc.attention_head(Q, K, V, NONE, None, c["scale"])
+    Vv = _vals(V)
+    blk = np.repeat(np.arange(6, dtype=np.int32), 8)
+    for i in range(48):
+        for order in (list(range(6)), list(reversed(range(6)))):
+            Ob, m, l = orc.online_blocks(S[i], Vv, blk, 6, order)
+            assert np.isfinite(Ob).all() and np.isfinite(l), (i, order)
+            assert np.allclose(Ob, O[i], rtol=0, atol=1e-12 * max(1.0, np.abs(O[i]).max()))
+
+
+def pin_exercise_5_3(orc):
+    """The page's single-step update with the element of Exercise 5-3 (score ln 4, value 5)."""
+    with open(os.path.join(GOLDEN, "exercise_5_3.json")) as f:
+        g = json.load(f)
+    prior, el, exp_ = g["prior"], g["element"], g["expected"]
+    m, l, u = orc.online_step(prior["m"], prior["l"], prior["u"], math.log(4.0), el["value"])
+    assert math.isclose(m, math.log(4.0), rel_tol=0, abs_tol=1e-15)
+    assert math.isclose(l, exp_["l_new"], rel_tol=1e-15)
+    assert np.allclose(u, exp_["u_new"], rtol=1e-15, atol=0)
+    assert np.allclose(u / l, exp_["output"], rtol=1e-15, atol=0)
+    # The same value from the blockwise recurrence with one element per block.
+    O, m2, l2 = orc.online_blocks(np.array([0.0, math.log(4.0)]), np.array([[1.0], [5.0]]),
+                                  np.array([0, 1]), 2)
+    assert np.allclose(O, exp_["output"], rtol=1e-15, atol=0)
+    assert math.isclose(l2, exp_["l_new"], rel_tol=1e-15)
+
+
+def pin_one_and_three(orc):
+    """Blocks holding 1 and 3: block-local outputs are 1 and 3 either way, and only the
+    kept (m, l, u) statistics recover 7/3 (weights 1:2) or 5/3 (weights 2:1)."""
+    with open(os.path.join(GOLDEN, "one_and_three.json")) as f:
+        g = json.load(f)
+    ln2 = math.log(2.0)
+    expected = {"7/3": 7.0 / 3.0, "5/3": 5.0 / 3.0}
+    for case in g["cases"]:
+        s = [ln2 if x == "ln 2" else float(x) for x in case["scores"]]
+        v = case["values"]
+        st1 = (s[0], 1.0, [v[0]])  # a block of one element: m = s, l = e^0 = 1, u = v
+        st2 = (s[1], 1.0, [v[1]])
+        assert [st1[2][0] / st1[1], st2[2][0] / st2[1]] == g["block_local_outputs"]
+        m, l, u = orc.online_merge(st1, st2)
+        assert math.isclose(u[0] / l, expected[case["expected"]], rel_tol=4 * EPS)
+        O, _, _ = orc.online_blocks(np.array(s), np.array([[v[0]], [v[1]]]), np.array([0, 1]), 2)
+        assert math.isclose(O[0], expected[case["expected"]], rel_tol=4 * EPS)
+
+
+def pin_merge_of_partial_states(orc):
+    """Partial states of two disjoint key sets of a row, merged with their (m, l, u)
+    statistics, give the full-row O_i, m_i and l_i (any split, unequal l's)."""
+    rng = np.random.default_rng(161)
+    c = _case(161, 30, 16, 5, NONE, qk_mult=2.0)
+    Q, K, V, _ = _head(c)
+    S, _, O, L = orc.attention_head(Q, K, V, NONE, None, c["scale"])
+    Vv = _vals(V)
+    for i in range(0, 30, 3):
+        side = rng.random(30) < rng.uniform(0.1, 0.9)
+        side[0], side[1] = True, False
+        states = []
+        for sel in (side, ~side):
+            blk = np.where(sel, 0, -1).astype(np.int32)
+            Ob, m, l = orc.online_blocks(S[i], Vv, blk, 1)
+            states.append((m, l, Ob * l))
+        m, l, u = orc.online_merge(states[0], states[1])
+        assert m == S[i].max()
+        assert math.isclose(m + math.log(l), L[i], rel_tol=0, abs_tol=1e-13)
+        assert np.allclose(u / l, O[i], rtol=0, atol=1e-13)
+
+
+def pin_bruteforce_tiny(orc):
+    """Tiny problems against 50-digit arithmetic (mpmath), relative error <= 1e-13."""
+    import mpmath
+
+    mpmath.mp.dps = 50
+    for seed, N, d, dv, mode in [(81, 1, 4, 3, NONE), (82, 3, 5, 2, CAUSAL), (83, 5, 3, 4, DENSE),
+                                 (84, 8, 6, 5, NONE), (85, 8, 4, 7, DENSE), (86, 6, 7, 3, CAUSAL)]:
+        c = _case(seed, N, d, dv, mode, p_mask=0.3, qk_mult=2.0)
+        Q, K, V, C = _head(c)
+        _, _, O, L = orc.attention_head(Q, K, V, mode, C, c["scale"])
+        Qv, Kv, Vv = _vals(Q), _vals(K), _vals(V)
+        sc = mpmath.mpf(c["scale"])
+        for i in range(N):
+            srow = []
+            for j in range(N):
+                if mode == CAUSAL and j > i:
+                    srow.append(None)
+                    continue
+                if mode == DENSE and np.isneginf(C[i, j]):
+                    srow.append(None)
+                    continue
+                acc = mpmath.mpf(0)
+                for k in range(d):
+                    acc += mpmath.mpf(float(Qv[i, k])) * mpmath.mpf(float(Kv[j, k]))
+                sij = sc * acc
+                if mode == DENSE:
+                    sij += mpmath.mpf(float(C[i, j]))
+                srow.append(sij)
+            if all(x is None for x in srow):
+                assert np.all(O[i] == 0.0) and np.isneginf(L[i])
+                continue
+            w = [mpmath.exp(x) if x is not None else mpmath.mpf(0) for x in srow]
+            tot = mpmath.fsum(w)
+            for col in range(dv):
+                ref = mpmath.fsum(w[j] * mpmath.mpf(float(Vv[j, col])) for j in range(N)) / tot
+                assert abs(O[i, col] - float(ref)) <= 1e-13 * max(1.0, abs(float(ref))), \
+                    (seed, i, col, O[i, col], float(ref))
+            assert abs(L[i] - float(mpmath.log(tot))) <= 1e-13 * max(1.0, abs(float(mpmath.log(tot))))
+
+
+def pin_two_keys_logistic(orc):
+    """N = 2 without a mask: P_i0 = 1 / (1 + e^{S_i1 - S_i0}) (the logistic function)."""
+    c = _case(91, 2, 16, 3, NONE, qk_mult=2.0)
+    Q, K, V, _ = _head(c)
+    S, P, O, _ = orc.attention_head(Q, K, V, NONE, None, c["scale"])
+    Vv = _vals(V)
+    for i in range(2):
+        p0 = 1.0 / (1.0 + math.exp(S[i, 1] - S[i, 0]))
+        assert math.isclose(P[i, 0], p0, rel_tol=4 * EPS)
+        assert np.allclose(O[i], p0 * Vv[0] + (1.0 - p0) * Vv[1], rtol=0, atol=8 * EPS * 4)
+
+
+def pin_large_scores(orc):
+    """Scores of magnitude ~1e4: no overflow; a row whose top score leads by more than 60
+    returns the top key's v exactly (every other weight is below e^-60)."""
+    c = _case(101, 24, 64, 8, NONE, qk_mult=32.0)
+    Q, K, V, _ = _head(c)
+    S, P, O, L = orc.attention_head(Q, K, V, NONE, None, c["scale"])
+    assert np.isfinite(O).all() and np.isfinite(L).all()
+    assert np.abs(S).max() > 1e3
+    Vv = _vals(V)
+    checked = 0
+    for i in range(24):
+        order = np.argsort(S[i])
+        if S[i, order[-1]] - S[i, order[-2]] > 60.0:
+            assert np.array_equal(O[i], Vv[order[-1]]), i
+            assert math.isclose(L[i], S[i, order[-1]], rel_tol=4 * EPS)
+            checked += 1
+    assert checked >= 3
+
+
+def pin_causal_is_triangular_bias(orc):
+    """The causal mode equals a dense C with -inf above the diagonal and 0 elsewhere."""
+    c = _case(111, 37, 16, 9, CAUSAL, BH=2)
+    N = 37
+    tri = np.where(np.arange(N)[None, :] > np.arange(N)[:, None], -np.inf, 0.0).astype(np.float32)
+    C = np.broadcast_to(tri, (2, N, N)).copy()
+    O1, L1, _ = orc.attention(c["Q"], c["K"], c["V"], CAUSAL, None, c["scale"])
+    O2, L2, _ = orc.attention(c["Q"], c["K"], c["V"], DENSE, C, c["scale"])
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+def pin_scale_wiring(orc):
+    """S = scale * Q K^T: doubling Q (exact in bf16) and halving the scale changes nothing;
+    and with K = Q = e_1 rows the score is exactly `scale`."""
+    c = _case(121, 11, 16, 4, NONE, BH=2)
+    Q2 = synth.bf16_bits(2.0 * synth.bf16_to_f32(c["Q"]))
+    O1, L1, _ = orc.attention(c["Q"], c["K"], c["V"], NONE, None, c["scale"])
+    O2, L2, _ = orc.attention(Q2, c["K"], c["V"], NONE, None, c["scale"] / 2.0)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+    # Two keys, one of them equal to the query direction: S_i0 = scale, S_i1 = 0.
+    e1 = np.zeros((2, 4), dtype=np.float32)
+    e1[:, 0] = 1.0
+    Qb = synth.bf16_bits(e1)
+    Kb = synth.bf16_bits(np.array([[1, 0, 0, 0], [0, 1, 0, 0]], dtype=np.float32))
+    Vb = synth.bf16_bits(np.array([[1.0], [0.0]], dtype=np.float32))
+    S, _, O, L = orc.attention_head(Qb, Kb, Vb, NONE, None, 0.75)
+    assert S[0, 0] == 0.75 and S[0, 1] == 0.0
+    assert math.isclose(O[0, 0], 1.0 / (1.0 + math.exp(-0.75)), rel_tol=4 * EPS)
+    assert math.isclose(L[0], math.log(math.exp(0.75) + 1.0), rel_tol=4 * EPS)
+
+
+def pin_key_permutation(orc):
+    """Permuting the keys (rows of K and V with the columns of C) leaves O and LSE unchanged."""
+    rng = np.random.default_rng(131)
+    for mode in (NONE, DENSE):
+        c = _case(131 + mode, 21, 16, 6, mode, p_mask=0.3)
+        Q, K, V, C = _head(c)
+        perm = rng.permutation(21)
+        C2 = None if C is None else C[:, perm]
+        _, _, O1, L1 = orc.attention_head(Q, K, V, mode, C, c["scale"])
+        _, _, O2, L2 = orc.attention_head(Q, K[perm], V[perm], mode, C2, c["scale"])
+        assert np.allclose(O1, O2, rtol=0, atol=1e-13)
+        assert np.allclose(L1, L2, rtol=0, atol=1e-13)
+
+
+def pin_row_subset_and_threads(orc):
+    """Evaluating a subset of rows, or with another thread count, gives identical bits."""
+    c = _case(141, 45, 32, 16, CAUSAL, BH=3)
+    O, L, _ = orc.attention(c["Q"], c["K"], c["V"], CAUSAL, None, c["scale"], nthreads=4)
+    O1, L1, used = orc.attention(c["Q"], c["K"], c["V"], CAUSAL, None, c["scale"], nthreads=1)
+    assert used == 1
+    assert np.array_equal(O, O1) and np.array_equal(L, L1)
+    rows = np.array([0, 44, 45, 89, 134, 70], dtype=np.int64)
+    Os, Ls, _ = orc.attention(c["Q"], c["K"], c["V"], CAUSAL, None, c["scale"], rows=rows)
+    assert np.array_equal(Os, O.reshape(-1, 16)[rows])
+    assert np.array_equal(Ls, L.reshape(-1)[rows])
+
+
+def pin_no_allowed_key(orc):
+    """Outside the pages' assumption (a row with no allowed key) the defined result is
+    O_i = 0 and LSE_i = -inf; the other rows are unaffected."""
+    c = _case(151, 6, 8, 3, DENSE)
+    Q, K, V, C = _head(c)
+    C = C.copy()
+    C[2, :] = -np.inf
+    _, _, O, L = orc.attention_head(Q, K, V, DENSE, C, c["scale"])
+    assert np.array_equal(O[2], np.zeros(3)) and np.isneginf(L[2])
+    assert np.isfinite(O).all() and np.isfinite(np.delete(L, 2)).all()
+
+
+ALL_PINS = [
+    pin_p_rows_sum_to_one,
+    pin_constant_v,
+    pin_single_allowed_key,
+    pin_uniform_weights,
+    pin_shift_invariance,
+    pin_blockwise_equals_full,
+    pin_exercise_5_3,
+    pin_one_and_three,
+    pin_merge_of_partial_states,
+    pin_bruteforce_tiny,
+    pin_two_keys_logistic,
+    pin_large_scores,
+    pin_causal_is_triangular_bias,
+    pin_scale_wiring,
+    pin_key_permutation,
+    pin_row_subset_and_threads,
+    pin_no_allowed_key,
+]
