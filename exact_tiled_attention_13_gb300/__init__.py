@@ -1,0 +1,72 @@
+"""Exact tiled attention forward pass for NVIDIA GB300 (sm_103a).
+
+O = softmax(Q K^T * scale + C) V with an additive bias or mask C, evaluated tile by
+tile with the online-softmax recurrence in a hand-written CUDA kernel (TMA, tcgen05
+tensor cores, tensor memory) behind the C ABI of include/attn.h. This module only
+checks tensor shapes and passes device pointers to that ABI; every step of the
+computation runs in the library's kernel.
+"""
+from __future__ import annotations
+
+from ._lib import (ATTN_BIAS_DENSE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_INVALID_ARG,
+                   ATTN_ERR_LAUNCH, ATTN_ERR_NO_DEVICE, ATTN_ERR_UNSUPPORTED,
+                   ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK,
+                   ATTN_OUT_BF16, ATTN_OUT_F32, AttnError, attn_device_status, attn_fwd_raw,
+                   attn_set_wait_timeout_ns, attn_version, library_path, load, strerror)
+
+__all__ = [
+    "attn_fwd", "attn_fwd_raw", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
+    "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
+    "ATTN_BIAS_DENSE", "ATTN_OUT_BF16", "ATTN_OUT_F32",
+]
+
+attn_strerror = strerror
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def attn_fwd(Q, K, V, mode, C, scale, O, LSE=None, stream=None):
+    """Launch O = softmax(Q K^T * scale + C) V (and LSE) through the C ABI.
+
+    Q, K: bf16 CUDA tensors [BH, N, d]; V: bf16 [BH, N, d_v]; C: fp32 [BH, N, N] for
+    mode ATTN_BIAS_DENSE, else None; O: bf16 or fp32 [BH, N, d_v]; LSE: fp32 [BH, N] or
+    None. All contiguous. `stream`: torch.cuda.Stream, a raw handle, or None for the
+    current stream. Raises AttnError with the library's code on failure.
+    """
+    import torch
+
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if Q.dtype != torch.bfloat16 or K.dtype != torch.bfloat16 or V.dtype != torch.bfloat16:
+        raise ValueError("Q, K and V must be bf16")
+    if Q.dim() != 3 or K.shape != Q.shape or V.dim() != 3 or V.shape[:2] != Q.shape[:2]:
+        raise ValueError("expected Q, K [BH, N, d] and V [BH, N, d_v]")
+    BH, N, d = Q.shape
+    dv = V.shape[2]
+    if tuple(O.shape) != (BH, N, dv) or O.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("O must be bf16 or fp32 [BH, N, d_v]")
+    out_dtype = ATTN_OUT_F32 if O.dtype == torch.float32 else ATTN_OUT_BF16
+    c_ptr = None
+    if C is not None:
+        if C.dtype != torch.float32 or tuple(C.shape) != (BH, N, N) or not C.is_contiguous():
+            raise ValueError("C must be a contiguous fp32 [BH, N, N] tensor")
+        c_ptr = C.data_ptr()
+    lse_ptr = None
+    if LSE is not None:
+        if LSE.dtype != torch.float32 or tuple(LSE.shape) != (BH, N) or not LSE.is_contiguous():
+            raise ValueError("LSE must be a contiguous fp32 [BH, N] tensor")
+        lse_ptr = LSE.data_ptr()
+    code = attn_fwd_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), mode, c_ptr, BH, N, d, dv, scale,
+                        O.data_ptr(), out_dtype, lse_ptr, _stream_handle(stream))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd")
+    return O, LSE

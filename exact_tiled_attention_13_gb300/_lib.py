@@ -1,0 +1,94 @@
+"""ctypes binding of libattn's C ABI (include/attn.h). Argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+ATTN_MASK_NONE = 0
+ATTN_MASK_CAUSAL = 1
+ATTN_BIAS_DENSE = 2
+ATTN_OUT_BF16 = 0
+ATTN_OUT_F32 = 1
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = -1
+ATTN_ERR_UNSUPPORTED = -2
+ATTN_ERR_NO_DEVICE = -3
+ATTN_ERR_UNSUPPORTED_DEVICE = -4
+ATTN_ERR_LAUNCH = -5
+ATTN_ERR_DEVICE_TIMEOUT = -6
+ATTN_ERR_CUDA = -7
+
+# Every symbol include/attn.h declares, with its ctypes signature.
+_P = ctypes.c_void_p
+SIGNATURES = {
+    "attn_fwd": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, ctypes.c_int, ctypes.c_float, _P, ctypes.c_int, _P,
+                                _P]),
+    "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "attn_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint)]),
+    "attn_set_wait_timeout_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
+    "attn_version": (ctypes.c_int, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+_path = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {strerror(code)} (code {code})")
+
+
+def load():
+    """Load libattn, building it in-tree first if the current sources have no library.
+
+    There is no fallback: if the library cannot be built or loaded this raises.
+    """
+    global _lib, _path
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = os.environ.get("ATTN_LIBRARY") or _build.build()
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib, _path = lib, path
+        return lib
+
+
+def library_path() -> str:
+    load()
+    return _path
+
+
+def strerror(code: int) -> str:
+    return load().attn_strerror(int(code)).decode()
+
+
+def attn_fwd_raw(Q, K, V, mode, C, BH, N, d, d_v, scale, O, out_dtype, LSE, stream) -> int:
+    """The C entry point with plain integers as pointers; returns its code unchanged."""
+    return load().attn_fwd(Q, K, V, int(mode), C, int(BH), int(N), int(d), int(d_v), float(scale), O,
+                           int(out_dtype), LSE, stream)
+
+
+def attn_device_status(stream=None):
+    """(code, raw watchdog word) after synchronising `stream` (a raw cudaStream_t or None)."""
+    word = ctypes.c_uint(0)
+    code = load().attn_device_status(stream, ctypes.byref(word))
+    return code, word.value
+
+
+def attn_set_wait_timeout_ns(ns: int) -> int:
+    return load().attn_set_wait_timeout_ns(int(ns))
+
+
+def attn_version() -> int:
+    return load().attn_version()

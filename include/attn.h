@@ -1,0 +1,125 @@
+/*
+ * attn.h -- C ABI of the exact tiled attention forward pass for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is exact scaled dot-product attention for B*H independent heads,
+ * as defined in "Compilers and kernels" (aaai.latere.ai/zh/infrastructure/
+ * compilers-kernels), section "FlashAttention rewrites the algorithm around IO",
+ * first display and its symbol list:
+ *
+ *     S = Q K^T * scale + C,  m_i = max_j S_ij,  l_i = sum_j exp(S_ij - m_i),
+ *     P_ij = exp(S_ij - m_i) / l_i,  O = P V,
+ *
+ * with C an additive bias or mask (-inf forbids a key) and at least one allowed key
+ * per query row. The library evaluates it tile by tile with the online recurrence of
+ * the same section (b_t, m_t = max(m_{t-1}, b_t), alpha_t = exp(m_{t-1} - m_t), l_t,
+ * o_t, O_i = o_T / l_T), so S and P never reach device memory. "Exact" means the same
+ * function, not the same bits: tiling changes the floating-point evaluation order
+ * (same section, the paragraph after the recurrence).
+ *
+ * Numeric contract of this implementation: Q K^T and P V run on the tensor cores with
+ * bf16 operands and fp32 accumulation; scores, the running max and sum, and O are fp32;
+ * P is rounded to bf16 before it multiplies V, while l_i sums the unrounded fp32 p.
+ * LSE_i = m_i + ln l_i (natural log, in the units of S, bias included).
+ *
+ * All entry points are plain C, take device pointers and sizes, and never allocate
+ * device memory. They are thread-safe: calls from several host threads or on several
+ * streams may overlap.
+ */
+#ifndef EXACT_TILED_ATTENTION_13_ATTN_H
+#define EXACT_TILED_ATTENTION_13_ATTN_H
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Mask / bias modes (argument `mode`). */
+#define ATTN_MASK_NONE 0  /* C = 0 */
+#define ATTN_MASK_CAUSAL 1 /* C_ij = -inf for key j > query i, else 0 (square, shared indexing) */
+#define ATTN_BIAS_DENSE 2 /* C read from a dense fp32 [BH][N][N] array */
+
+/* Output element types (argument `out_dtype`). */
+#define ATTN_OUT_BF16 0
+#define ATTN_OUT_F32 1
+
+/* Return codes. Zero is success; every error is negative. */
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID_ARG (-1)        /* null/misaligned/overlapping pointer, bad size, mode or scale */
+#define ATTN_ERR_UNSUPPORTED (-2)        /* a head width d or d_v this build has no kernel for */
+#define ATTN_ERR_NO_DEVICE (-3)          /* no CUDA device, or no CUDA driver */
+#define ATTN_ERR_UNSUPPORTED_DEVICE (-4) /* the current device is not compute capability 10.3 */
+#define ATTN_ERR_LAUNCH (-5)             /* the kernel launch was rejected by the CUDA runtime */
+#define ATTN_ERR_DEVICE_TIMEOUT (-6)     /* a kernel gave up on a pipeline wait (see attn_device_status) */
+#define ATTN_ERR_CUDA (-7)               /* another CUDA runtime or driver call failed */
+
+/*
+ * attn_fwd -- O = softmax(Q K^T * scale + C) V and LSE for BH heads, on `stream`.
+ *
+ * Arguments (all pointers are device pointers, or managed memory):
+ *   Q     bf16, contiguous row-major [BH][N][d]      queries
+ *   K     bf16, contiguous row-major [BH][N][d]      keys
+ *   V     bf16, contiguous row-major [BH][N][d_v]    values
+ *   mode  ATTN_MASK_NONE, ATTN_MASK_CAUSAL or ATTN_BIAS_DENSE
+ *   C     fp32, contiguous row-major [BH][N][N] when mode == ATTN_BIAS_DENSE, else NULL.
+ *         Entries are finite or -inf; C is added after the scaling and is not scaled.
+ *   BH    number of heads (batch times heads), >= 1
+ *   N     sequence length (queries = keys), >= 0; N == 0 is a successful no-op
+ *   d     query/key width, 64 or 128
+ *   d_v   value width, 64 or 128
+ *   scale score scale, finite and > 0 (the pages use 1/sqrt(d))
+ *   O     [BH][N][d_v] output, bf16 (out_dtype ATTN_OUT_BF16) or fp32 (ATTN_OUT_F32)
+ *   LSE   fp32 [BH][N] output, ln sum_j exp(S_ij); may be NULL to skip it
+ *   stream cudaStream_t to launch on; NULL means the legacy default stream
+ *
+ * Alignment: Q, K, V, C and O must be 16-byte aligned; LSE 4-byte aligned.
+ * Aliasing: O and LSE must not overlap each other or any input. Inputs are not
+ * modified.
+ * Ownership: the caller owns every buffer and must keep it alive until the work on
+ * `stream` completes. The library keeps no pointer after the call returns.
+ * Asynchrony: the call validates its arguments, launches one kernel and returns; the
+ * results are ready when `stream` reaches that point.
+ * Determinism: the same inputs give bit-identical outputs (no atomics, fixed order).
+ * Precondition (the pages' assumption): every query row has at least one allowed
+ * key. A row with none gets O_i = 0 and LSE_i = -inf.
+ *
+ * Returns ATTN_OK or one of the negative codes above. Argument errors are reported
+ * before anything is launched. A wait that times out inside the kernel is reported
+ * by attn_device_status, not here.
+ */
+ATTN_API int attn_fwd(const void *Q, const void *K, const void *V, int mode, const float *C, int BH, int N,
+             int d, int d_v, float scale, void *O, int out_dtype, float *LSE, void *stream);
+
+/* Static English text for a return code (never NULL). */
+ATTN_API const char *attn_strerror(int code);
+
+/*
+ * attn_device_status -- synchronizes `stream` (NULL: the legacy default stream),
+ * then reads and clears the current device's watchdog word. Every pipeline wait in
+ * the kernels is bounded; a wait that runs out records where it stopped in that
+ * word and the kernel returns without hanging the device.
+ * Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA / ATTN_ERR_NO_DEVICE
+ * when the synchronization or the read itself fails.
+ * If `detail` is not NULL it receives the raw watchdog word (0 when clear).
+ */
+ATTN_API int attn_device_status(void *stream, unsigned int *detail);
+
+/*
+ * attn_set_wait_timeout_ns -- the bound on each pipeline wait inside the kernels,
+ * in nanoseconds, for launches that follow (process-wide). 0 restores the default
+ * of 2 seconds. Returns the previous value.
+ */
+ATTN_API unsigned long long attn_set_wait_timeout_ns(unsigned long long ns);
+
+/* ABI version of this header (major * 100 + minor). */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_TILED_ATTENTION_13_ATTN_H */

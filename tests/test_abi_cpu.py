@@ -1,0 +1,115 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports every symbol
+include/attn.h declares, and rejects bad arguments before touching a device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_tiled_attention_13_gb300 as eta
+from exact_tiled_attention_13_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+def _header_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^ATTN_API\s+[\w\s\*]*?\b(attn_\w+)\s*\(", text, re.M)))
+
+
+def _header_defines():
+    text = open(HEADER).read()
+    return {k: int(v) for k, v in re.findall(r"#define\s+(ATTN_\w+)\s+\(?(-?\d+)\)?", text)}
+
+
+def _gpu_present():
+    try:
+        import torch
+
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def test_every_declared_symbol_is_exported():
+    lib = eta.load()
+    names = _header_functions()
+    assert names == sorted(_lib.SIGNATURES), names
+    for name in names:
+        assert hasattr(lib, name)
+    out = subprocess.run(["nm", "-D", "--defined-only", eta.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(attn_\w+)$", out, re.M))
+    assert exported == set(names)
+
+
+def test_library_is_in_tree_and_for_sm103a():
+    path = eta.library_path()
+    assert path.startswith(os.path.join(ROOT, "exact_tiled_attention_13_gb300", "_build"))
+    from exact_tiled_attention_13_gb300 import _build
+
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_header_constants_match_binding():
+    defs = _header_defines()
+    for name, value in defs.items():
+        assert getattr(_lib, name) == value, name
+
+
+def test_strerror_and_version():
+    for code in range(-7, 1):
+        assert eta.attn_strerror(code)
+    assert "unknown" in eta.attn_strerror(-99)
+    assert eta.attn_version() == 100
+
+
+def test_timeout_setting_roundtrip():
+    prev = eta.attn_set_wait_timeout_ns(12345)
+    assert eta.attn_set_wait_timeout_ns(0) == 12345
+    assert eta.attn_set_wait_timeout_ns(prev) == 2_000_000_000
+
+
+# Fake, 16-byte aligned "device" addresses: validation must reject bad calls before it
+# ever dereferences or registers them.
+QP, KP, VP, OP, LP, CP = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000
+GOOD = dict(Q=QP, K=KP, V=VP, mode=0, C=None, BH=2, N=64, d=64, d_v=64, scale=0.125, O=OP,
+            out_dtype=1, LSE=LP, stream=None)
+
+
+def call(**over):
+    a = dict(GOOD)
+    a.update(over)
+    return eta.attn_fwd_raw(a["Q"], a["K"], a["V"], a["mode"], a["C"], a["BH"], a["N"], a["d"],
+                            a["d_v"], a["scale"], a["O"], a["out_dtype"], a["LSE"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(Q=None), dict(K=None), dict(V=None), dict(O=None),
+    dict(Q=QP + 8), dict(V=VP + 2), dict(O=OP + 4), dict(LSE=LP + 2),
+    dict(mode=3), dict(mode=-1), dict(out_dtype=2),
+    dict(BH=0), dict(N=-1),
+    dict(scale=0.0), dict(scale=-0.5), dict(scale=float("nan")), dict(scale=float("inf")),
+    dict(mode=2, C=None), dict(mode=0, C=CP), dict(mode=1, C=CP), dict(mode=2, C=CP + 8),
+    dict(O=QP), dict(O=KP + 64), dict(LSE=VP), dict(LSE=OP + 128),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_invalid_arguments(over):
+    assert call(**over) == eta.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d,dv", [(32, 64), (96, 64), (64, 256), (256, 128)])
+def test_unsupported_widths(d, dv):
+    assert call(d=d, d_v=dv) == _lib.ATTN_ERR_UNSUPPORTED
+
+
+def test_zero_length_is_noop():
+    assert call(N=0) == eta.ATTN_OK
+
+
+@pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
+def test_valid_call_without_gpu_reports_no_device():
+    assert call() == eta.ATTN_ERR_NO_DEVICE
+    code, word = eta.attn_device_status(None)
+    assert code == eta.ATTN_ERR_NO_DEVICE and word == 0
