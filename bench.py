@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the exact attention forward pass; prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 3] [--impl ours|reference]
+
+A step is one forward pass (one kernel launch) over the whole workload: by default
+batch 2 x 32 heads, N = 8192, d = d_v = 128, causal, bf16 output plus fp32 LSE.
+Inputs are seeded synthetic tensors already resident in device memory; they are
+larger than L2 (514 MiB vs 129 MB), so no flush runs between steps.
+
+value     : TFLOP/s over the K timed steps (FLOPs 2 BH N^2 (d + d_v), halved for causal),
+            summed over ranks, timed with CUDA events between barriers, max over ranks
+roofline  : the kernel's achieved TFLOP/s (or GB/s when bandwidth-bound) over the
+            measured peak; traffic from the committed ncu summary when the kernel
+            source still matches it
+e2e       : the same metric through the public call with pinned host inputs copied in
+            and O, LSE copied back every step
+cpu_baseline: the fp64 CPU oracle timed on a bounded row sample on this host's cores
+--impl reference: the same line for the oracle alone (the reference arm)
+
+Under torchrun (WORLD_SIZE > 1) every rank runs an independent replica of the
+workload on its own GPU (the heads need no exchange); scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from exact_tiled_attention_13_gb300 import accounting  # noqa: E402
+
+HEADLINE_WORKLOAD = 3
+METRIC = "attention fwd TFLOP/s and % of GB300 BF16 tensor roofline (N=8192,d=128 causal)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1000 * 1000
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "ptx.cuh"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description="exact attention forward benchmark")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=HEADLINE_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-rows", type=int, default=0,
+                    help="rows in the CPU-baseline sample (0: sized to ~15 s of oracle work)")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- ranks
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_max(dist, value: float, device=None) -> float:
+    """Max of a float over all ranks (identity on one rank)."""
+    if dist is None:
+        return value
+    import torch
+
+    dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(dist, value: float, device=None) -> float:
+    if dist is None:
+        return value
+    import torch
+
+    dev = device if (device is not None and dist.get_backend() == "nccl") else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock, power and throttle reasons."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu_index)], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[4], parts[6:10]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:2]
+            window = "nearest samples to a short timed region"
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4]) if v == "Active"})
+        return {"sm_mhz": float(np.median([r[1] for r in inside])),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------- roofline inputs
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, ValueError, KeyError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_tiled_attention_13_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_id: int):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(PROFILE_DIR, f"attn_fwd_{synth.WORKLOADS[workload_id].name}_traffic.txt")
+    try:
+        with open(path) as f:
+            kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
+        if kv.get("kernel_source_sha", "").strip() != kernel_source_sha():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def workload_figures(w):
+    causal = w.mode == synth.MODE_CAUSAL
+    F = accounting.flops(w.BH, w.N, w.d, w.dv, causal)
+    B = accounting.required_bytes(w.BH, w.N, w.d, w.dv, 4 if w.out_dtype == "f32" else 2, lse=True,
+                                  dense_bias=w.mode == synth.MODE_DENSE)
+    return F, B
+
+
+def config_dict(w, world):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "d_v": w.dv,
+            "mask": synth.MODE_NAMES[w.mode], "out_dtype": w.out_dtype, "lse": "fp32",
+            "qk_scale_mult": w.qk_mult, "key_pad_p": w.p_mask,
+            "parallelism": f"replicas x{world} (heads independent, no collective)",
+            "l2": "inputs larger than L2 (no flush)" if workload_figures(w)[1] > L2_BYTES
+            else "L2 flushed between steps"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_rows(w, nrows: int) -> np.ndarray:
+    total = w.BH * w.N
+    nrows = max(1, min(nrows, total))
+    return np.unique(np.linspace(0, total - 1, nrows).astype(np.int64))
+
+
+def time_oracle(w, inputs, rows):
+    import oracle
+
+    t0 = time.perf_counter()
+    _, _, threads = oracle.attention(inputs["Q"], inputs["K"], inputs["V"], w.mode, inputs["C"],
+                                     w.scale, rows=rows)
+    return time.perf_counter() - t0, threads
+
+
+def cpu_rows_for_seconds(w, inputs, seconds: float) -> int:
+    """Rows the oracle finishes in about `seconds` on this host (calibrated on a small sample)."""
+    probe = oracle_rows(w, 64)
+    dt, _ = time_oracle(w, inputs, probe)
+    rate = len(probe) / max(dt, 1e-6)
+    return int(max(16, min(w.BH * w.N, rate * seconds)))
+
+
+def cpu_baseline(w, inputs, nrows):
+    F, _ = workload_figures(w)
+    rows = oracle_rows(w, nrows)
+    dt, threads = time_oracle(w, inputs, rows)
+    flops = F * len(rows) / (w.BH * w.N)  # the workload's average algorithmic FLOPs per row
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} query rows evenly strided over all {w.BH} heads x {w.N} rows "
+                      f"of the workload, fp64 C oracle with each row of S and P materialised; "
+                      f"FLOPs counted as the workload's per-row average; {dt:.1f} s wall"}
+
+
+# ----------------------------------------------------------------------------- arms
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = synth.WORKLOADS[args.workload]
+    inputs = synth.make_inputs(w, args.workload)
+    F, _ = workload_figures(w)
+    total_steps = args.steps + args.warmup
+    rows_per_step = max(8, cpu_rows_for_seconds(w, inputs, 90.0) // max(1, total_steps))
+    rows = oracle_rows(w, rows_per_step)
+    for _ in range(args.warmup):
+        time_oracle(w, inputs, rows)
+    t0 = time.perf_counter()
+    threads = 1
+    for _ in range(args.steps):
+        _, threads = time_oracle(w, inputs, rows)
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = F * len(rows) / (w.BH * w.N)
+    value = flops / dt / 1e12
+    sample = (f"{len(rows)} query rows per step, evenly strided over the workload's {w.BH} heads; "
+              f"fp64 C oracle materialising each row of S and P; FLOPs counted as the workload's "
+              f"per-row average")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, 1),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import exact_tiled_attention_13_gb300 as eta
+    from exact_tiled_attention_13_gb300.workload import DeviceWorkload
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    eta.load()
+    w = synth.WORKLOADS[args.workload]
+    F, B = workload_figures(w)
+    wl = DeviceWorkload(args.workload, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(max(3, args.warmup)):
+        wl.launch(stream)
+    torch.cuda.synchronize(device)
+    code, word = eta.attn_device_status(None)
+    if code != eta.ATTN_OK:
+        raise SystemExit(f"watchdog tripped during warm-up: {word:#x}")
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    region_start = torch.cuda.Event(enable_timing=True)
+    region_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    region_start.record(stream)
+    for i in range(K):
+        starts[i].record(stream)
+        wl.launch(stream)
+        ends[i].record(stream)
+    region_end.record(stream)
+    torch.cuda.synchronize(device)
+    t_wall1 = time.time()
+    barrier(dist, device)
+    clock_info = clocks.stop(t_wall0, t_wall1)
+    code, word = eta.attn_device_status(None)
+    if code != eta.ATTN_OK:
+        raise SystemExit(f"watchdog tripped in the timed region: {word:#x}")
+
+    region_ms = region_start.elapsed_time(region_end)
+    kernel_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
+    step_ms = reduce_max(dist, region_ms / K, device)
+    value = world * F / (step_ms * 1e-3) / 1e12
+
+    # End to end through the public call: pinned host inputs in, host outputs out.
+    E = max(3, args.e2e_steps)
+    for _ in range(2):
+        wl.end_to_end(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        wl.end_to_end(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = reduce_max(dist, e0.elapsed_time(e1) / E, device)
+    barrier(dist, device)
+
+    peaks, peak_src = measured_peaks()
+    bound = "tensor" if F / (peaks["bf16_tflops"] * 1e12) >= B / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    traffic = recorded_traffic(args.workload)
+    if bound == "tensor":
+        achieved = F / (kernel_ms * 1e-3) / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+        peak_note = f"dense bf16 tensor peak, {peak_src} (burst: kernel timed alone)"
+    else:
+        achieved = B / (kernel_ms * 1e-3) / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+        peak_note = f"HBM copy bandwidth, {peak_src}"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
+                "kernel_ms": kernel_ms, "algorithmic_flops": F, "algorithmic_bytes": B,
+                "roofline_time_ms": accounting.roofline_time_s(F, B, peaks["bf16_tflops"] * 1e12,
+                                                               peaks["hbm_gbs"] * 1e9) * 1e3}
+
+    line = None
+    if rank == 0:
+        nrows = args.cpu_rows or cpu_rows_for_seconds(w, wl.host, 15.0)
+        cpu = cpu_baseline(w, wl.host, nrows)
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+                "warmup": max(3, args.warmup), "ms_per_step": step_ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic (seeded SplitMix64/Box-Muller N(0,1) rounded to bf16)",
+                "config": config_dict(w, world), "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": world * F / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                        "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes(),
+                        "ms_per_step": e2e_ms, "steps": E},
+                "gpu_launches": K, "clocks": clock_info,
+                "library": os.path.relpath(eta.library_path(), ROOT)}
+    barrier(dist, device)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("--steps must be >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

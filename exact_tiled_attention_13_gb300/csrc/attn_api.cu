@@ -173,12 +173,13 @@ extern "C" int attn_fwd(const void *Q, const void *K, const void *V, int mode, c
   if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
   if (BH < 1 || N < 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if ((d != 64 && d != 128) || (d_v != 64 && d_v != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (N == 0) return ATTN_OK;  // empty buffers may be null
   if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
   if ((mode == ATTN_BIAS_DENSE) != (C != nullptr)) return ATTN_ERR_INVALID_ARG;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
       (C && !aligned(C, 16)) || (LSE && !aligned(LSE, 4)))
     return ATTN_ERR_INVALID_ARG;
-  if ((d != 64 && d != 128) || (d_v != 64 && d_v != 128)) return ATTN_ERR_UNSUPPORTED;
 
   const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(N);
   const size_t o_bytes = rows * d_v * (out_dtype == ATTN_OUT_F32 ? 4 : 2);
@@ -192,7 +193,6 @@ extern "C" int attn_fwd(const void *Q, const void *K, const void *V, int mode, c
       return ATTN_ERR_INVALID_ARG;
   }
   if (ranges_overlap(O, o_bytes, LSE, lse_bytes)) return ATTN_ERR_INVALID_ARG;
-  if (N == 0) return ATTN_OK;
 
   // ---- device
   int dev = -1;

@@ -1,0 +1,103 @@
+"""Put one of the synthetic attention workloads on the GPU and launch the forward pass.
+
+    python -m exact_tiled_attention_13_gb300.workload --workload 3 --iters 3
+
+generates the seeded inputs of the workload, copies them to cuda:0, launches
+attn_fwd `--iters` times on the current stream and synchronises. It is the command
+the profiler summaries under profiles/ were taken with.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+class DeviceWorkload:
+    """Seeded host inputs (pinned) and device buffers of one synthetic workload."""
+
+    def __init__(self, workload_id: int, device="cuda"):
+        import torch
+
+        import synth
+
+        self.id = workload_id
+        self.w = synth.WORKLOADS[workload_id]
+        self.host = synth.make_inputs(self.w, workload_id)
+        w = self.w
+
+        def pinned(arr, dtype):
+            t = torch.from_numpy(np.ascontiguousarray(arr))
+            if dtype is not None:
+                t = t.view(dtype)
+            return t.pin_memory()
+
+        self.Q_h = pinned(self.host["Q"].view(np.int16), torch.bfloat16)
+        self.K_h = pinned(self.host["K"].view(np.int16), torch.bfloat16)
+        self.V_h = pinned(self.host["V"].view(np.int16), torch.bfloat16)
+        self.C_h = None if self.host["C"] is None else pinned(self.host["C"], None)
+        self.Q = self.Q_h.to(device)
+        self.K = self.K_h.to(device)
+        self.V = self.V_h.to(device)
+        self.C = None if self.C_h is None else self.C_h.to(device)
+        odt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
+        self.O = torch.empty(w.BH, w.N, w.dv, dtype=odt, device=device)
+        self.LSE = torch.empty(w.BH, w.N, dtype=torch.float32, device=device)
+        self.O_h = torch.empty(self.O.shape, dtype=odt).pin_memory()
+        self.LSE_h = torch.empty(self.LSE.shape, dtype=torch.float32).pin_memory()
+
+    def launch(self, stream=None):
+        import exact_tiled_attention_13_gb300 as eta
+
+        eta.attn_fwd(self.Q, self.K, self.V, self.w.mode, self.C, self.w.scale, self.O, self.LSE,
+                     stream=stream)
+
+    def h2d_bytes(self) -> int:
+        n = sum(t.numel() * t.element_size() for t in (self.Q_h, self.K_h, self.V_h))
+        return n + (0 if self.C_h is None else self.C_h.numel() * self.C_h.element_size())
+
+    def d2h_bytes(self) -> int:
+        return self.O.numel() * self.O.element_size() + self.LSE.numel() * 4
+
+    def end_to_end(self, stream):
+        """One call the way a host-side user makes it: pinned host inputs in, host outputs out."""
+        import exact_tiled_attention_13_gb300 as eta
+
+        self.Q.copy_(self.Q_h, non_blocking=True)
+        self.K.copy_(self.K_h, non_blocking=True)
+        self.V.copy_(self.V_h, non_blocking=True)
+        if self.C is not None:
+            self.C.copy_(self.C_h, non_blocking=True)
+        eta.attn_fwd(self.Q, self.K, self.V, self.w.mode, self.C, self.w.scale, self.O, self.LSE,
+                     stream=stream)
+        self.O_h.copy_(self.O, non_blocking=True)
+        self.LSE_h.copy_(self.LSE, non_blocking=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args(argv)
+    import torch
+
+    wl = DeviceWorkload(args.workload)
+    for _ in range(args.iters):
+        wl.launch()
+    torch.cuda.synchronize()
+    import exact_tiled_attention_13_gb300 as eta
+
+    code, word = eta.attn_device_status(None)
+    if code != eta.ATTN_OK:
+        raise SystemExit(f"watchdog tripped: {word:#x}")
+    print(f"workload {args.workload} ({wl.w.name}): {args.iters} launches done")
+
+
+if __name__ == "__main__":
+    main()

@@ -68,7 +68,8 @@ extern "C" {
  *   C     fp32, contiguous row-major [BH][N][N] when mode == ATTN_BIAS_DENSE, else NULL.
  *         Entries are finite or -inf; C is added after the scaling and is not scaled.
  *   BH    number of heads (batch times heads), >= 1
- *   N     sequence length (queries = keys), >= 0; N == 0 is a successful no-op
+ *   N     sequence length (queries = keys), >= 0; N == 0 is a successful no-op in which
+ *         the pointers are not inspected (empty buffers may be NULL)
  *   d     query/key width, 64 or 128
  *   d_v   value width, 64 or 128
  *   scale score scale, finite and > 0 (the pages use 1/sqrt(d))

@@ -17,8 +17,10 @@ N(0,1) bias with a random key-padding mask (-inf with probability p per key).
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 
 import numpy as np
 
@@ -31,7 +33,7 @@ MODE_NAMES = {MODE_NONE: "none", MODE_CAUSAL: "causal", MODE_DENSE: "dense_bias"
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
-_CHUNK = 1 << 22
+_CHUNK = 1 << 21
 
 
 def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
@@ -50,22 +52,39 @@ def uniform01(seed: int, start: int, count: int) -> np.ndarray:
     return (x.astype(np.float64) + 1.0) * (2.0 ** -53)
 
 
+def _normal_chunk(seed: int, out: np.ndarray, count: int, p0: int, pn: int) -> None:
+    u = uniform01(seed, 2 * p0, 2 * pn)
+    r = np.sqrt(-2.0 * np.log(u[0::2]))
+    th = (2.0 * math.pi) * u[1::2]
+    z = np.empty(2 * pn, dtype=np.float64)
+    z[0::2] = r * np.cos(th)
+    z[1::2] = r * np.sin(th)
+    lo = 2 * p0
+    hi = min(count, lo + 2 * pn)
+    out[lo:hi] = z[: hi - lo].astype(np.float32)
+
+
 def normal_f32(seed: int, count: int) -> np.ndarray:
-    """`count` standard normal deviates (Box-Muller on consecutive uniform pairs), as fp32."""
+    """`count` standard normal deviates (Box-Muller on consecutive uniform pairs), as fp32.
+
+    Element k depends only on (seed, k): chunks are generated independently (in
+    parallel threads for large counts) and the result does not depend on chunking.
+    """
     out = np.empty(count, dtype=np.float32)
     pairs = (count + 1) // 2
-    for p0 in range(0, pairs, _CHUNK):
-        pn = min(_CHUNK, pairs - p0)
-        u = uniform01(seed, 2 * p0, 2 * pn)
-        r = np.sqrt(-2.0 * np.log(u[0::2]))
-        th = (2.0 * math.pi) * u[1::2]
-        z = np.empty(2 * pn, dtype=np.float64)
-        z[0::2] = r * np.cos(th)
-        z[1::2] = r * np.sin(th)
-        lo = 2 * p0
-        hi = min(count, lo + 2 * pn)
-        out[lo:hi] = z[: hi - lo].astype(np.float32)
+    starts = list(range(0, pairs, _CHUNK))
+    jobs = [(p0, min(_CHUNK, pairs - p0)) for p0 in starts]
+    if len(jobs) <= 1:
+        for p0, pn in jobs:
+            _normal_chunk(seed, out, count, p0, pn)
+        return out
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(len(jobs), _threads())) as ex:
+        list(ex.map(lambda j: _normal_chunk(seed, out, count, j[0], j[1]), jobs))
     return out
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:

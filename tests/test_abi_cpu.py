@@ -106,6 +106,8 @@ def test_unsupported_widths(d, dv):
 
 def test_zero_length_is_noop():
     assert call(N=0) == eta.ATTN_OK
+    assert call(N=0, Q=None, K=None, V=None, O=None, LSE=None) == eta.ATTN_OK
+    assert call(N=0, mode=7) == eta.ATTN_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
