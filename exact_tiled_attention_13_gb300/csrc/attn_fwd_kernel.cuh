@@ -10,18 +10,22 @@
 //
 // One CTA owns NQ query tiles of 128 rows of one head (NQ = 2 without a dense bias,
 // so one tile's softmax overlaps the other tile's matrix products; NQ = 1 with a
-// dense bias, whose time is the bias bytes). Warp roles:
+// dense bias, whose time is the bias bytes). Warp roles (16 or 12 warps):
 //   softmax warpgroup q (warps 4q..4q+3): thread = query row = tensor-memory lane.
-//     Reads its row of S from tensor memory, masks, takes the tile max, the new
-//     running max and alpha, writes P as bf16 back over S, rescales its row of o by
-//     alpha when some alpha in the warp differs from 1, and at the end writes O and LSE.
-//   MMA warp: issues S_q = Q_q K_t^T (A and B from shared memory) and o_q += P_q V_t
-//     (A = P from tensor memory, B = V from shared memory) with tcgen05.mma; fp32
-//     accumulators stay in tensor memory.
-//   load warp: TMA copies of Q once and K_t, V_t into rings of shared-memory slots
-//     guarded by full/empty mbarrier pairs (AI Infra ch. 5, Fig. 5-5: producer
-//     copies, consumer computes, one full and one empty barrier per slot).
-//   bias load warp (dense bias only): TMA copies of 128 x 32 fp32 bias chunks.
+//     Reads its row of S from tensor memory, masks, takes the tile max b_t, the new
+//     running max m_t and alpha_t, hands alpha_t to the correction warpgroup, writes P
+//     as bf16 back over S, accumulates l_t, and at the end writes O = o/l and LSE.
+//   correction warpgroup: o_t = alpha_t o_{t-1} in tensor memory (skipped when every
+//     alpha of a warp is 1), between the previous P V and the next, while the softmax
+//     warpgroup computes P.
+//   control warpgroup, one thread per role:
+//     MMA: issues S_q = Q_q K_t^T (A and B from shared memory) and o_q += P_q V_t
+//       (A = P from tensor memory, B = V from shared memory) with tcgen05.mma; fp32
+//       accumulators stay in tensor memory.
+//     Q/K load, V load: TMA copies of Q once and of K_t, V_t into rings of shared-memory
+//       slots guarded by full/empty mbarrier pairs (AI Infra ch. 5, Fig. 5-5: producer
+//       copies, consumer computes, one full and one empty barrier per slot).
+//     bias load (dense bias only): TMA copies of 128 x 32 fp32 bias chunks.
 // Causal tiles above the diagonal are never loaded or multiplied; tiles are visited
 // from the diagonal down so each row meets an allowed key in its first tile.
 //
@@ -41,6 +45,25 @@
 namespace eta {
 
 enum { MODE_NONE = 0, MODE_CAUSAL = 1, MODE_DENSE = 2 };
+
+// Phase trace (diagnostics only; compiled in with -DETA_PHASE_TRACE): lane 0 of every
+// warp of the first ETA_TRACE_CTAS CTAs appends (clock64 << 8 | event) records.
+#ifdef ETA_PHASE_TRACE
+constexpr int ETA_TRACE_CTAS = 8;
+constexpr int ETA_TRACE_WARPS = 16;
+constexpr int ETA_TRACE_EVENTS = 1024;
+__device__ unsigned long long g_eta_trace[ETA_TRACE_CTAS][ETA_TRACE_WARPS][ETA_TRACE_EVENTS];
+#define ETA_TRACE(ev)                                                                        \
+  do {                                                                                       \
+    if (blockIdx.x < ETA_TRACE_CTAS && (threadIdx.x % 32) == 0 && trace_n < ETA_TRACE_EVENTS) \
+      g_eta_trace[blockIdx.x][threadIdx.x / 32][trace_n++] =                                 \
+          (static_cast<unsigned long long>(clock64()) << 8) | (ev);                          \
+  } while (0)
+#else
+#define ETA_TRACE(ev) \
+  do {                \
+  } while (0)
+#endif
 
 constexpr int BM = 128;     // query rows per Q tile (= tensor-memory lanes)
 constexpr int BN = 128;     // keys per K/V tile
@@ -94,7 +117,8 @@ struct Cfg {
   static constexpr int K_OFF = Q_OFF + NQ * Q_TILE;
   static constexpr int V_OFF = K_OFF + KS * K_TILE;
   static constexpr int C_OFF = V_OFF + VS * V_TILE;
-  static constexpr int BAR_OFF = C_OFF + CS * CCHUNK_BYTES;
+  static constexpr int ALPHA_OFF = C_OFF + CS * CCHUNK_BYTES;  // float alpha[NQ][128]
+  static constexpr int BAR_OFF = ALPHA_OFF + NQ * BM * 4;
   // barrier indices
   static constexpr int B_QFULL = 0;
   static constexpr int B_KFULL = 1;
@@ -103,9 +127,11 @@ struct Cfg {
   static constexpr int B_VEMPTY = B_VFULL + VS;
   static constexpr int B_CFULL = B_VEMPTY + VS;
   static constexpr int B_CEMPTY = B_CFULL + CS;
-  static constexpr int B_SFULL = B_CEMPTY + CS;
-  static constexpr int B_PFULL = B_SFULL + NQ;
-  static constexpr int B_OFULL = B_PFULL + NQ;
+  static constexpr int B_SFULL = B_CEMPTY + CS;   // S_q ready (and the previous P_q V done)
+  static constexpr int B_PFULL = B_SFULL + NQ;    // P_q written to tensor memory
+  static constexpr int B_AFULL = B_PFULL + NQ;    // alpha_q of every row in shared memory
+  static constexpr int B_OREADY = B_AFULL + NQ;   // o_q rescaled by alpha_q
+  static constexpr int B_OFULL = B_OREADY + NQ;   // last P_q V done
   static constexpr int B_DRAIN = B_OFULL + NQ;
   static constexpr int NUM_BARS = B_DRAIN + 1;
   static constexpr int TMEMPTR_OFF = BAR_OFF + NUM_BARS * 8;
@@ -114,11 +140,26 @@ struct Cfg {
   static constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // room to align the base to 1024 B
   static_assert(SMEM_TOTAL <= 232448, "shared memory over the sm_103a per-CTA limit");
 
-  static constexpr int MMA_WARP = 4 * NQ;
-  static constexpr int LOAD_WARP = 4 * NQ + 1;
-  static constexpr int CLOAD_WARP = 4 * NQ + 2;
-  static constexpr int NUM_WARPS = 4 * NQ + 2 + (C_RING ? 1 : 0);
+  // Warpgroups: NQ softmax warpgroups, one correction warpgroup, one control warpgroup
+  // (MMA warp, Q/K load warp, V load warp, bias load warp).
+  static constexpr int CORR_WARP0 = 4 * NQ;
+  static constexpr int CTRL_WARP0 = 4 * NQ + 4;
+  static constexpr int MMA_WARP = CTRL_WARP0;
+  static constexpr int LOAD_WARP = CTRL_WARP0 + 1;   // Q and K
+  static constexpr int VLOAD_WARP = CTRL_WARP0 + 2;  // V
+  static constexpr int CLOAD_WARP = CTRL_WARP0 + 3;  // dense bias
+  static constexpr int NUM_WARPS = 4 * NQ + 8;
   static constexpr int THREADS = 32 * NUM_WARPS;
+  // Register budgets per warpgroup (setmaxnreg). Their sum over the block stays within
+  // the 64K registers the block is launched with.
+  static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
+  static constexpr int REGS_SOFTMAX = NQ == 2 ? 168 : 224;
+  static constexpr int REGS_CORR = NQ == 2 ? 80 : 152;
+  static constexpr int REGS_CTRL = 96;
+  static_assert(128 * (NQ * REGS_SOFTMAX + REGS_CORR + REGS_CTRL) <= 65536,
+                "register split exceeds the register file");
+  static_assert(REGS_SOFTMAX >= LAUNCH_REGS && REGS_CORR <= LAUNCH_REGS && REGS_CTRL <= LAUNCH_REGS,
+                "softmax warpgroups grow, the others shrink");
   // tensor memory: S_q at columns [q*128, q*128+128), o_q after all S tiles
   static constexpr int S_COL = 0;
   static constexpr int O_COL = NQ * BN;
@@ -130,7 +171,7 @@ struct Cfg {
 };
 
 // Watchdog codes: bit 31 set, role in bits 24-27, barrier index in bits 8-23.
-enum { ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_CLOAD = 4, ROLE_DRAIN = 5 };
+enum { ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_CLOAD = 4, ROLE_DRAIN = 5, ROLE_CORR = 6 };
 
 struct Watchdog {
   volatile int *abort_flag;
@@ -176,7 +217,6 @@ struct Watchdog {
 template <int NQ, int MODE>
 struct Schedule {
   int bh, cta_q, n_exist, hi_max, n_it;
-  int first_it[NQ];
 
   __device__ Schedule(const KernelParams &p) {
     bh = blockIdx.x / p.ctas_per_head;
@@ -185,14 +225,27 @@ struct Schedule {
     n_exist = cmin(NQ, p.num_tiles - cta_q * NQ);
     hi_max = (MODE == MODE_CAUSAL) ? cta_q * NQ + n_exist - 1 : p.num_tiles - 1;
     n_it = hi_max + 1;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-      const int hi_q = (MODE == MODE_CAUSAL) ? cta_q * NQ + q : p.num_tiles - 1;
-      first_it[q] = (q < n_exist) ? hi_max - hi_q : n_it;  // n_it: never active
-    }
+  }
+  // First iteration query tile q takes part in; n_it when the tile does not exist.
+  __device__ int first_it(int q) const {
+    const int hi_q = (MODE == MODE_CAUSAL) ? cta_q * NQ + q : hi_max;
+    return (q < n_exist) ? hi_max - hi_q : n_it;
   }
   __device__ int q_tile(int q) const { return cta_q * NQ + q; }
 };
+
+// Row maximum of 128 values with eight independent three-input max chains.
+__device__ __forceinline__ float row_max128(const float (&x)[BN]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+  for (int c = 16; c < BN; c += 16) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = fmax3(m[k], x[c + 2 * k], x[c + 2 * k + 1]);
+  }
+  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
+}
 
 template <int D, int DV, int MODE, bool C_TMA>
 __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
@@ -209,9 +262,13 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + CF::TMEMPTR_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::ABORT_OFF);
+  float *alpha_s = reinterpret_cast<float *>(smem + CF::ALPHA_OFF);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+#ifdef ETA_PHASE_TRACE
+  int trace_n = 0;
+#endif
   const Schedule<NQ, MODE> sch(p);
   Watchdog wd{abort_flag, p.status, p.timeout_ns};
 
@@ -232,7 +289,9 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
     }
     for (int q = 0; q < NQ; ++q) {
       mbar_init(BAR(CF::B_SFULL + q), 1);
-      mbar_init(BAR(CF::B_PFULL + q), 4);  // one arrival per softmax warp
+      mbar_init(BAR(CF::B_PFULL + q), 4);   // one arrival per softmax warp
+      mbar_init(BAR(CF::B_AFULL + q), 4);   // one arrival per softmax warp
+      mbar_init(BAR(CF::B_OREADY + q), 4);  // one arrival per correction warp
       mbar_init(BAR(CF::B_OFULL + q), 1);
     }
     mbar_init(BAR(CF::B_DRAIN), 1);
@@ -248,8 +307,9 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
 
-  if (warp < 4 * NQ) {
+  if (warp < CF::CORR_WARP0) {
     // ================================================================ softmax
+    regs_increase<CF::REGS_SOFTMAX>();
     const int q = warp / 4;
     const int row = threadIdx.x % BM;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
@@ -265,12 +325,13 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
     bool ok = true;
     int cpos = 0;  // dense-bias ring position
     if (exists) {
-      for (int it = sch.first_it[q]; it < sch.n_it; ++it) {
+      for (int it = sch.first_it(q); it < sch.n_it; ++it) {
         const int j = sch.hi_max - it;
         ok = wd.wait(BAR(CF::B_SFULL + q), s_phase, ROLE_SOFTMAX, CF::B_SFULL + q);
         s_phase ^= 1;
         if (!ok) break;
         tc_fence_after();
+        ETA_TRACE(1);
 
         // Row of S (raw Q K^T) for this thread's query, 128 keys.
         uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -282,6 +343,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
         tmem_wait_ld(r1);
         tmem_wait_ld(r2);
         tmem_wait_ld(r3);
+        ETA_TRACE(2);
         float x[BN];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -306,10 +368,11 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
                 const float4 cv =
                     *reinterpret_cast<const float4 *>(chunk + ((u ^ (row & 7)) << 4));
                 const int c = cc * CCHUNK + 4 * u;
-                x[c + 0] = fmaf(x[c + 0], sl2, cv.x * LOG2E);
-                x[c + 1] = fmaf(x[c + 1], sl2, cv.y * LOG2E);
-                x[c + 2] = fmaf(x[c + 2], sl2, cv.z * LOG2E);
-                x[c + 3] = fmaf(x[c + 3], sl2, cv.w * LOG2E);
+                float b0, b1, b2, b3;
+                mul2(b0, b1, cv.x, cv.y, LOG2E, LOG2E);
+                mul2(b2, b3, cv.z, cv.w, LOG2E, LOG2E);
+                fma2(x[c + 0], x[c + 1], x[c + 0], x[c + 1], sl2, sl2, b0, b1);
+                fma2(x[c + 2], x[c + 3], x[c + 2], x[c + 3], sl2, sl2, b2, b3);
               }
               __syncwarp();
               if (lane == 0) mbar_arrive(BAR(CF::B_CEMPTY + slot));
@@ -340,64 +403,62 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
           }
         }
 
-        // b_t and m_t = max(m_{t-1}, b_t)
-        float b = x[0];
-#pragma unroll
-        for (int c = 1; c + 1 < BN; c += 2) b = fmax3(b, x[c], x[c + 1]);
-        b = fmaxf(b, x[BN - 1]);
+        // b_t and m_t = max(m_{t-1}, b_t); alpha_t = exp(m_{t-1} - m_t) goes to the
+        // correction warpgroup, which rescales o while this warpgroup computes P.
+        const float b = row_max128(x);
         const float m_new = CF::DENSE ? fmaxf(m2, b) : fmaxf(m2, b * sl2);
         // No allowed key seen yet: every p is 0 and alpha is irrelevant; use 0 as reference.
         const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-        const float alpha = ex2_approx(m2 - m_use);  // alpha_t = exp(m_{t-1} - m_t)
+        const float alpha = (m_new == m2) ? 1.0f : ex2_approx(m2 - m_use);
+        alpha_s[q * BM + row] = alpha;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(CF::B_AFULL + q));
+        ETA_TRACE(3);
 
-        // p_ij = exp(S_ij - m_t) as bf16 into tensor memory over S; l_t accumulates fp32 p.
-        uint32_t pk0[32], pk1[32];
-        float rs0 = 0.0f, rs1 = 0.0f;
+        // p_ij = exp(S_ij - m_t) as bf16 into tensor memory over S, 64 keys at a time;
+        // the row sum runs alongside in four independent packed chains.
+        const float neg_m = -m_use;
+        float s[8];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int k0 = 2 * c, k1 = 2 * c + 1;
-          const float p0 = CF::DENSE ? ex2_approx(x[k0] - m_use) : ex2_approx(fmaf(x[k0], sl2, -m_use));
-          const float p1 = CF::DENSE ? ex2_approx(x[k1] - m_use) : ex2_approx(fmaf(x[k1], sl2, -m_use));
-          rs0 += p0;
-          rs1 += p1;
-          pk0[c] = pack_bf16(p0, p1);
-        }
+        for (int k = 0; k < 8; ++k) s[k] = 0.0f;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int k0 = 64 + 2 * c, k1 = 64 + 2 * c + 1;
-          const float p0 = CF::DENSE ? ex2_approx(x[k0] - m_use) : ex2_approx(fmaf(x[k0], sl2, -m_use));
-          const float p1 = CF::DENSE ? ex2_approx(x[k1] - m_use) : ex2_approx(fmaf(x[k1], sl2, -m_use));
-          rs0 += p0;
-          rs1 += p1;
-          pk1[c] = pack_bf16(p0, p1);
-        }
-        l = alpha * l + (rs0 + rs1);
-        tmem_st32(t_s + 0, pk0);
-        tmem_st32(t_s + 32, pk1);
-        tmem_wait_st();
-
-        // o_t = alpha_t o_{t-1}: the previous P V has completed (the S tile just read was
-        // committed after it). Skipped when alpha is 1 for every row of the warp.
-        if (it > sch.first_it[q] && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
 #pragma unroll
-          for (int cc = 0; cc < DV / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(t_o + 32 * cc, o);
-            tmem_wait_ld(o);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-            tmem_st32(t_o + 32 * cc, o);
+          for (int c2 = 0; c2 < 32; ++c2) {
+            const int c = 64 * half + 2 * c2;
+            float a0, a1;
+            if constexpr (CF::DENSE) {
+              add2(a0, a1, x[c], x[c + 1], neg_m, neg_m);
+            } else {
+              fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg_m, neg_m);
+            }
+            const float p0 = ex2_approx(a0);
+            const float p1 = ex2_approx(a1);
+            const int k = 2 * (c2 & 3);
+            add2(s[k], s[k + 1], s[k], s[k + 1], p0, p1);
+            pk[c2] = pack_bf16(p0, p1);
           }
-          tmem_wait_st();
+          tmem_st32(t_s + 32 * half, pk);
         }
-        m2 = m_new;
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(CF::B_PFULL + q));
+        ETA_TRACE(4);
+
+        // l_t = alpha_t l_{t-1} + sum_j p_ij (l sums the fp32 p, before bf16 rounding).
+        add2(s[0], s[1], s[0], s[1], s[2], s[3]);
+        add2(s[4], s[5], s[4], s[5], s[6], s[7]);
+        add2(s[0], s[1], s[0], s[1], s[4], s[5]);
+        l = fmaf(alpha, l, s[0] + s[1]);
+        ETA_TRACE(5);
+        m2 = m_new;
       }
 
       // ------------------------------------------------ epilogue: O = o_T / l_T, LSE
       if (ok) ok = wd.wait(BAR(CF::B_OFULL + q), 0, ROLE_SOFTMAX, CF::B_OFULL + q);
+      ETA_TRACE(6);
       if (ok) {
         tc_fence_after();
         const bool row_ok = q_row < p.N;
@@ -408,24 +469,25 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
           uint32_t o[32];
           tmem_ld32(t_o + 32 * cc, o);
           tmem_wait_ld(o);
+          float f[32];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            mul2(f[c], f[c + 1], __uint_as_float(o[c]), __uint_as_float(o[c + 1]), inv_l, inv_l);
           if (row_ok) {
             if (p.out_f32) {
               float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.O) + orow + 32 * cc);
 #pragma unroll
               for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv_l,
-                                     __uint_as_float(o[4 * v + 1]) * inv_l,
-                                     __uint_as_float(o[4 * v + 2]) * inv_l,
-                                     __uint_as_float(o[4 * v + 3]) * inv_l);
+                dst[v] = make_float4(f[4 * v + 0], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
             } else {
               uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.O) + orow + 32 * cc);
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
                 uint4 w;
-                w.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-                w.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-                w.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-                w.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+                w.x = pack_bf16(f[8 * v + 0], f[8 * v + 1]);
+                w.y = pack_bf16(f[8 * v + 2], f[8 * v + 3]);
+                w.z = pack_bf16(f[8 * v + 4], f[8 * v + 5]);
+                w.w = pack_bf16(f[8 * v + 6], f[8 * v + 7]);
                 dst[v] = w;
               }
             }
@@ -438,169 +500,220 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
         }
       }
     }
-  } else if (warp == CF::MMA_WARP) {
-    // ================================================================ MMA issue
-    uint32_t p_phase[NQ];
+  } else if (warp < CF::CTRL_WARP0) {
+    // ================================================================ correction
+    // o_t = alpha_t o_{t-1}, in tensor memory, between the previous P V and the next.
+    if constexpr (CF::REGS_CORR < CF::LAUNCH_REGS) regs_decrease<CF::REGS_CORR>();
+    const int row = threadIdx.x % BM;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
+    uint32_t a_phase[NQ];
 #pragma unroll
-    for (int q = 0; q < NQ; ++q) p_phase[q] = 0;
-    bool ok = wd.wait(BAR(CF::B_QFULL), 0, ROLE_MMA, CF::B_QFULL);
-    tc_fence_after();
-
-    auto issue_s = [&](int q, int kslot) {
-      const uint32_t a0 = sbase + CF::Q_OFF + q * CF::Q_TILE;
-      const uint32_t b0 = sbase + CF::K_OFF + kslot * CF::K_TILE;
-#pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks) {
-        const uint32_t off = (ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32;
-        mma_ss(tmem + CF::S_COL + q * BN, smem_desc(a0 + off, 16, 1024),
-               smem_desc(b0 + off, 16, 1024), CF::IDESC_S, ks > 0 ? 1u : 0u);
-      }
-    };
-    auto issue_pv = [&](int q, int vslot, bool accumulate) {
-      const uint32_t b0 = sbase + CF::V_OFF + vslot * CF::V_TILE;
-#pragma unroll
-      for (int ks = 0; ks < BN / 16; ++ks) {
-        mma_ts(tmem + CF::O_COL + q * DV, tmem + CF::S_COL + q * BN + ks * 8,
-               smem_desc(b0 + ks * 16 * 128, SW_CHUNK_BYTES, 1024), CF::IDESC_PV,
-               (ks > 0 || accumulate) ? 1u : 0u);
-      }
-    };
-
+    for (int q = 0; q < NQ; ++q) a_phase[q] = 0;
+    bool ok = true;
     for (int it = 0; ok && it < sch.n_it; ++it) {
-      const int kslot = it % CF::KS;
-      const int vprev = (it + CF::VS - 1) % CF::VS;
-      ok = wd.wait(BAR(CF::B_KFULL + kslot), (it / CF::KS) & 1, ROLE_MMA, CF::B_KFULL + kslot);
-      if (ok && it > 0)
-        ok = wd.wait(BAR(CF::B_VFULL + vprev), ((it - 1) / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vprev);
-      if (!ok) break;
-      tc_fence_after();
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
-        if (it < sch.first_it[q]) continue;
-        if (it > sch.first_it[q]) {
-          // o_q += P_q V_{it-1}, once the softmax has written P and rescaled o.
-          ok = wd.wait(BAR(CF::B_PFULL + q), p_phase[q], ROLE_MMA, CF::B_PFULL + q);
-          p_phase[q] ^= 1;
-          if (!ok) break;
+        if (!ok || it < sch.first_it(q)) continue;
+        ok = wd.wait(BAR(CF::B_AFULL + q), a_phase[q], ROLE_CORR, CF::B_AFULL + q);
+        a_phase[q] ^= 1;
+        if (!ok) break;
+        ETA_TRACE(10 + q);
+        const float alpha = alpha_s[q * BM + row];
+        // The S tile the softmax read was committed after the previous P V, so o is stable.
+        if (it > sch.first_it(q) && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
           tc_fence_after();
-          if (lane == 0) issue_pv(q, vprev, it - 1 > sch.first_it[q]);
-          __syncwarp();
-        }
-        if (lane == 0) {
-          issue_s(q, kslot);  // S_q = Q_q K_it^T
-          mma_commit(BAR(CF::B_SFULL + q));
-        }
-        __syncwarp();
-      }
-      if (!ok) break;
-      if (lane == 0) {
-        mma_commit(BAR(CF::B_KEMPTY + kslot));
-        if (it > 0) mma_commit(BAR(CF::B_VEMPTY + vprev));
-      }
-      __syncwarp();
-    }
-    if (ok) {
-      const int last = sch.n_it - 1;
-      const int vslot = last % CF::VS;
-      ok = wd.wait(BAR(CF::B_VFULL + vslot), (last / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
-      if (ok) tc_fence_after();
+          const uint32_t t_o = tmem + lane_off + CF::O_COL + q * DV;
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        if (!ok || sch.first_it[q] >= sch.n_it) continue;
-        ok = wd.wait(BAR(CF::B_PFULL + q), p_phase[q], ROLE_MMA, CF::B_PFULL + q);
+          for (int cc = 0; cc < DV / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(t_o + 32 * cc, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float f0, f1;
+              mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), alpha, alpha);
+              o[c] = __float_as_uint(f0);
+              o[c + 1] = __float_as_uint(f1);
+            }
+            tmem_st32(t_o + 32 * cc, o);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(CF::B_OREADY + q));
+        ETA_TRACE(12 + q);
+      }
+    }
+  } else {
+    // Control warpgroup. The MMA role runs on the whole warp with one elected lane issuing
+    // each instruction; each copy role runs on lane 0 alone while the other lanes wait at
+    // the warp barrier below.
+    regs_decrease<CF::REGS_CTRL>();
+    if (warp == CF::MMA_WARP) {
+      // ============================================================== MMA issue
+      // The whole warp runs this loop; each MMA and commit is issued by one elected lane.
+      uint32_t p_phase[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) p_phase[q] = 0;
+      bool ok = wd.wait(BAR(CF::B_QFULL), 0, ROLE_MMA, CF::B_QFULL);
+      tc_fence_after();
+
+      // The descriptors' address field holds (address >> 4) in 14 bits; shared-memory
+      // addresses stay below 2^18, so adding (offset >> 4) to a descriptor never carries.
+      auto issue_s = [&](int q, int kslot) {
+        const uint64_t a_desc = smem_desc(sbase + CF::Q_OFF + q * CF::Q_TILE, 16, 1024);
+        const uint64_t b_desc = smem_desc(sbase + CF::K_OFF + kslot * CF::K_TILE, 16, 1024);
+        const uint32_t d_tmem = tmem + CF::S_COL + q * BN;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = ((ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32) >> 4;
+          mma_ss_elect(d_tmem, a_desc + off, b_desc + off, CF::IDESC_S, ks > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int q, int vslot, bool accumulate) {
+        const uint64_t b_desc =
+            smem_desc(sbase + CF::V_OFF + vslot * CF::V_TILE, SW_CHUNK_BYTES, 1024);
+        const uint32_t d_tmem = tmem + CF::O_COL + q * DV;
+        const uint32_t a_tmem = tmem + CF::S_COL + q * BN;
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ts_elect(d_tmem, a_tmem + ks * 8, b_desc + ((ks * 16 * 128) >> 4), CF::IDESC_PV,
+                       (ks > 0 || accumulate) ? 1u : 0u);
+      };
+      // P_q and the rescaled o_q must both be ready before o_q += P_q V.
+      auto wait_pv_inputs = [&](int q) -> bool {
+        bool r = wd.wait(BAR(CF::B_PFULL + q), p_phase[q], ROLE_MMA, CF::B_PFULL + q);
+        if (r) r = wd.wait(BAR(CF::B_OREADY + q), p_phase[q], ROLE_MMA, CF::B_OREADY + q);
         p_phase[q] ^= 1;
+        return r;
+      };
+
+      for (int it = 0; ok && it < sch.n_it; ++it) {
+        const int kslot = it % CF::KS;
+        const int vprev = (it + CF::VS - 1) % CF::VS;
+        ok = wd.wait(BAR(CF::B_KFULL + kslot), (it / CF::KS) & 1, ROLE_MMA, CF::B_KFULL + kslot);
+        ETA_TRACE(20);
+        if (ok && it > 0)
+          ok = wd.wait(BAR(CF::B_VFULL + vprev), ((it - 1) / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vprev);
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) {
-          issue_pv(q, vslot, last > sch.first_it[q]);
-          mma_commit(BAR(CF::B_OFULL + q));
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (it < sch.first_it(q)) continue;
+          ETA_TRACE(21);
+          if (it > sch.first_it(q)) {
+            ok = wait_pv_inputs(q);
+            if (!ok) break;
+            ETA_TRACE(22 + q);
+            tc_fence_after();
+            issue_pv(q, vprev, it - 1 > sch.first_it(q));  // o_q += P_q V_{it-1}
+          }
+          issue_s(q, kslot);  // S_q = Q_q K_it^T
+          mma_commit_elect(BAR(CF::B_SFULL + q));
+          ETA_TRACE(24 + q);
         }
-        __syncwarp();
+        if (!ok) break;
+        mma_commit_elect(BAR(CF::B_KEMPTY + kslot));
+        if (it > 0) mma_commit_elect(BAR(CF::B_VEMPTY + vprev));
       }
-      if (ok && lane == 0) mma_commit(BAR(CF::B_VEMPTY + vslot));
-      __syncwarp();
-    }
-    // Nothing may still be in flight on the tensor cores when tensor memory is freed.
-    if (lane == 0) mma_commit(BAR(CF::B_DRAIN));
-    __syncwarp();
-    wd.drain(BAR(CF::B_DRAIN), 0, CF::B_DRAIN);
-  } else if (warp == CF::LOAD_WARP) {
-    // ================================================================ TMA: Q, K, V
-    if (lane == 0) {
+      if (ok) {
+        const int last = sch.n_it - 1;
+        const int vslot = last % CF::VS;
+        ok = wd.wait(BAR(CF::B_VFULL + vslot), (last / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
+        if (ok) tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (!ok || sch.first_it(q) >= sch.n_it) continue;
+          ok = wait_pv_inputs(q);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(q, vslot, last > sch.first_it(q));
+          mma_commit_elect(BAR(CF::B_OFULL + q));
+        }
+        if (ok) mma_commit_elect(BAR(CF::B_VEMPTY + vslot));
+      }
+      // Nothing may still be in flight on the tensor cores when tensor memory is freed.
+      mma_commit_elect(BAR(CF::B_DRAIN));
+      wd.drain(BAR(CF::B_DRAIN), 0, CF::B_DRAIN);
+    } else if (warp == CF::LOAD_WARP && lane == 0) {
+      // ============================================================== TMA: Q, K
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(BAR(CF::B_QFULL), sch.n_exist * CF::Q_TILE);
       for (int q = 0; q < sch.n_exist; ++q)
         for (int kc = 0; kc < D / SW_CHUNK; ++kc)
-          tma_load_3d(sbase + CF::Q_OFF + q * CF::Q_TILE + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK,
-                      sch.q_tile(q) * BM, sch.bh, BAR(CF::B_QFULL));
-    }
-    __syncwarp();
-    bool ok = true;
-    int k_issued = 0, v_issued = 0;
-    for (int it = 0; it < sch.n_it; ++it) {
-      const int j = sch.hi_max - it;
-      const int ks = it % CF::KS;
-      ok = wd.wait(BAR(CF::B_KEMPTY + ks), ((it / CF::KS) & 1) ^ 1, ROLE_LOAD, CF::B_KEMPTY + ks);
-      if (!ok) break;
-      if (lane == 0) {
+          tma_load_3d(sbase + CF::Q_OFF + q * CF::Q_TILE + kc * SW_CHUNK_BYTES, &tmQ,
+                      kc * SW_CHUNK, sch.q_tile(q) * BM, sch.bh, BAR(CF::B_QFULL));
+      // K runs ahead on its own ring; V has its own producer so neither blocks the other.
+      bool ok = true;
+      int k_issued = 0;
+      for (int it = 0; it < sch.n_it; ++it) {
+        const int j = sch.hi_max - it;
+        const int ks = it % CF::KS;
+        ok = wd.wait1(BAR(CF::B_KEMPTY + ks), ((it / CF::KS) & 1) ^ 1, ROLE_LOAD, CF::B_KEMPTY + ks, false);
+        ETA_TRACE(30);
+        if (!ok) break;
         mbar_arrive_expect_tx(BAR(CF::B_KFULL + ks), CF::K_TILE);
         for (int kc = 0; kc < D / SW_CHUNK; ++kc)
-          tma_load_3d(sbase + CF::K_OFF + ks * CF::K_TILE + kc * SW_CHUNK_BYTES, &tmK, kc * SW_CHUNK,
-                      j * BN, sch.bh, BAR(CF::B_KFULL + ks));
+          tma_load_3d(sbase + CF::K_OFF + ks * CF::K_TILE + kc * SW_CHUNK_BYTES, &tmK,
+                      kc * SW_CHUNK, j * BN, sch.bh, BAR(CF::B_KFULL + ks));
+        ++k_issued;
       }
-      __syncwarp();
-      ++k_issued;
-      const int vs = it % CF::VS;
-      ok = wd.wait(BAR(CF::B_VEMPTY + vs), ((it / CF::VS) & 1) ^ 1, ROLE_LOAD, CF::B_VEMPTY + vs);
-      if (!ok) break;
-      if (lane == 0) {
+      // Wait for the last copy into each slot to land before the CTA may exit.
+      wd.wait1(BAR(CF::B_QFULL), 0, ROLE_DRAIN, CF::B_QFULL, true);
+      for (int s = 0; s < CF::KS && s < k_issued; ++s) {
+        const int last = s + ((k_issued - 1 - s) / CF::KS) * CF::KS;
+        wd.wait1(BAR(CF::B_KFULL + s), (last / CF::KS) & 1, ROLE_DRAIN, CF::B_KFULL + s, true);
+      }
+    } else if (warp == CF::VLOAD_WARP && lane == 0) {
+      // ============================================================== TMA: V
+      tma_prefetch_desc(&tmV);
+      int v_issued = 0;
+      for (int it = 0; it < sch.n_it; ++it) {
+        const int j = sch.hi_max - it;
+        const int vs = it % CF::VS;
+        const bool ok =
+            wd.wait1(BAR(CF::B_VEMPTY + vs), ((it / CF::VS) & 1) ^ 1, ROLE_LOAD, CF::B_VEMPTY + vs, false);
+        ETA_TRACE(31);
+        if (!ok) break;
         mbar_arrive_expect_tx(BAR(CF::B_VFULL + vs), CF::V_TILE);
         for (int kc = 0; kc < DV / SW_CHUNK; ++kc)
-          tma_load_3d(sbase + CF::V_OFF + vs * CF::V_TILE + kc * SW_CHUNK_BYTES, &tmV, kc * SW_CHUNK,
-                      j * BN, sch.bh, BAR(CF::B_VFULL + vs));
+          tma_load_3d(sbase + CF::V_OFF + vs * CF::V_TILE + kc * SW_CHUNK_BYTES, &tmV,
+                      kc * SW_CHUNK, j * BN, sch.bh, BAR(CF::B_VFULL + vs));
+        ++v_issued;
       }
-      __syncwarp();
-      ++v_issued;
-    }
-    // Wait for the last copy into each slot to land before the CTA may exit.
-    wd.drain(BAR(CF::B_QFULL), 0, CF::B_QFULL);
-    for (int s = 0; s < CF::KS && s < k_issued; ++s) {
-      const int last = s + ((k_issued - 1 - s) / CF::KS) * CF::KS;
-      wd.drain(BAR(CF::B_KFULL + s), (last / CF::KS) & 1, CF::B_KFULL + s);
-    }
-    for (int s = 0; s < CF::VS && s < v_issued; ++s) {
-      const int last = s + ((v_issued - 1 - s) / CF::VS) * CF::VS;
-      wd.drain(BAR(CF::B_VFULL + s), (last / CF::VS) & 1, CF::B_VFULL + s);
-    }
-  } else if (CF::C_RING && warp == CF::CLOAD_WARP) {
-    // ================================================================ TMA: dense bias
-    if (lane == 0) tma_prefetch_desc(&tmC);
-    int issued = 0;
-    for (int it = 0; it < sch.n_it; ++it) {
-      const int j = sch.hi_max - it;
-      bool ok = true;
-      for (int cc = 0; cc < BN / CCHUNK; ++cc) {
-        const int pos = issued;
-        const int slot = pos % CF::CS;
-        ok = wd.wait(BAR(CF::B_CEMPTY + slot), ((pos / CF::CS) & 1) ^ 1, ROLE_CLOAD,
-                     CF::B_CEMPTY + slot);
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(BAR(CF::B_CFULL + slot), CCHUNK_BYTES);
-          tma_load_3d(sbase + CF::C_OFF + slot * CCHUNK_BYTES, &tmC, j * BN + cc * CCHUNK,
-                      sch.q_tile(0) * BM, sch.bh, BAR(CF::B_CFULL + slot));
+      for (int s = 0; s < CF::VS && s < v_issued; ++s) {
+        const int last = s + ((v_issued - 1 - s) / CF::VS) * CF::VS;
+        wd.wait1(BAR(CF::B_VFULL + s), (last / CF::VS) & 1, ROLE_DRAIN, CF::B_VFULL + s, true);
+      }
+    } else if (warp == CF::CLOAD_WARP && lane == 0) {
+      // ============================================================== TMA: dense bias
+      if constexpr (CF::C_RING) {
+        tma_prefetch_desc(&tmC);
+        int issued = 0;
+        bool ok = true;
+        for (int it = 0; ok && it < sch.n_it; ++it) {
+          const int j = sch.hi_max - it;
+          for (int cc = 0; cc < BN / CCHUNK; ++cc) {
+            const int pos = issued;
+            const int slot = pos % CF::CS;
+            ok = wd.wait1(BAR(CF::B_CEMPTY + slot), ((pos / CF::CS) & 1) ^ 1, ROLE_CLOAD,
+                          CF::B_CEMPTY + slot, false);
+            if (!ok) break;
+            mbar_arrive_expect_tx(BAR(CF::B_CFULL + slot), CCHUNK_BYTES);
+            tma_load_3d(sbase + CF::C_OFF + slot * CCHUNK_BYTES, &tmC, j * BN + cc * CCHUNK,
+                        sch.q_tile(0) * BM, sch.bh, BAR(CF::B_CFULL + slot));
+            ++issued;
+          }
         }
-        __syncwarp();
-        ++issued;
+        for (int s = 0; s < CF::CS && s < issued; ++s) {
+          const int last = s + ((issued - 1 - s) / CF::CS) * CF::CS;
+          wd.wait1(BAR(CF::B_CFULL + s), (last / CF::CS) & 1, ROLE_DRAIN, CF::B_CFULL + s, true);
+        }
       }
-      if (!ok) break;
     }
-    for (int s = 0; s < CF::CS && s < issued; ++s) {
-      const int last = s + ((issued - 1 - s) / CF::CS) * CF::CS;
-      wd.drain(BAR(CF::B_CFULL + s), (last / CF::CS) & 1, CF::B_CFULL + s);
-    }
+    __syncwarp();
   }
 
   // ------------------------------------------------------------------ teardown
