@@ -10,18 +10,17 @@
 //
 // One CTA owns NQ query tiles of 128 rows of one head (NQ = 2 without a dense bias,
 // so one tile's softmax overlaps the other tile's matrix products; NQ = 1 with a
-// dense bias, whose time is the bias bytes). Warp roles (16 or 12 warps):
+// dense bias, whose time is the bias bytes). Warp roles (12 or 8 warps):
 //   softmax warpgroup q (warps 4q..4q+3): thread = query row = tensor-memory lane.
 //     Reads its row of S from tensor memory, masks, takes the tile max b_t, the new
-//     running max m_t and alpha_t, hands alpha_t to the correction warpgroup, writes P
-//     as bf16 back over S, accumulates l_t, and at the end writes O = o/l and LSE.
-//   correction warpgroup: o_t = alpha_t o_{t-1} in tensor memory (skipped when every
-//     alpha of a warp is 1), between the previous P V and the next, while the softmax
-//     warpgroup computes P.
-//   control warpgroup, one thread per role:
-//     MMA: issues S_q = Q_q K_t^T (A and B from shared memory) and o_q += P_q V_t
-//       (A = P from tensor memory, B = V from shared memory) with tcgen05.mma; fp32
-//       accumulators stay in tensor memory.
+//     running max m_t and alpha_t, writes P as bf16 back over S, rescales its row of o
+//     by alpha_t in tensor memory between the quarters of the exponential loop (skipped
+//     when every alpha of the warp is 1), accumulates l_t, and at the end writes
+//     O = o/l and LSE.
+//   control warpgroup, one thread per copy role:
+//     MMA (whole warp, one elected lane issues): S_q = Q_q K_t^T (A and B from shared
+//       memory) and o_q += P_q V_t (A = P from tensor memory, B = V from shared memory)
+//       with tcgen05.mma; fp32 accumulators stay in tensor memory.
 //     Q/K load, V load: TMA copies of Q once and of K_t, V_t into rings of shared-memory
 //       slots guarded by full/empty mbarrier pairs (AI Infra ch. 5, Fig. 5-5: producer
 //       copies, consumer computes, one full and one empty barrier per slot).
@@ -55,9 +54,10 @@ constexpr int ETA_TRACE_EVENTS = 1024;
 __device__ unsigned long long g_eta_trace[ETA_TRACE_CTAS][ETA_TRACE_WARPS][ETA_TRACE_EVENTS];
 #define ETA_TRACE(ev)                                                                        \
   do {                                                                                       \
+    const unsigned long long eta_t = (static_cast<unsigned long long>(clock64()) << 8) | (ev); \
     if (blockIdx.x < ETA_TRACE_CTAS && (threadIdx.x % 32) == 0 && trace_n < ETA_TRACE_EVENTS) \
-      g_eta_trace[blockIdx.x][threadIdx.x / 32][trace_n++] =                                 \
-          (static_cast<unsigned long long>(clock64()) << 8) | (ev);                          \
+      g_eta_trace[blockIdx.x][threadIdx.x / 32][trace_n] = eta_t;                            \
+    ++trace_n;                                                                               \
   } while (0)
 #else
 #define ETA_TRACE(ev) \
@@ -117,8 +117,7 @@ struct Cfg {
   static constexpr int K_OFF = Q_OFF + NQ * Q_TILE;
   static constexpr int V_OFF = K_OFF + KS * K_TILE;
   static constexpr int C_OFF = V_OFF + VS * V_TILE;
-  static constexpr int ALPHA_OFF = C_OFF + CS * CCHUNK_BYTES;  // float alpha[NQ][128]
-  static constexpr int BAR_OFF = ALPHA_OFF + NQ * BM * 4;
+  static constexpr int BAR_OFF = C_OFF + CS * CCHUNK_BYTES;
   // barrier indices
   static constexpr int B_QFULL = 0;
   static constexpr int B_KFULL = 1;
@@ -128,38 +127,42 @@ struct Cfg {
   static constexpr int B_CFULL = B_VEMPTY + VS;
   static constexpr int B_CEMPTY = B_CFULL + CS;
   static constexpr int B_SFULL = B_CEMPTY + CS;   // S_q ready (and the previous P_q V done)
-  static constexpr int B_PFULL = B_SFULL + NQ;    // P_q written to tensor memory
-  static constexpr int B_AFULL = B_PFULL + NQ;    // alpha_q of every row in shared memory
-  static constexpr int B_OREADY = B_AFULL + NQ;   // o_q rescaled by alpha_q
-  static constexpr int B_OFULL = B_OREADY + NQ;   // last P_q V done
+  static constexpr int B_PFULL = B_SFULL + NQ;    // P_q written and o_q rescaled
+  static constexpr int B_OFULL = B_PFULL + NQ;    // last P_q V done
   static constexpr int B_DRAIN = B_OFULL + NQ;
   static constexpr int NUM_BARS = B_DRAIN + 1;
   static constexpr int TMEMPTR_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = TMEMPTR_OFF + 4;
   static constexpr int SMEM_USED = ABORT_OFF + 4;
-  static constexpr int SMEM_TOTAL = SMEM_USED + 1024;  // room to align the base to 1024 B
+  // Room to align the base to 1024 B, and at least 120 KB so that one CTA holds an SM:
+  // the CTA allocates most of the SM's tensor memory, and a second resident CTA would
+  // block in tcgen05.alloc.
+  static constexpr int SMEM_TOTAL = SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
   static_assert(SMEM_TOTAL <= 232448, "shared memory over the sm_103a per-CTA limit");
 
-  // Warpgroups: NQ softmax warpgroups, one correction warpgroup, one control warpgroup
-  // (MMA warp, Q/K load warp, V load warp, bias load warp).
-  static constexpr int CORR_WARP0 = 4 * NQ;
-  static constexpr int CTRL_WARP0 = 4 * NQ + 4;
+  // Warpgroups: NQ softmax warpgroups and one control warpgroup (MMA warp, Q/K load
+  // warp, V load warp, bias load warp).
+  static constexpr int CTRL_WARP0 = 4 * NQ;
   static constexpr int MMA_WARP = CTRL_WARP0;
   static constexpr int LOAD_WARP = CTRL_WARP0 + 1;   // Q and K
   static constexpr int VLOAD_WARP = CTRL_WARP0 + 2;  // V
   static constexpr int CLOAD_WARP = CTRL_WARP0 + 3;  // dense bias
-  static constexpr int NUM_WARPS = 4 * NQ + 8;
+  static constexpr int NUM_WARPS = 4 * NQ + 4;
   static constexpr int THREADS = 32 * NUM_WARPS;
-  // Register budgets per warpgroup (setmaxnreg). Their sum over the block stays within
-  // the 64K registers the block is launched with.
+  // Register budgets per warpgroup (setmaxnreg, two query tiles only): the softmax
+  // warpgroups keep a whole row of S and the packed P in registers; the control
+  // warpgroup needs few. setmaxnreg redistributes the registers the block was launched
+  // with (THREADS x LAUNCH_REGS = 384 x 168 = 64512), so the budgets must add up to at
+  // most that: 128 * (2 * 216 + 72) = 64512. A larger sum would never be granted.
   static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
-  static constexpr int REGS_SOFTMAX = NQ == 2 ? 168 : 224;
-  static constexpr int REGS_CORR = NQ == 2 ? 80 : 152;
-  static constexpr int REGS_CTRL = 96;
-  static_assert(128 * (NQ * REGS_SOFTMAX + REGS_CORR + REGS_CTRL) <= 65536,
-                "register split exceeds the register file");
-  static_assert(REGS_SOFTMAX >= LAUNCH_REGS && REGS_CORR <= LAUNCH_REGS && REGS_CTRL <= LAUNCH_REGS,
-                "softmax warpgroups grow, the others shrink");
+  static constexpr bool SPLIT_REGS = NQ == 2;
+  static constexpr int REGS_SOFTMAX = 216;
+  static constexpr int REGS_CTRL = 72;
+  static constexpr int REGS_NEEDED = SPLIT_REGS ? 128 * (NQ * REGS_SOFTMAX + REGS_CTRL) : 0;
+  static_assert(!SPLIT_REGS || REGS_NEEDED <= THREADS * LAUNCH_REGS,
+                "register split exceeds the registers the block is launched with");
+  static_assert(!SPLIT_REGS || (REGS_SOFTMAX >= LAUNCH_REGS && REGS_CTRL <= LAUNCH_REGS),
+                "softmax warpgroups grow, the control warpgroup shrinks");
   // tensor memory: S_q at columns [q*128, q*128+128), o_q after all S tiles
   static constexpr int S_COL = 0;
   static constexpr int O_COL = NQ * BN;
@@ -171,7 +174,7 @@ struct Cfg {
 };
 
 // Watchdog codes: bit 31 set, role in bits 24-27, barrier index in bits 8-23.
-enum { ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_CLOAD = 4, ROLE_DRAIN = 5, ROLE_CORR = 6 };
+enum { ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_CLOAD = 4, ROLE_DRAIN = 5 };
 
 struct Watchdog {
   volatile int *abort_flag;
@@ -201,7 +204,9 @@ struct Watchdog {
   }
 
   // Whole-warp bounded wait: every lane observes the barrier; the result is uniform.
+  // The common case (phase already complete) is one try_wait and one vote.
   __device__ bool wait(uint32_t bar_addr, uint32_t parity, int role, int bar) {
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar_addr, parity))) return true;
     const bool ok = wait1(bar_addr, parity, role, bar, false);
     return __all_sync(0xFFFFFFFFu, ok);
   }
@@ -262,7 +267,6 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + CF::TMEMPTR_OFF);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::ABORT_OFF);
-  float *alpha_s = reinterpret_cast<float *>(smem + CF::ALPHA_OFF);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -289,9 +293,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
     }
     for (int q = 0; q < NQ; ++q) {
       mbar_init(BAR(CF::B_SFULL + q), 1);
-      mbar_init(BAR(CF::B_PFULL + q), 4);   // one arrival per softmax warp
-      mbar_init(BAR(CF::B_AFULL + q), 4);   // one arrival per softmax warp
-      mbar_init(BAR(CF::B_OREADY + q), 4);  // one arrival per correction warp
+      mbar_init(BAR(CF::B_PFULL + q), 4);  // one arrival per softmax warp
       mbar_init(BAR(CF::B_OFULL + q), 1);
     }
     mbar_init(BAR(CF::B_DRAIN), 1);
@@ -307,9 +309,9 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
 
-  if (warp < CF::CORR_WARP0) {
+  if (warp < CF::CTRL_WARP0) {
     // ================================================================ softmax
-    regs_increase<CF::REGS_SOFTMAX>();
+    if constexpr (CF::SPLIT_REGS) regs_increase<CF::REGS_SOFTMAX>();
     const int q = warp / 4;
     const int row = threadIdx.x % BM;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
                 fma2(x[c + 2], x[c + 3], x[c + 2], x[c + 3], sl2, sl2, b2, b3);
               }
               __syncwarp();
-              if (lane == 0) mbar_arrive(BAR(CF::B_CEMPTY + slot));
+              mbar_arrive_elect(BAR(CF::B_CEMPTY + slot));
               ++cpos;
             }
             if (!ok) break;
@@ -403,30 +405,33 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
           }
         }
 
-        // b_t and m_t = max(m_{t-1}, b_t); alpha_t = exp(m_{t-1} - m_t) goes to the
-        // correction warpgroup, which rescales o while this warpgroup computes P.
+        // b_t and m_t = max(m_{t-1}, b_t); alpha_t = exp(m_{t-1} - m_t).
         const float b = row_max128(x);
         const float m_new = CF::DENSE ? fmaxf(m2, b) : fmaxf(m2, b * sl2);
         // No allowed key seen yet: every p is 0 and alpha is irrelevant; use 0 as reference.
         const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
         const float alpha = (m_new == m2) ? 1.0f : ex2_approx(m2 - m_use);
-        alpha_s[q * BM + row] = alpha;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(CF::B_AFULL + q));
-        ETA_TRACE(3);
+        // o_t = alpha_t o_{t-1}, skipped when alpha is 1 for every row of the warp. The
+        // previous P V has completed (the S tile just read was committed after it). The
+        // 32-column chunks of o are loaded, scaled and stored between the quarters of
+        // the exponential loop, in the shadow of the exponential unit.
+        const bool rescale = it > sch.first_it(q) && __any_sync(0xFFFFFFFFu, alpha != 1.0f);
+        constexpr int OCH = DV / 32;  // chunks of o
+        uint32_t o[32];
+        if (rescale) tmem_ld32(t_o, o);
 
-        // p_ij = exp(S_ij - m_t) as bf16 into tensor memory over S, 64 keys at a time;
+        // p_ij = exp(S_ij - m_t) as bf16 into tensor memory over S, 32 keys at a time;
         // the row sum runs alongside in four independent packed chains.
         const float neg_m = -m_use;
         float s[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) s[k] = 0.0f;
+        uint32_t pk[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t pk[32];
+        for (int qq = 0; qq < 4; ++qq) {
 #pragma unroll
-          for (int c2 = 0; c2 < 32; ++c2) {
-            const int c = 64 * half + 2 * c2;
+          for (int c2 = 0; c2 < 16; ++c2) {
+            const int c = 32 * qq + 2 * c2;
             float a0, a1;
             if constexpr (CF::DENSE) {
               add2(a0, a1, x[c], x[c + 1], neg_m, neg_m);
@@ -437,14 +442,26 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
             const float p1 = ex2_approx(a1);
             const int k = 2 * (c2 & 3);
             add2(s[k], s[k + 1], s[k], s[k + 1], p0, p1);
-            pk[c2] = pack_bf16(p0, p1);
+            pk[16 * (qq & 1) + c2] = pack_bf16(p0, p1);
           }
-          tmem_st32(t_s + 32 * half, pk);
+          if (qq & 1) tmem_st32(t_s + 32 * (qq / 2), pk);
+          if (rescale && qq < OCH) {
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float f0, f1;
+              mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), alpha, alpha);
+              o[c] = __float_as_uint(f0);
+              o[c + 1] = __float_as_uint(f1);
+            }
+            tmem_st32(t_o + 32 * qq, o);
+            if (qq + 1 < OCH) tmem_ld32(t_o + 32 * (qq + 1), o);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(CF::B_PFULL + q));
+        mbar_arrive_elect(BAR(CF::B_PFULL + q));
         ETA_TRACE(4);
 
         // l_t = alpha_t l_{t-1} + sum_j p_ij (l sums the fp32 p, before bf16 rounding).
@@ -500,56 +517,11 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
         }
       }
     }
-  } else if (warp < CF::CTRL_WARP0) {
-    // ================================================================ correction
-    // o_t = alpha_t o_{t-1}, in tensor memory, between the previous P V and the next.
-    if constexpr (CF::REGS_CORR < CF::LAUNCH_REGS) regs_decrease<CF::REGS_CORR>();
-    const int row = threadIdx.x % BM;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
-    uint32_t a_phase[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) a_phase[q] = 0;
-    bool ok = true;
-    for (int it = 0; ok && it < sch.n_it; ++it) {
-#pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        if (!ok || it < sch.first_it(q)) continue;
-        ok = wd.wait(BAR(CF::B_AFULL + q), a_phase[q], ROLE_CORR, CF::B_AFULL + q);
-        a_phase[q] ^= 1;
-        if (!ok) break;
-        ETA_TRACE(10 + q);
-        const float alpha = alpha_s[q * BM + row];
-        // The S tile the softmax read was committed after the previous P V, so o is stable.
-        if (it > sch.first_it(q) && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-          tc_fence_after();
-          const uint32_t t_o = tmem + lane_off + CF::O_COL + q * DV;
-#pragma unroll
-          for (int cc = 0; cc < DV / 32; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(t_o + 32 * cc, o);
-            tmem_wait_ld(o);
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              float f0, f1;
-              mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), alpha, alpha);
-              o[c] = __float_as_uint(f0);
-              o[c + 1] = __float_as_uint(f1);
-            }
-            tmem_st32(t_o + 32 * cc, o);
-          }
-          tmem_wait_st();
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(CF::B_OREADY + q));
-        ETA_TRACE(12 + q);
-      }
-    }
   } else {
     // Control warpgroup. The MMA role runs on the whole warp with one elected lane issuing
     // each instruction; each copy role runs on lane 0 alone while the other lanes wait at
     // the warp barrier below.
-    regs_decrease<CF::REGS_CTRL>();
+    if constexpr (CF::SPLIT_REGS) regs_decrease<CF::REGS_CTRL>();
     if (warp == CF::MMA_WARP) {
       // ============================================================== MMA issue
       // The whole warp runs this loop; each MMA and commit is issued by one elected lane.
@@ -581,10 +553,9 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
           mma_ts_elect(d_tmem, a_tmem + ks * 8, b_desc + ((ks * 16 * 128) >> 4), CF::IDESC_PV,
                        (ks > 0 || accumulate) ? 1u : 0u);
       };
-      // P_q and the rescaled o_q must both be ready before o_q += P_q V.
+      // P_q written and o_q rescaled (one barrier) before o_q += P_q V.
       auto wait_pv_inputs = [&](int q) -> bool {
-        bool r = wd.wait(BAR(CF::B_PFULL + q), p_phase[q], ROLE_MMA, CF::B_PFULL + q);
-        if (r) r = wd.wait(BAR(CF::B_OREADY + q), p_phase[q], ROLE_MMA, CF::B_OREADY + q);
+        const bool r = wd.wait(BAR(CF::B_PFULL + q), p_phase[q], ROLE_MMA, CF::B_PFULL + q);
         p_phase[q] ^= 1;
         return r;
       };
@@ -739,6 +710,14 @@ cudaError_t launch_attn(const LaunchArgs &a) {
   auto kern = attn_fwd_kernel<D, DV, MODE, C_TMA>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_TOTAL);
   if (e != cudaSuccess) return e;
+  if constexpr (CF::SPLIT_REGS) {
+    // The per-warpgroup register budgets are granted out of the registers the block is
+    // launched with; refuse to launch if the compiled kernel was given fewer.
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, kern);
+    if (e != cudaSuccess) return e;
+    if (attr.numRegs * CF::THREADS < CF::REGS_NEEDED) return cudaErrorLaunchOutOfResources;
+  }
   const unsigned grid = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ctas_per_head);
   kern<<<grid, CF::THREADS, CF::SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmC, a.p);
   return cudaGetLastError();
