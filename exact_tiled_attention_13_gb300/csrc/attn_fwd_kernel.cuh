@@ -411,14 +411,15 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
         // No allowed key seen yet: every p is 0 and alpha is irrelevant; use 0 as reference.
         const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
         const float alpha = (m_new == m2) ? 1.0f : ex2_approx(m2 - m_use);
-        // o_t = alpha_t o_{t-1}, skipped when alpha is 1 for every row of the warp. The
-        // previous P V has completed (the S tile just read was committed after it). The
-        // 32-column chunks of o are loaded, scaled and stored between the quarters of
-        // the exponential loop, in the shadow of the exponential unit.
-        const bool rescale = it > sch.first_it(q) && __any_sync(0xFFFFFFFFu, alpha != 1.0f);
+        // o_t = alpha_t o_{t-1}. The previous P V has completed (the S tile just read was
+        // committed after it). The 32-column chunks of o are loaded, scaled and stored
+        // between the quarters of the exponential loop, in the shadow of the exponential
+        // unit. It runs on every tile: multiplying by alpha = 1 is exact, and costs less
+        // than a branch in the unrolled loop; on a query tile's first K/V tile o holds no
+        // result yet and is overwritten by the first P V, which does not accumulate.
         constexpr int OCH = DV / 32;  // chunks of o
         uint32_t o[32];
-        if (rescale) tmem_ld32(t_o, o);
+        tmem_ld32(t_o, o);
 
         // p_ij = exp(S_ij - m_t) as bf16 into tensor memory over S, 32 keys at a time;
         // the row sum runs alongside in four independent packed chains.
@@ -445,7 +446,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
             pk[16 * (qq & 1) + c2] = pack_bf16(p0, p1);
           }
           if (qq & 1) tmem_st32(t_s + 32 * (qq / 2), pk);
-          if (rescale && qq < OCH) {
+          if (qq < OCH) {
             tmem_wait_ld(o);
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
