@@ -10,13 +10,14 @@ from __future__ import annotations
 
 from ._lib import (ATTN_BIAS_DENSE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_INVALID_ARG,
                    ATTN_ERR_LAUNCH, ATTN_ERR_NO_DEVICE, ATTN_ERR_UNSUPPORTED,
-                   ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK,
-                   ATTN_OUT_BF16, ATTN_OUT_F32, AttnError, attn_device_status, attn_fwd_raw,
+                   ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_FAULT_NONE, ATTN_FAULT_SKIP_FIRST_K,
+                   ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK, ATTN_OUT_BF16, ATTN_OUT_F32,
+                   AttnError, attn_device_status, attn_fwd_raw, attn_set_fault_injection,
                    attn_set_wait_timeout_ns, attn_version, library_path, load, strerror)
 
 __all__ = [
     "attn_fwd", "attn_fwd_raw", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
-    "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
+    "attn_set_fault_injection", "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
     "ATTN_BIAS_DENSE", "ATTN_OUT_BF16", "ATTN_OUT_F32",
 ]
 

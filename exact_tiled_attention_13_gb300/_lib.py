@@ -22,6 +22,9 @@ ATTN_ERR_LAUNCH = -5
 ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_CUDA = -7
 
+ATTN_FAULT_NONE = 0
+ATTN_FAULT_SKIP_FIRST_K = 1
+
 # Every symbol include/attn.h declares, with its ctypes signature.
 _P = ctypes.c_void_p
 SIGNATURES = {
@@ -31,6 +34,7 @@ SIGNATURES = {
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
+    "attn_set_fault_injection": (ctypes.c_int, [ctypes.c_int]),
     "attn_version": (ctypes.c_int, []),
 }
 
@@ -88,6 +92,11 @@ def attn_device_status(stream=None):
 
 def attn_set_wait_timeout_ns(ns: int) -> int:
     return load().attn_set_wait_timeout_ns(int(ns))
+
+
+def attn_set_fault_injection(fault: int) -> int:
+    """Test hook of the watchdog (see include/attn.h); returns the library's code."""
+    return load().attn_set_fault_injection(int(fault))
 
 
 def attn_version() -> int:

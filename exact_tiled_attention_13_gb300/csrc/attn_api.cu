@@ -33,6 +33,7 @@ __device__ unsigned int g_watchdog = 0;
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_fault{FAULT_NONE};
 
 constexpr int kMaxDevices = 64;
 struct DeviceInfo {
@@ -164,6 +165,12 @@ extern "C" unsigned long long attn_set_wait_timeout_ns(unsigned long long ns) {
   return g_timeout_ns.exchange(ns == 0 ? kDefaultTimeoutNs : ns);
 }
 
+extern "C" int attn_set_fault_injection(int fault) {
+  if (fault != FAULT_NONE && fault != FAULT_SKIP_FIRST_K) return ATTN_ERR_INVALID_ARG;
+  g_fault.store(fault);
+  return ATTN_OK;
+}
+
 extern "C" int attn_fwd(const void *Q, const void *K, const void *V, int mode, const float *C,
                         int BH, int N, int d, int d_v, float scale, void *O, int out_dtype,
                         float *LSE, void *stream) {
@@ -231,6 +238,7 @@ extern "C" int attn_fwd(const void *Q, const void *K, const void *V, int mode, c
   a.p.C = C;
   a.p.status = watchdog;
   a.p.timeout_ns = g_timeout_ns.load();
+  a.p.fault = g_fault.load();
   a.stream = static_cast<cudaStream_t>(stream);
   if (static_cast<uint64_t>(BH) * a.p.ctas_per_head > 0x7FFFFFFFull) return ATTN_ERR_INVALID_ARG;
 

@@ -86,7 +86,11 @@ struct KernelParams {
   const float *C;           // dense bias, read directly when it cannot go through TMA
   unsigned int *status;     // watchdog word (device memory)
   unsigned long long timeout_ns;
+  int fault;                // test hook: FAULT_SKIP_FIRST_K makes a wait run out
 };
+
+// Test hook values (KernelParams::fault).
+enum { FAULT_NONE = 0, FAULT_SKIP_FIRST_K = 1 };
 
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int pow2_at_least(int x) {
@@ -618,30 +622,34 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
           tma_load_3d(sbase + CF::Q_OFF + q * CF::Q_TILE + kc * SW_CHUNK_BYTES, &tmQ,
                       kc * SW_CHUNK, sch.q_tile(q) * BM, sch.bh, BAR(CF::B_QFULL));
       // K runs ahead on its own ring; V has its own producer so neither blocks the other.
-      bool ok = true;
-      int k_issued = 0;
+      // last[s] is the last iteration whose copy was issued into slot s (-1: none).
+      int last[CF::KS];
+      for (int s = 0; s < CF::KS; ++s) last[s] = -1;
       for (int it = 0; it < sch.n_it; ++it) {
         const int j = sch.hi_max - it;
         const int ks = it % CF::KS;
-        ok = wd.wait1(BAR(CF::B_KEMPTY + ks), ((it / CF::KS) & 1) ^ 1, ROLE_LOAD, CF::B_KEMPTY + ks, false);
+        const bool ok =
+            wd.wait1(BAR(CF::B_KEMPTY + ks), ((it / CF::KS) & 1) ^ 1, ROLE_LOAD, CF::B_KEMPTY + ks, false);
         ETA_TRACE(30);
         if (!ok) break;
+        // Test hook: the first K tile is never copied, so its consumer's wait runs out.
+        if (p.fault == FAULT_SKIP_FIRST_K && it == 0) continue;
         mbar_arrive_expect_tx(BAR(CF::B_KFULL + ks), CF::K_TILE);
         for (int kc = 0; kc < D / SW_CHUNK; ++kc)
           tma_load_3d(sbase + CF::K_OFF + ks * CF::K_TILE + kc * SW_CHUNK_BYTES, &tmK,
                       kc * SW_CHUNK, j * BN, sch.bh, BAR(CF::B_KFULL + ks));
-        ++k_issued;
+        last[ks] = it;
       }
       // Wait for the last copy into each slot to land before the CTA may exit.
       wd.wait1(BAR(CF::B_QFULL), 0, ROLE_DRAIN, CF::B_QFULL, true);
-      for (int s = 0; s < CF::KS && s < k_issued; ++s) {
-        const int last = s + ((k_issued - 1 - s) / CF::KS) * CF::KS;
-        wd.wait1(BAR(CF::B_KFULL + s), (last / CF::KS) & 1, ROLE_DRAIN, CF::B_KFULL + s, true);
-      }
+      for (int s = 0; s < CF::KS; ++s)
+        if (last[s] >= 0)
+          wd.wait1(BAR(CF::B_KFULL + s), (last[s] / CF::KS) & 1, ROLE_DRAIN, CF::B_KFULL + s, true);
     } else if (warp == CF::VLOAD_WARP && lane == 0) {
       // ============================================================== TMA: V
       tma_prefetch_desc(&tmV);
-      int v_issued = 0;
+      int last[CF::VS];
+      for (int s = 0; s < CF::VS; ++s) last[s] = -1;
       for (int it = 0; it < sch.n_it; ++it) {
         const int j = sch.hi_max - it;
         const int vs = it % CF::VS;
@@ -653,24 +661,22 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
         for (int kc = 0; kc < DV / SW_CHUNK; ++kc)
           tma_load_3d(sbase + CF::V_OFF + vs * CF::V_TILE + kc * SW_CHUNK_BYTES, &tmV,
                       kc * SW_CHUNK, j * BN, sch.bh, BAR(CF::B_VFULL + vs));
-        ++v_issued;
+        last[vs] = it;
       }
-      for (int s = 0; s < CF::VS && s < v_issued; ++s) {
-        const int last = s + ((v_issued - 1 - s) / CF::VS) * CF::VS;
-        wd.wait1(BAR(CF::B_VFULL + s), (last / CF::VS) & 1, ROLE_DRAIN, CF::B_VFULL + s, true);
-      }
+      for (int s = 0; s < CF::VS; ++s)
+        if (last[s] >= 0)
+          wd.wait1(BAR(CF::B_VFULL + s), (last[s] / CF::VS) & 1, ROLE_DRAIN, CF::B_VFULL + s, true);
     } else if (warp == CF::CLOAD_WARP && lane == 0) {
       // ============================================================== TMA: dense bias
       if constexpr (CF::C_RING) {
         tma_prefetch_desc(&tmC);
-        int issued = 0;
+        int issued = 0;  // chunks issued, in ring order
         bool ok = true;
         for (int it = 0; ok && it < sch.n_it; ++it) {
           const int j = sch.hi_max - it;
           for (int cc = 0; cc < BN / CCHUNK; ++cc) {
-            const int pos = issued;
-            const int slot = pos % CF::CS;
-            ok = wd.wait1(BAR(CF::B_CEMPTY + slot), ((pos / CF::CS) & 1) ^ 1, ROLE_CLOAD,
+            const int slot = issued % CF::CS;
+            ok = wd.wait1(BAR(CF::B_CEMPTY + slot), ((issued / CF::CS) & 1) ^ 1, ROLE_CLOAD,
                           CF::B_CEMPTY + slot, false);
             if (!ok) break;
             mbar_arrive_expect_tx(BAR(CF::B_CFULL + slot), CCHUNK_BYTES);
@@ -679,9 +685,10 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
             ++issued;
           }
         }
+        // Chunks are issued consecutively, so the last fill of each slot follows from the count.
         for (int s = 0; s < CF::CS && s < issued; ++s) {
-          const int last = s + ((issued - 1 - s) / CF::CS) * CF::CS;
-          wd.wait1(BAR(CF::B_CFULL + s), (last / CF::CS) & 1, ROLE_DRAIN, CF::B_CFULL + s, true);
+          const int lastpos = s + ((issued - 1 - s) / CF::CS) * CF::CS;
+          wd.wait1(BAR(CF::B_CFULL + s), (lastpos / CF::CS) & 1, ROLE_DRAIN, CF::B_CFULL + s, true);
         }
       }
     }

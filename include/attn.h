@@ -116,6 +116,19 @@ ATTN_API int attn_device_status(void *stream, unsigned int *detail);
  */
 ATTN_API unsigned long long attn_set_wait_timeout_ns(unsigned long long ns);
 
+/*
+ * attn_set_fault_injection -- test hook for the watchdog (process-wide, for launches
+ * that follow). ATTN_FAULT_SKIP_FIRST_K makes each CTA's first K tile never be
+ * copied, so the wait on it runs out after the wait timeout: the kernel records the
+ * timeout in the watchdog word, every warp of the CTA stops waiting, copies already
+ * issued are drained, tensor memory is freed and the kernel returns. Outputs of such a
+ * launch are undefined. ATTN_FAULT_NONE (the default) turns it off.
+ * Returns ATTN_OK, or ATTN_ERR_INVALID_ARG for an unknown value.
+ */
+#define ATTN_FAULT_NONE 0
+#define ATTN_FAULT_SKIP_FIRST_K 1
+ATTN_API int attn_set_fault_injection(int fault);
+
 /* ABI version of this header (major * 100 + minor). */
 ATTN_API int attn_version(void);
 

@@ -115,3 +115,9 @@ def test_valid_call_without_gpu_reports_no_device():
     assert call() == eta.ATTN_ERR_NO_DEVICE
     code, word = eta.attn_device_status(None)
     assert code == eta.ATTN_ERR_NO_DEVICE and word == 0
+
+
+def test_fault_injection_setting():
+    assert eta.attn_set_fault_injection(eta.ATTN_FAULT_SKIP_FIRST_K) == eta.ATTN_OK
+    assert eta.attn_set_fault_injection(eta.ATTN_FAULT_NONE) == eta.ATTN_OK
+    assert eta.attn_set_fault_injection(7) == eta.ATTN_ERR_INVALID_ARG
