@@ -26,7 +26,7 @@ import threading
 
 import numpy as np
 
-MODE_NONE, MODE_CAUSAL, MODE_DENSE = 0, 1, 2
+MODE_NONE, MODE_CAUSAL, MODE_DENSE, MODE_KEY = 0, 1, 2, 4
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
@@ -72,6 +72,9 @@ def _bind(path: str):
     lib.oracle_attention.argtypes = [p, p, p, ctypes.c_int, p, i64, i64, i64, i64, dbl, p, i64,
                                      p, p, ctypes.c_int]
     lib.oracle_attention.restype = ctypes.c_int
+    lib.oracle_attention_ex.argtypes = [p, p, p, ctypes.c_int, p, p, i64, i64, i64, i64, i64, dbl,
+                                        p, i64, p, p, ctypes.c_int]
+    lib.oracle_attention_ex.restype = ctypes.c_int
     lib.oracle_attention_head.argtypes = [p, p, p, ctypes.c_int, p, i64, i64, i64, dbl, p, p,
                                           p, p]
     lib.oracle_attention_head.restype = ctypes.c_int
@@ -134,6 +137,42 @@ class Oracle:
         if rows is None:
             O = O.reshape(BH, N, dv)
             LSE = LSE.reshape(BH, N)
+        return O, LSE, used
+
+    def attention_ex(self, Q, K, V, mode, C, ckey, scale, rows=None, nthreads=0):
+        """Queries and keys of their own lengths; mode is a bit set of CAUSAL (key j >
+        i + Nk - Nq forbidden), DENSE (C fp32 [BH, Nq, Nk]) and KEY (ckey fp32 [BH, Nk]).
+        Q: bf16 bits [BH, Nq, d]; K: [BH, Nk, d]; V: [BH, Nk, dv]. Returns (O, LSE, threads)
+        shaped [BH, Nq, dv] / [BH, Nq], or [nrows, dv] / [nrows] for a row subset."""
+        Q, K, V = _bits(Q, 3), _bits(K, 3), _bits(V, 3)
+        BH, Nq, d = Q.shape
+        Nk, dv = K.shape[1], V.shape[2]
+        if K.shape != (BH, Nk, d) or V.shape[:2] != (BH, Nk):
+            raise ValueError("inconsistent Q/K/V shapes")
+        Cc = kk = None
+        if mode & MODE_DENSE:
+            Cc = np.ascontiguousarray(C, dtype=np.float32)
+            if Cc.shape != (BH, Nq, Nk):
+                raise ValueError("C must be [BH, Nq, Nk]")
+        if mode & MODE_KEY:
+            kk = np.ascontiguousarray(ckey, dtype=np.float32)
+            if kk.shape != (BH, Nk):
+                raise ValueError("ckey must be [BH, Nk]")
+        rows_arr = None
+        nrows = BH * Nq
+        if rows is not None:
+            rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+            nrows = rows_arr.size
+        O = np.empty((nrows, dv), dtype=np.float64)
+        LSE = np.empty(nrows, dtype=np.float64)
+        used = self.lib.oracle_attention_ex(_ptr(Q), _ptr(K), _ptr(V), int(mode), _ptr(Cc), _ptr(kk),
+                                            BH, Nq, Nk, d, dv, float(scale), _ptr(rows_arr), nrows,
+                                            _ptr(O), _ptr(LSE), int(nthreads))
+        if used < 0:
+            raise ValueError("oracle_attention_ex rejected its arguments")
+        if rows is None:
+            O = O.reshape(BH, Nq, dv)
+            LSE = LSE.reshape(BH, Nq)
         return O, LSE, used
 
     def attention_head(self, Q, K, V, mode, C, scale):
@@ -208,6 +247,10 @@ def default() -> Oracle:
 
 def attention(*args, **kwargs):
     return default().attention(*args, **kwargs)
+
+
+def attention_ex(*args, **kwargs):
+    return default().attention_ex(*args, **kwargs)
 
 
 def attention_head(*args, **kwargs):

@@ -20,8 +20,11 @@
  * Readings where the pages are silent:
  *   - A row with no allowed key is excluded by the pages' assumption; the oracle
  *     defines O_i = 0 and LSE_i = -inf for it instead of dividing 0 by 0.
- *   - Mask mode CAUSAL means C_ij = -inf for j > i and 0 otherwise (square, same
- *     indexing for queries and keys); NONE means C = 0; DENSE reads C[bh][i][j].
+ *   - The additive C is the sum of the terms the mode bits select: CAUSAL gives
+ *     -inf for key j > i + (Nk - Nq) and 0 otherwise (queries are the last Nq positions
+ *     of the key sequence; for Nq = Nk this is j > i with shared indexing); DENSE reads
+ *     C[bh][i][j]; KEY reads a per-key vector c[bh][j] (the same for every query row).
+ *     No bit set means C = 0.
  *
  * The second, test-only path is the pages' blockwise online recurrence (same
  * section, the display for b_t, m_t, alpha_t, l_t, o_t and O_i = o_T / l_T) and
@@ -38,7 +41,7 @@
 #include <string.h>
 #include <unistd.h>
 
-enum { ORACLE_NONE = 0, ORACLE_CAUSAL = 1, ORACLE_DENSE = 2 };
+enum { ORACLE_NONE = 0, ORACLE_CAUSAL = 1, ORACLE_DENSE = 2, ORACLE_KEY = 4 };
 
 /* Exact value of a bf16 bit pattern: the high half of an fp32. */
 static double bf16_value(uint16_t bits)
@@ -50,21 +53,25 @@ static double bf16_value(uint16_t bits)
 }
 
 typedef struct {
-    const uint16_t *Q, *K, *V; /* bf16 bits, [BH][N][d], [BH][N][d], [BH][N][dv] */
-    const float *C;            /* fp32 [BH][N][N] for DENSE, else unused */
-    int mode;
-    int64_t BH, N, d, dv;
+    const uint16_t *Q, *K, *V; /* bf16 bits, [BH][Nq][d], [BH][Nk][d], [BH][Nk][dv] */
+    const float *C;            /* fp32 [BH][Nq][Nk] when the DENSE bit is set */
+    const float *ckey;         /* fp32 [BH][Nk] when the KEY bit is set */
+    int mode;                  /* bit set of CAUSAL, DENSE, KEY */
+    int64_t BH, Nq, Nk, d, dv;
     double scale;
 } problem_t;
 
-/* C_ij of head bh under the problem's mask mode. */
+/* C_ij of head bh: the sum of the terms the mode bits select. */
 static double bias_value(const problem_t *p, int64_t bh, int64_t i, int64_t j)
 {
-    if (p->mode == ORACLE_CAUSAL)
-        return j > i ? -INFINITY : 0.0;
-    if (p->mode == ORACLE_DENSE)
-        return (double)p->C[(bh * p->N + i) * p->N + j];
-    return 0.0;
+    double c = 0.0;
+    if ((p->mode & ORACLE_CAUSAL) && j > i + (p->Nk - p->Nq))
+        return -INFINITY;
+    if (p->mode & ORACLE_DENSE)
+        c += (double)p->C[(bh * p->Nq + i) * p->Nk + j];
+    if (p->mode & ORACLE_KEY)
+        c += (double)p->ckey[bh * p->Nk + j];
+    return c;
 }
 
 /*
@@ -80,8 +87,8 @@ static double bias_value(const problem_t *p, int64_t bh, int64_t i, int64_t j)
 static void attention_row(const problem_t *p, int64_t bh, int64_t i, double *S_row,
                           double *P_row, double *O_row, double *lse)
 {
-    const int64_t N = p->N, d = p->d, dv = p->dv;
-    const uint16_t *q = p->Q + (bh * N + i) * d;
+    const int64_t N = p->Nk, d = p->d, dv = p->dv;
+    const uint16_t *q = p->Q + (bh * p->Nq + i) * d;
 
     for (int64_t j = 0; j < N; j++) {
         const uint16_t *k = p->K + (bh * N + j) * d;
@@ -137,8 +144,8 @@ static void *worker(void *arg)
 {
     job_t *job = (job_t *)arg;
     const problem_t *p = job->p;
-    double *S_row = (double *)malloc(sizeof(double) * (size_t)p->N);
-    double *P_row = (double *)malloc(sizeof(double) * (size_t)p->N);
+    double *S_row = (double *)malloc(sizeof(double) * (size_t)p->Nk);
+    double *P_row = (double *)malloc(sizeof(double) * (size_t)p->Nk);
     if (!S_row || !P_row) {
         free(S_row);
         free(P_row);
@@ -154,7 +161,7 @@ static void *worker(void *arg)
         int64_t end = r + 16 < job->nrows ? r + 16 : job->nrows;
         for (; r < end; r++) {
             int64_t flat = job->rows ? job->rows[r] : r;
-            int64_t bh = flat / p->N, i = flat % p->N;
+            int64_t bh = flat / p->Nq, i = flat % p->Nq;
             attention_row(p, bh, i, S_row, P_row, job->O + r * p->dv, job->LSE + r);
         }
     }
@@ -164,31 +171,36 @@ static void *worker(void *arg)
 }
 
 /*
- * Attention output rows by the definition.
- *   Q, K, V : bf16 bit patterns, row-major [BH][N][d], [BH][N][d], [BH][N][dv]
- *   C       : fp32 [BH][N][N] when mode == DENSE (may hold -inf), else ignored
- *   rows    : flat row ids (bh * N + i) to evaluate, or NULL for all BH * N rows
+ * Attention output rows by the definition, queries and keys of their own lengths.
+ *   Q       : bf16 bit patterns, row-major [BH][Nq][d]
+ *   K, V    : bf16 bit patterns, row-major [BH][Nk][d], [BH][Nk][dv]
+ *   mode    : bit set: 1 CAUSAL (key j > i + Nk - Nq forbidden), 2 DENSE, 4 KEY
+ *   C       : fp32 [BH][Nq][Nk] when DENSE is set (may hold -inf), else ignored
+ *   ckey    : fp32 [BH][Nk] when KEY is set (may hold -inf), else ignored
+ *   rows    : flat row ids (bh * Nq + i) to evaluate, or NULL for all BH * Nq rows
  *   O, LSE  : fp64 outputs, [nrows][dv] and [nrows], in the order of `rows`
  *   nthreads: worker threads; <= 0 means every online core
  * Returns the number of threads used, or -1 on bad arguments / allocation failure.
  */
-int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int mode,
-                     const float *C, int64_t BH, int64_t N, int64_t d, int64_t dv, double scale,
-                     const int64_t *rows, int64_t nrows, double *O, double *LSE, int nthreads)
+int oracle_attention_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int mode,
+                        const float *C, const float *ckey, int64_t BH, int64_t Nq, int64_t Nk,
+                        int64_t d, int64_t dv, double scale, const int64_t *rows, int64_t nrows,
+                        double *O, double *LSE, int nthreads)
 {
-    if (!Q || !K || !V || !O || !LSE || BH < 1 || N < 1 || d < 1 || dv < 1 || nrows < 0)
+    if (!Q || !K || !V || !O || !LSE || BH < 1 || Nq < 1 || Nk < 1 || d < 1 || dv < 1 ||
+        nrows < 0)
         return -1;
-    if (mode == ORACLE_DENSE && !C)
+    if (mode & ~(ORACLE_CAUSAL | ORACLE_DENSE | ORACLE_KEY))
         return -1;
-    if (mode != ORACLE_NONE && mode != ORACLE_CAUSAL && mode != ORACLE_DENSE)
+    if (((mode & ORACLE_DENSE) && !C) || ((mode & ORACLE_KEY) && !ckey))
         return -1;
     if (!rows)
-        nrows = BH * N;
+        nrows = BH * Nq;
     for (int64_t r = 0; rows && r < nrows; r++)
-        if (rows[r] < 0 || rows[r] >= BH * N)
+        if (rows[r] < 0 || rows[r] >= BH * Nq)
             return -1;
 
-    problem_t p = {Q, K, V, C, mode, BH, N, d, dv, scale};
+    problem_t p = {Q, K, V, C, ckey, mode, BH, Nq, Nk, d, dv, scale};
     job_t job;
     job.p = &p;
     job.rows = rows;
@@ -226,6 +238,17 @@ int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, in
     return failed ? -1 : (started > 0 ? started : 1);
 }
 
+/* The square problem (Nq = Nk = N) with mode NONE, CAUSAL or DENSE. */
+int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int mode,
+                     const float *C, int64_t BH, int64_t N, int64_t d, int64_t dv, double scale,
+                     const int64_t *rows, int64_t nrows, double *O, double *LSE, int nthreads)
+{
+    if (mode != ORACLE_NONE && mode != ORACLE_CAUSAL && mode != ORACLE_DENSE)
+        return -1;
+    return oracle_attention_ex(Q, K, V, mode, C, NULL, BH, N, N, d, dv, scale, rows, nrows, O,
+                               LSE, nthreads);
+}
+
 /*
  * The full score and probability matrices of one head (N x N each), with O and LSE,
  * by the same definition. For small N only: it materialises N^2 values twice.
@@ -238,7 +261,9 @@ int oracle_attention_head(const uint16_t *Q, const uint16_t *K, const uint16_t *
         return -1;
     if (mode == ORACLE_DENSE && !C)
         return -1;
-    problem_t p = {Q, K, V, C, mode, 1, N, d, dv, scale};
+    if (mode != ORACLE_NONE && mode != ORACLE_CAUSAL && mode != ORACLE_DENSE)
+        return -1;
+    problem_t p = {Q, K, V, C, NULL, mode, 1, N, N, d, dv, scale};
     for (int64_t i = 0; i < N; i++)
         attention_row(&p, 0, i, S + i * N, P + i * N, O + i * dv, LSE + i);
     return 0;

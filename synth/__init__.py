@@ -25,10 +25,12 @@ import os
 import numpy as np
 
 BASE_SEED = 20261202
-TENSOR_ID = {"Q": 0, "K": 1, "V": 2, "C": 3, "mask": 4}
+TENSOR_ID = {"Q": 0, "K": 1, "V": 2, "C": 3, "mask": 4, "ckey": 5}
 
-MODE_NONE, MODE_CAUSAL, MODE_DENSE = 0, 1, 2
-MODE_NAMES = {MODE_NONE: "none", MODE_CAUSAL: "causal", MODE_DENSE: "dense_bias"}
+MODE_NONE, MODE_CAUSAL, MODE_DENSE, MODE_KEY = 0, 1, 2, 4
+MODE_NAMES = {MODE_NONE: "none", MODE_CAUSAL: "causal", MODE_DENSE: "dense_bias",
+              MODE_KEY: "key_bias", MODE_CAUSAL | MODE_DENSE: "causal_dense_bias",
+              MODE_CAUSAL | MODE_KEY: "causal_key_bias"}
 
 _GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
@@ -166,17 +168,35 @@ def dense_bias(seed_c: int, seed_mask: int, BH: int, N: int, p_mask: float) -> n
     return C
 
 
+def key_bias(seed_c: int, seed_mask: int, BH: int, Nk: int, p_mask: float, std: float = 1.0) -> np.ndarray:
+    """fp32 per-key bias c[BH, Nk] ~ N(0, std^2) with key padding: each key is forbidden
+    (-inf) with probability p_mask; a head that lost every key gets key 0 back."""
+    c = normal_f32(seed_c, BH * Nk).reshape(BH, Nk)
+    if std != 1.0:
+        c = (c.astype(np.float64) * std).astype(np.float32)
+    if p_mask > 0.0:
+        masked = uniform01(seed_mask, 0, BH * Nk).reshape(BH, Nk) <= p_mask
+        for bh in range(BH):
+            if masked[bh].all():
+                masked[bh, 0] = False
+        c[masked] = -np.inf
+    return c
+
+
 def make_inputs(w: Workload, workload_id: int, base: int = BASE_SEED) -> dict:
     """Seeded inputs of workload `w`: Q, K, V as bf16 bit arrays, C fp32 or None."""
     BH, N = w.BH, w.N
     Q = bf16_tensor(seed_for(workload_id, "Q", base), (BH, N, w.d), w.qk_mult)
     K = bf16_tensor(seed_for(workload_id, "K", base), (BH, N, w.d), w.qk_mult)
     V = bf16_tensor(seed_for(workload_id, "V", base), (BH, N, w.dv))
-    C = None
-    if w.mode == MODE_DENSE:
+    C = ckey = None
+    if w.mode & MODE_DENSE:
         C = dense_bias(seed_for(workload_id, "C", base), seed_for(workload_id, "mask", base),
                        BH, N, w.p_mask)
-    return {"Q": Q, "K": K, "V": V, "C": C, "scale": w.scale, "mode": w.mode}
+    if w.mode & MODE_KEY:
+        ckey = key_bias(seed_for(workload_id, "ckey", base), seed_for(workload_id, "mask", base),
+                        BH, N, w.p_mask)
+    return {"Q": Q, "K": K, "V": V, "C": C, "ckey": ckey, "scale": w.scale, "mode": w.mode}
 
 
 def random_case(seed: int, BH: int, N: int, d: int, dv: int, mode: int, qk_mult: float = 1.0,
@@ -184,3 +204,22 @@ def random_case(seed: int, BH: int, N: int, d: int, dv: int, mode: int, qk_mult:
     """A seeded case of arbitrary shape (for parity tests at small and ragged sizes)."""
     w = Workload("case", 1, BH, N, d, dv, mode, "f32", qk_mult, p_mask)
     return make_inputs(w, 0, base=seed)
+
+
+def random_case_ex(seed: int, BH: int, Nq: int, Nk: int, d: int, dv: int, mode: int,
+                   qk_mult: float = 1.0, p_mask: float = 0.0) -> dict:
+    """A seeded case with Nq queries and Nk keys; C is [BH, Nq, Nk], ckey [BH, Nk]."""
+    Q = bf16_tensor(seed + TENSOR_ID["Q"], (BH, Nq, d), qk_mult)
+    K = bf16_tensor(seed + TENSOR_ID["K"], (BH, Nk, d), qk_mult)
+    V = bf16_tensor(seed + TENSOR_ID["V"], (BH, Nk, dv))
+    C = ckey = None
+    if mode & MODE_DENSE:
+        C = normal_f32(seed + TENSOR_ID["C"], BH * Nq * Nk).reshape(BH, Nq, Nk)
+        if p_mask > 0.0:
+            masked = uniform01(seed + TENSOR_ID["mask"], 0, BH * Nk).reshape(BH, Nk) <= p_mask
+            masked[:, 0] = False
+            C[np.broadcast_to(masked[:, None, :], C.shape)] = -np.inf
+    if mode & MODE_KEY:
+        ckey = key_bias(seed + TENSOR_ID["ckey"], seed + TENSOR_ID["mask"], BH, Nk, p_mask)
+    return {"Q": Q, "K": K, "V": V, "C": C, "ckey": ckey, "scale": 1.0 / math.sqrt(d),
+            "mode": mode}

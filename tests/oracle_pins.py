@@ -411,6 +411,122 @@ def pin_no_allowed_key(orc):
     assert np.isfinite(O).all() and np.isfinite(np.delete(L, 2)).all()
 
 
+# ------------------------------------------------------------------ rectangular and key bias
+def _case_ex(seed, BH, Nq, Nk, d, dv, mode, p_mask=0.0, qk_mult=1.0):
+    return synth.random_case_ex(seed, BH, Nq, Nk, d, dv, mode, qk_mult, p_mask)
+
+
+def pin_key_bias_is_a_broadcast_dense_bias(orc):
+    """A per-key bias c_j is the dense bias C_ij = c_j for every row: identical bits."""
+    for mode_extra in (0, CAUSAL):
+        c = _case_ex(171 + mode_extra, 2, 37, 37, 16, 8, synth.MODE_KEY | mode_extra, p_mask=0.3)
+        C = np.broadcast_to(c["ckey"][:, None, :], (2, 37, 37)).copy()
+        O1, L1, _ = orc.attention_ex(c["Q"], c["K"], c["V"], synth.MODE_KEY | mode_extra, None,
+                                     c["ckey"], c["scale"])
+        O2, L2, _ = orc.attention_ex(c["Q"], c["K"], c["V"], DENSE | mode_extra, C, None, c["scale"])
+        assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+
+
+def pin_rows_depend_only_on_their_query(orc):
+    """Without a causal mask, a problem holding any subset of a square problem's queries
+    (same keys, values and bias columns) returns exactly those rows."""
+    N = 29
+    c = _case_ex(181, 2, N, N, 16, 6, synth.MODE_KEY, p_mask=0.2)
+    O, L, _ = orc.attention_ex(c["Q"], c["K"], c["V"], synth.MODE_KEY, None, c["ckey"], c["scale"])
+    rows = np.array([3, 0, 17, 28, 9])
+    Os, Ls, _ = orc.attention_ex(np.ascontiguousarray(c["Q"][:, rows]), c["K"], c["V"],
+                                 synth.MODE_KEY, None, c["ckey"], c["scale"])
+    assert np.array_equal(Os, O[:, rows]) and np.array_equal(Ls, L[:, rows])
+
+
+def pin_causal_offset(orc):
+    """Causal with Nq != Nk aligns the last query with the last key: query i may see keys
+    j <= i + Nk - Nq. It equals a dense bias with that -inf pattern, and it reproduces the
+    square causal problem on the rows the two share."""
+    for Nq, Nk in ((13, 40), (40, 13), (1, 17), (25, 25)):
+        c = _case_ex(191 + Nq, 2, Nq, Nk, 16, 5, CAUSAL)
+        off = Nk - Nq
+        tri = np.where(np.arange(Nk)[None, :] > np.arange(Nq)[:, None] + off, -np.inf, 0.0)
+        C = np.broadcast_to(tri.astype(np.float32), (2, Nq, Nk)).copy()
+        O1, L1, _ = orc.attention_ex(c["Q"], c["K"], c["V"], CAUSAL, None, None, c["scale"])
+        O2, L2, _ = orc.attention_ex(c["Q"], c["K"], c["V"], DENSE, C, None, c["scale"])
+        assert np.array_equal(O1, O2) and np.array_equal(L1, L2), (Nq, Nk)
+        # Shared rows with the square causal problem over the same keys.
+        Qsq = synth.bf16_tensor(777 + Nq, (2, Nk, 16))
+        if Nq <= Nk:
+            Qsq[:, Nk - Nq:] = c["Q"]
+            Osq, Lsq, _ = orc.attention_ex(Qsq, c["K"], c["V"], CAUSAL, None, None, c["scale"])
+            assert np.array_equal(O1, Osq[:, Nk - Nq:]) and np.array_equal(L1, Lsq[:, Nk - Nq:])
+            # The last query sees every key: the unmasked result.
+            On, Ln, _ = orc.attention_ex(c["Q"], c["K"], c["V"], NONE, None, None, c["scale"])
+            assert np.array_equal(O1[:, -1], On[:, -1]) and np.array_equal(L1[:, -1], Ln[:, -1])
+        else:
+            # The first Nq - Nk queries have no allowed key: O = 0, LSE = -inf.
+            assert np.all(O1[:, :Nq - Nk] == 0.0) and np.all(np.isneginf(L1[:, :Nq - Nk]))
+            Osq, Lsq, _ = orc.attention_ex(np.ascontiguousarray(c["Q"][:, Nq - Nk:]), c["K"],
+                                           c["V"], CAUSAL, None, None, c["scale"])
+            assert np.array_equal(O1[:, Nq - Nk:], Osq) and np.array_equal(L1[:, Nq - Nk:], Lsq)
+
+
+def pin_bias_terms_add(orc):
+    """Causal with a dense bias is the dense bias plus the causal -inf pattern; a key bias
+    plus a dense bias is their sum (exact in fp64 for these fp32 values)."""
+    Nq, Nk = 21, 30
+    c = _case_ex(201, 2, Nq, Nk, 16, 4, CAUSAL | DENSE, p_mask=0.2)
+    off = Nk - Nq
+    tri = np.where(np.arange(Nk)[None, :] > np.arange(Nq)[:, None] + off, -np.inf, 0.0)
+    C2 = (c["C"] + tri[None].astype(np.float32)).astype(np.float32)
+    O1, L1, _ = orc.attention_ex(c["Q"], c["K"], c["V"], CAUSAL | DENSE, c["C"], None, c["scale"])
+    O2, L2, _ = orc.attention_ex(c["Q"], c["K"], c["V"], DENSE, C2, None, c["scale"])
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+    rng = np.random.default_rng(201)
+    ck = (np.round(rng.standard_normal((2, Nk)) * 8) / 8).astype(np.float32)
+    Cq = (np.round(rng.standard_normal((2, Nq, Nk)) * 8) / 8).astype(np.float32)
+    O3, L3, _ = orc.attention_ex(c["Q"], c["K"], c["V"], DENSE | synth.MODE_KEY, Cq, ck, c["scale"])
+    O4, L4, _ = orc.attention_ex(c["Q"], c["K"], c["V"], DENSE, (Cq + ck[:, None, :]).astype(np.float32),
+                                 None, c["scale"])
+    assert np.allclose(O3, O4, rtol=0, atol=1e-15) and np.allclose(L3, L4, rtol=0, atol=1e-14)
+
+
+def pin_bruteforce_rectangular(orc):
+    """Nq != Nk with causal, key and dense terms against 50-digit arithmetic."""
+    import mpmath
+
+    mpmath.mp.dps = 50
+    for seed, Nq, Nk, mode in [(211, 3, 7, CAUSAL | synth.MODE_KEY), (212, 6, 4, CAUSAL | DENSE),
+                               (213, 5, 8, synth.MODE_KEY), (214, 2, 9, CAUSAL)]:
+        c = _case_ex(seed, 1, Nq, Nk, 5, 3, mode, p_mask=0.3, qk_mult=2.0)
+        O, L, _ = orc.attention_ex(c["Q"], c["K"], c["V"], mode, c["C"], c["ckey"], c["scale"])
+        Qv, Kv, Vv = _vals(c["Q"][0]), _vals(c["K"][0]), _vals(c["V"][0])
+        for i in range(Nq):
+            w = []
+            for j in range(Nk):
+                if (mode & CAUSAL) and j > i + (Nk - Nq):
+                    w.append(mpmath.mpf(0))
+                    continue
+                sij = mpmath.mpf(c["scale"]) * mpmath.fsum(
+                    mpmath.mpf(float(Qv[i, k])) * mpmath.mpf(float(Kv[j, k])) for k in range(5))
+                if mode & DENSE:
+                    if np.isneginf(c["C"][0, i, j]):
+                        w.append(mpmath.mpf(0))
+                        continue
+                    sij += mpmath.mpf(float(c["C"][0, i, j]))
+                if mode & synth.MODE_KEY:
+                    if np.isneginf(c["ckey"][0, j]):
+                        w.append(mpmath.mpf(0))
+                        continue
+                    sij += mpmath.mpf(float(c["ckey"][0, j]))
+                w.append(mpmath.exp(sij))
+            tot = mpmath.fsum(w)
+            if tot == 0:
+                assert np.all(O[0, i] == 0.0) and np.isneginf(L[0, i])
+                continue
+            for col in range(3):
+                ref = mpmath.fsum(w[j] * mpmath.mpf(float(Vv[j, col])) for j in range(Nk)) / tot
+                assert abs(O[0, i, col] - float(ref)) <= 1e-13 * max(1.0, abs(float(ref))), (seed, i)
+            assert abs(L[0, i] - float(mpmath.log(tot))) <= 1e-13 * max(1.0, abs(float(mpmath.log(tot))))
+
+
 ALL_PINS = [
     pin_p_rows_sum_to_one,
     pin_constant_v,
@@ -429,4 +545,9 @@ ALL_PINS = [
     pin_key_permutation,
     pin_row_subset_and_threads,
     pin_no_allowed_key,
+    pin_key_bias_is_a_broadcast_dense_bias,
+    pin_rows_depend_only_on_their_query,
+    pin_causal_offset,
+    pin_bias_terms_add,
+    pin_bruteforce_rectangular,
 ]
