@@ -206,10 +206,11 @@ def recorded_traffic(workload_id: int):
 
 
 def workload_figures(w):
-    causal = w.mode == synth.MODE_CAUSAL
+    causal = bool(w.mode & synth.MODE_CAUSAL)
     F = accounting.flops(w.BH, w.N, w.d, w.dv, causal)
     B = accounting.required_bytes(w.BH, w.N, w.d, w.dv, 4 if w.out_dtype == "f32" else 2, lse=True,
-                                  dense_bias=w.mode == synth.MODE_DENSE)
+                                  dense_bias=bool(w.mode & synth.MODE_DENSE),
+                                  key_bias=bool(w.mode & synth.MODE_KEY))
     return F, B
 
 
@@ -233,8 +234,8 @@ def time_oracle(w, inputs, rows):
     import oracle
 
     t0 = time.perf_counter()
-    _, _, threads = oracle.attention(inputs["Q"], inputs["K"], inputs["V"], w.mode, inputs["C"],
-                                     w.scale, rows=rows)
+    _, _, threads = oracle.attention_ex(inputs["Q"], inputs["K"], inputs["V"], w.mode, inputs["C"],
+                                        inputs.get("ckey"), w.scale, rows=rows)
     return time.perf_counter() - t0, threads
 
 

@@ -8,17 +8,18 @@ computation runs in the library's kernel.
 """
 from __future__ import annotations
 
-from ._lib import (ATTN_BIAS_DENSE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_INVALID_ARG,
+from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_INVALID_ARG,
                    ATTN_ERR_LAUNCH, ATTN_ERR_NO_DEVICE, ATTN_ERR_UNSUPPORTED,
                    ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_FAULT_NONE, ATTN_FAULT_SKIP_FIRST_K,
                    ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK, ATTN_OUT_BF16, ATTN_OUT_F32,
-                   AttnError, attn_device_status, attn_fwd_raw, attn_set_fault_injection,
+                   AttnError, attn_device_status, attn_fwd_ex_raw, attn_fwd_raw,
+                   attn_set_fault_injection,
                    attn_set_wait_timeout_ns, attn_version, library_path, load, strerror)
 
 __all__ = [
-    "attn_fwd", "attn_fwd_raw", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
+    "attn_fwd", "attn_fwd_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
     "attn_set_fault_injection", "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
-    "ATTN_BIAS_DENSE", "ATTN_OUT_BF16", "ATTN_OUT_F32",
+    "ATTN_BIAS_DENSE", "ATTN_BIAS_KEY", "ATTN_OUT_BF16", "ATTN_OUT_F32",
 ]
 
 attn_strerror = strerror
@@ -70,4 +71,47 @@ def attn_fwd(Q, K, V, mode, C, scale, O, LSE=None, stream=None):
                         O.data_ptr(), out_dtype, lse_ptr, _stream_handle(stream))
     if code != ATTN_OK:
         raise AttnError(code, "attn_fwd")
+    return O, LSE
+
+
+def attn_fwd_ex(Q, K, V, mode, C, ckey, scale, O, LSE=None, stream=None):
+    """attn_fwd with Nq queries and Nk keys and the per-key bias term, through the C ABI.
+
+    Q: bf16 [BH, Nq, d]; K: bf16 [BH, Nk, d]; V: bf16 [BH, Nk, d_v]; mode: bit set of
+    ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, ATTN_BIAS_KEY; C: fp32 [BH, Nq, Nk] or None;
+    ckey: fp32 [BH, Nk] or None; O: bf16/fp32 [BH, Nq, d_v]; LSE: fp32 [BH, Nq] or None.
+    """
+    import torch
+
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if Q.dtype != torch.bfloat16 or K.dtype != torch.bfloat16 or V.dtype != torch.bfloat16:
+        raise ValueError("Q, K and V must be bf16")
+    if Q.dim() != 3 or K.dim() != 3 or V.dim() != 3:
+        raise ValueError("expected Q [BH, Nq, d], K [BH, Nk, d], V [BH, Nk, d_v]")
+    BH, Nq, d = Q.shape
+    Nk, dv = K.shape[1], V.shape[2]
+    if tuple(K.shape) != (BH, Nk, d) or tuple(V.shape[:2]) != (BH, Nk):
+        raise ValueError("inconsistent Q, K, V shapes")
+    if tuple(O.shape) != (BH, Nq, dv) or O.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("O must be bf16 or fp32 [BH, Nq, d_v]")
+    out_dtype = ATTN_OUT_F32 if O.dtype == torch.float32 else ATTN_OUT_BF16
+    c_ptr = k_ptr = lse_ptr = None
+    if C is not None:
+        if C.dtype != torch.float32 or tuple(C.shape) != (BH, Nq, Nk) or not C.is_contiguous():
+            raise ValueError("C must be a contiguous fp32 [BH, Nq, Nk] tensor")
+        c_ptr = C.data_ptr()
+    if ckey is not None:
+        if ckey.dtype != torch.float32 or tuple(ckey.shape) != (BH, Nk) or not ckey.is_contiguous():
+            raise ValueError("ckey must be a contiguous fp32 [BH, Nk] tensor")
+        k_ptr = ckey.data_ptr()
+    if LSE is not None:
+        if LSE.dtype != torch.float32 or tuple(LSE.shape) != (BH, Nq) or not LSE.is_contiguous():
+            raise ValueError("LSE must be a contiguous fp32 [BH, Nq] tensor")
+        lse_ptr = LSE.data_ptr()
+    code = attn_fwd_ex_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), mode, c_ptr, k_ptr, BH, Nq, Nk,
+                           d, dv, scale, O.data_ptr(), out_dtype, lse_ptr, _stream_handle(stream))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd_ex")
     return O, LSE

@@ -10,6 +10,7 @@ from . import _build
 ATTN_MASK_NONE = 0
 ATTN_MASK_CAUSAL = 1
 ATTN_BIAS_DENSE = 2
+ATTN_BIAS_KEY = 4
 ATTN_OUT_BF16 = 0
 ATTN_OUT_F32 = 1
 
@@ -31,6 +32,9 @@ SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_float, _P, ctypes.c_int, _P,
                                 _P]),
+    "attn_fwd_ex": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int,
+                                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P,
+                                   ctypes.c_int, _P, _P]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
@@ -81,6 +85,13 @@ def attn_fwd_raw(Q, K, V, mode, C, BH, N, d, d_v, scale, O, out_dtype, LSE, stre
     """The C entry point with plain integers as pointers; returns its code unchanged."""
     return load().attn_fwd(Q, K, V, int(mode), C, int(BH), int(N), int(d), int(d_v), float(scale), O,
                            int(out_dtype), LSE, stream)
+
+
+def attn_fwd_ex_raw(Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, O, out_dtype, LSE,
+                    stream) -> int:
+    """attn_fwd_ex with plain integers as pointers; returns its code unchanged."""
+    return load().attn_fwd_ex(Q, K, V, int(mode), C, ckey, int(BH), int(Nq), int(Nk), int(d),
+                              int(d_v), float(scale), O, int(out_dtype), LSE, stream)
 
 
 def attn_device_status(stream=None):

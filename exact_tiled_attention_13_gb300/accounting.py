@@ -27,13 +27,16 @@ def flops(BH: int, N: int, d: int, dv: int, causal: bool) -> float:
 
 
 def required_bytes(BH: int, N: int, d: int, dv: int, out_bytes: int, lse: bool = True,
-                   dense_bias: bool = False) -> int:
-    """Bytes of reading Q, K, V (bf16) and C (fp32, dense mode) once and writing O and LSE once."""
+                   dense_bias: bool = False, key_bias: bool = False) -> int:
+    """Bytes of reading Q, K, V (bf16) and the bias (fp32 C [N, N] or vector [N]) once and
+    writing O and LSE once."""
     b = BH * N * (d + d + dv) * BF16 + BH * N * dv * out_bytes
     if lse:
         b += BH * N * F32
     if dense_bias:
         b += BH * N * N * F32
+    if key_bias:
+        b += BH * N * F32
     return b
 
 

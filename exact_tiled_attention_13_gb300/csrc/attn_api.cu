@@ -16,16 +16,18 @@
 namespace eta {
 
 // Instantiated in the attn_inst_*.cu translation units.
-#define ETA_DECLARE(D, DV)                                                   \
-  extern template cudaError_t launch_attn<D, DV, MODE_NONE, false>(const LaunchArgs &);   \
-  extern template cudaError_t launch_attn<D, DV, MODE_CAUSAL, false>(const LaunchArgs &); \
-  extern template cudaError_t launch_attn<D, DV, MODE_DENSE, true>(const LaunchArgs &);   \
-  extern template cudaError_t launch_attn<D, DV, MODE_DENSE, false>(const LaunchArgs &);
+#define ETA_DECLARE_C(D, DV, C)                                                          \
+  extern template cudaError_t launch_attn<D, DV, C, BIAS_NONE>(const LaunchArgs &);         \
+  extern template cudaError_t launch_attn<D, DV, C, BIAS_DENSE_TMA>(const LaunchArgs &);    \
+  extern template cudaError_t launch_attn<D, DV, C, BIAS_DENSE_DIRECT>(const LaunchArgs &); \
+  extern template cudaError_t launch_attn<D, DV, C, BIAS_KEY>(const LaunchArgs &);
+#define ETA_DECLARE(D, DV) ETA_DECLARE_C(D, DV, false) ETA_DECLARE_C(D, DV, true)
 ETA_DECLARE(64, 64)
 ETA_DECLARE(64, 128)
 ETA_DECLARE(128, 64)
 ETA_DECLARE(128, 128)
 #undef ETA_DECLARE
+#undef ETA_DECLARE_C
 
 namespace {
 
@@ -133,11 +135,18 @@ int encode_3d(CUtensorMap *map, CUtensorMapDataType type, size_t elem, const voi
   return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+template <int D, int DV, bool C>
+cudaError_t dispatch_bias(int bias, const LaunchArgs &a) {
+  switch (bias) {
+    case BIAS_DENSE_TMA: return launch_attn<D, DV, C, BIAS_DENSE_TMA>(a);
+    case BIAS_DENSE_DIRECT: return launch_attn<D, DV, C, BIAS_DENSE_DIRECT>(a);
+    case BIAS_KEY: return launch_attn<D, DV, C, BIAS_KEY>(a);
+    default: return launch_attn<D, DV, C, BIAS_NONE>(a);
+  }
+}
 template <int D, int DV>
-cudaError_t dispatch_mode(int mode, bool c_tma, const LaunchArgs &a) {
-  if (mode == MODE_NONE) return launch_attn<D, DV, MODE_NONE, false>(a);
-  if (mode == MODE_CAUSAL) return launch_attn<D, DV, MODE_CAUSAL, false>(a);
-  return c_tma ? launch_attn<D, DV, MODE_DENSE, true>(a) : launch_attn<D, DV, MODE_DENSE, false>(a);
+cudaError_t dispatch(bool causal, int bias, const LaunchArgs &a) {
+  return causal ? dispatch_bias<D, DV, true>(bias, a) : dispatch_bias<D, DV, false>(bias, a);
 }
 
 }  // namespace
@@ -171,31 +180,35 @@ extern "C" int attn_set_fault_injection(int fault) {
   return ATTN_OK;
 }
 
-extern "C" int attn_fwd(const void *Q, const void *K, const void *V, int mode, const float *C,
-                        int BH, int N, int d, int d_v, float scale, void *O, int out_dtype,
-                        float *LSE, void *stream) {
+extern "C" int attn_fwd_ex(const void *Q, const void *K, const void *V, int mode, const float *C,
+                           const float *ckey, int BH, int Nq, int Nk, int d, int d_v, float scale,
+                           void *O, int out_dtype, float *LSE, void *stream) {
   // ---- arguments (no CUDA call before these pass)
-  if (mode != ATTN_MASK_NONE && mode != ATTN_MASK_CAUSAL && mode != ATTN_BIAS_DENSE)
-    return ATTN_ERR_INVALID_ARG;
+  if (mode & ~(ATTN_MASK_CAUSAL | ATTN_BIAS_DENSE | ATTN_BIAS_KEY)) return ATTN_ERR_INVALID_ARG;
+  const bool causal = (mode & ATTN_MASK_CAUSAL) != 0;
+  const bool dense = (mode & ATTN_BIAS_DENSE) != 0;
+  const bool key = (mode & ATTN_BIAS_KEY) != 0;
+  if (dense && key) return ATTN_ERR_INVALID_ARG;
   if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
-  if (BH < 1 || N < 0) return ATTN_ERR_INVALID_ARG;
+  if (BH < 1 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if ((d != 64 && d != 128) || (d_v != 64 && d_v != 128)) return ATTN_ERR_UNSUPPORTED;
-  if (N == 0) return ATTN_OK;  // empty buffers may be null
+  if (Nq == 0) return ATTN_OK;  // empty buffers may be null
+  if (Nk == 0) return ATTN_ERR_INVALID_ARG;  // every row would lack an allowed key
   if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
-  if ((mode == ATTN_BIAS_DENSE) != (C != nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (dense != (C != nullptr) || key != (ckey != nullptr)) return ATTN_ERR_INVALID_ARG;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
-      (C && !aligned(C, 16)) || (LSE && !aligned(LSE, 4)))
+      (C && !aligned(C, 16)) || (ckey && !aligned(ckey, 4)) || (LSE && !aligned(LSE, 4)))
     return ATTN_ERR_INVALID_ARG;
 
-  const size_t rows = static_cast<size_t>(BH) * static_cast<size_t>(N);
-  const size_t o_bytes = rows * d_v * (out_dtype == ATTN_OUT_F32 ? 4 : 2);
-  const size_t lse_bytes = LSE ? rows * 4 : 0;
-  const size_t qk_bytes = rows * d * 2, v_bytes = rows * d_v * 2;
-  const size_t c_bytes = C ? rows * static_cast<size_t>(N) * 4 : 0;
-  const void *ins[4] = {Q, K, V, C};
-  const size_t in_bytes[4] = {qk_bytes, qk_bytes, v_bytes, c_bytes};
-  for (int i = 0; i < 4; ++i) {
+  const size_t qrows = static_cast<size_t>(BH) * static_cast<size_t>(Nq);
+  const size_t krows = static_cast<size_t>(BH) * static_cast<size_t>(Nk);
+  const size_t o_bytes = qrows * d_v * (out_dtype == ATTN_OUT_F32 ? 4 : 2);
+  const size_t lse_bytes = LSE ? qrows * 4 : 0;
+  const void *ins[5] = {Q, K, V, C, ckey};
+  const size_t in_bytes[5] = {qrows * d * 2, krows * d * 2, krows * d_v * 2,
+                              C ? qrows * static_cast<size_t>(Nk) * 4 : 0, ckey ? krows * 4 : 0};
+  for (int i = 0; i < 5; ++i) {
     if (ranges_overlap(O, o_bytes, ins[i], in_bytes[i]) || ranges_overlap(LSE, lse_bytes, ins[i], in_bytes[i]))
       return ATTN_ERR_INVALID_ARG;
   }
@@ -206,36 +219,43 @@ extern "C" int attn_fwd(const void *Q, const void *K, const void *V, int mode, c
   unsigned int *watchdog = nullptr;
   int rc = current_device(&dev, &watchdog);
   if (rc != ATTN_OK) return rc;
-  const void *ptrs[6] = {Q, K, V, O, C, LSE};
+  const void *ptrs[7] = {Q, K, V, O, C, ckey, LSE};
   for (const void *ptr : ptrs)
     if (ptr && device_pointer_ok(ptr, dev) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
   if ((rc = get_encoder()) != ATTN_OK) return rc;
 
   LaunchArgs a;
   std::memset(&a, 0, sizeof(a));
-  const uint64_t n = static_cast<uint64_t>(N), bh = static_cast<uint64_t>(BH);
-  if (encode_3d(&a.tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, d, n, bh, SW_CHUNK, BM) != ATTN_OK ||
-      encode_3d(&a.tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, d, n, bh, SW_CHUNK, BN) != ATTN_OK ||
-      encode_3d(&a.tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, V, d_v, n, bh, SW_CHUNK, BN) != ATTN_OK)
+  const uint64_t nq = static_cast<uint64_t>(Nq), nk = static_cast<uint64_t>(Nk),
+                 bh = static_cast<uint64_t>(BH);
+  if (encode_3d(&a.tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, d, nq, bh, SW_CHUNK, BM) != ATTN_OK ||
+      encode_3d(&a.tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, d, nk, bh, SW_CHUNK, BN) != ATTN_OK ||
+      encode_3d(&a.tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, V, d_v, nk, bh, SW_CHUNK, BN) != ATTN_OK)
     return ATTN_ERR_CUDA;
   // The dense bias goes through TMA when its rows are 16-byte multiples; otherwise the
   // softmax warps read it directly.
-  const bool c_tma = (mode == ATTN_BIAS_DENSE) && (N % 4 == 0);
-  if (c_tma &&
-      encode_3d(&a.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, n, n, bh, CCHUNK, BM) != ATTN_OK)
+  int bias = BIAS_NONE;
+  if (dense) bias = (Nk % 4 == 0) ? BIAS_DENSE_TMA : BIAS_DENSE_DIRECT;
+  if (key) bias = BIAS_KEY;
+  if (bias == BIAS_DENSE_TMA &&
+      encode_3d(&a.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, nk, nq, bh, CCHUNK, BM) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
-  const int tiles = (N + BN - 1) / BN;
-  const int nq = q_tiles_per_cta(mode);
+  const int nq_tiles = (Nq + BM - 1) / BM;
+  const int nqc = q_tiles_per_cta(bias);
   a.p.BH = BH;
-  a.p.N = N;
-  a.p.num_tiles = tiles;
-  a.p.ctas_per_head = (tiles + nq - 1) / nq;
+  a.p.Nq = Nq;
+  a.p.Nk = Nk;
+  a.p.nq_tiles = nq_tiles;
+  a.p.nkv_tiles = (Nk + BN - 1) / BN;
+  a.p.causal_off = Nk - Nq;
+  a.p.ctas_per_head = (nq_tiles + nqc - 1) / nqc;
   a.p.scale_log2 = scale * LOG2E;
   a.p.out_f32 = out_dtype == ATTN_OUT_F32 ? 1 : 0;
   a.p.O = O;
   a.p.LSE = LSE;
   a.p.C = C;
+  a.p.ckey = ckey;
   a.p.status = watchdog;
   a.p.timeout_ns = g_timeout_ns.load();
   a.p.fault = g_fault.load();
@@ -243,15 +263,22 @@ extern "C" int attn_fwd(const void *Q, const void *K, const void *V, int mode, c
   if (static_cast<uint64_t>(BH) * a.p.ctas_per_head > 0x7FFFFFFFull) return ATTN_ERR_INVALID_ARG;
 
   cudaError_t e;
-  if (d == 64 && d_v == 64) e = dispatch_mode<64, 64>(mode, c_tma, a);
-  else if (d == 64) e = dispatch_mode<64, 128>(mode, c_tma, a);
-  else if (d_v == 64) e = dispatch_mode<128, 64>(mode, c_tma, a);
-  else e = dispatch_mode<128, 128>(mode, c_tma, a);
+  if (d == 64 && d_v == 64) e = dispatch<64, 64>(causal, bias, a);
+  else if (d == 64) e = dispatch<64, 128>(causal, bias, a);
+  else if (d_v == 64) e = dispatch<128, 64>(causal, bias, a);
+  else e = dispatch<128, 128>(causal, bias, a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;
   }
   return ATTN_OK;
+}
+
+extern "C" int attn_fwd(const void *Q, const void *K, const void *V, int mode, const float *C,
+                        int BH, int N, int d, int d_v, float scale, void *O, int out_dtype,
+                        float *LSE, void *stream) {
+  if (mode & ATTN_BIAS_KEY) return ATTN_ERR_INVALID_ARG;  // the per-key vector needs attn_fwd_ex
+  return attn_fwd_ex(Q, K, V, mode, C, nullptr, BH, N, N, d, d_v, scale, O, out_dtype, LSE, stream);
 }
 
 extern "C" int attn_device_status(void *stream, unsigned int *detail) {

@@ -37,13 +37,15 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "ptx.cuh"
 
 namespace eta {
 
-enum { MODE_NONE = 0, MODE_CAUSAL = 1, MODE_DENSE = 2 };
+// Bias source of a kernel instance (the causal mask is a separate template flag).
+enum { BIAS_NONE = 0, BIAS_DENSE_TMA = 1, BIAS_DENSE_DIRECT = 2, BIAS_KEY = 3 };
 
 // Phase trace (diagnostics only; compiled in with -DETA_PHASE_TRACE): lane 0 of every
 // warp of the first ETA_TRACE_CTAS CTAs appends (clock64 << 8 | event) records.
@@ -76,14 +78,17 @@ constexpr float LN2 = 0.6931471805599453f;
 
 struct KernelParams {
   int BH;
-  int N;
-  int num_tiles;      // ceil(N / 128): number of Q tiles and of K/V tiles per head
-  int ctas_per_head;  // ceil(num_tiles / NQ)
+  int Nq, Nk;         // queries and keys per head
+  int nq_tiles;       // ceil(Nq / 128)
+  int nkv_tiles;      // ceil(Nk / 128)
+  int causal_off;     // Nk - Nq: query i may see keys j <= i + causal_off
+  int ctas_per_head;  // ceil(nq_tiles / NQ)
   float scale_log2;   // scale * log2(e)
   int out_f32;        // O element type: 1 fp32, 0 bf16
   void *O;
   float *LSE;
-  const float *C;           // dense bias, read directly when it cannot go through TMA
+  const float *C;           // dense bias [BH][Nq][Nk], read directly when it cannot go through TMA
+  const float *ckey;        // per-key bias [BH][Nk]
   unsigned int *status;     // watchdog word (device memory)
   unsigned long long timeout_ns;
   int fault;                // test hook: FAULT_SKIP_FIRST_K makes a wait run out
@@ -99,17 +104,20 @@ constexpr int pow2_at_least(int x) {
   return p;
 }
 
-template <int D, int DV, int MODE, bool C_TMA>
+template <int D, int DV, bool CAUSAL, int BIAS>
 struct Cfg {
   static_assert(D == 64 || D == 128, "d must be 64 or 128");
   static_assert(DV == 64 || DV == 128, "d_v must be 64 or 128");
-  static constexpr bool DENSE = MODE == MODE_DENSE;
-  static constexpr bool C_RING = DENSE && C_TMA;
+  static constexpr bool DENSE = BIAS == BIAS_DENSE_TMA || BIAS == BIAS_DENSE_DIRECT;
+  static constexpr bool C_RING = BIAS == BIAS_DENSE_TMA;
+  static constexpr bool KEY = BIAS == BIAS_KEY;
+  static constexpr bool BIASED = DENSE || KEY;  // scores carry an additive bias
   static constexpr int NQ = DENSE ? 1 : 2;
   static constexpr int Q_TILE = BM * D * 2;
   static constexpr int K_TILE = BN * D * 2;
   static constexpr int V_TILE = BN * DV * 2;
-  static constexpr int BUDGET = 224 * 1024;
+  static constexpr int KB = KEY ? 4 : 0;  // per-key bias ring: 128 fp32 per K/V tile
+  static constexpr int BUDGET = 224 * 1024 - KB * BN * 4;
   static constexpr int KV_PAIRS = cmin(4, (BUDGET - NQ * Q_TILE) / (K_TILE + V_TILE));
   static constexpr int KS = DENSE ? 2 : cmin(4, KV_PAIRS + ((BUDGET - NQ * Q_TILE - KV_PAIRS * (K_TILE + V_TILE)) >= K_TILE ? 1 : 0));
   static constexpr int VS = DENSE ? 2 : KV_PAIRS;
@@ -121,7 +129,8 @@ struct Cfg {
   static constexpr int K_OFF = Q_OFF + NQ * Q_TILE;
   static constexpr int V_OFF = K_OFF + KS * K_TILE;
   static constexpr int C_OFF = V_OFF + VS * V_TILE;
-  static constexpr int BAR_OFF = C_OFF + CS * CCHUNK_BYTES;
+  static constexpr int KB_OFF = C_OFF + CS * CCHUNK_BYTES;
+  static constexpr int BAR_OFF = KB_OFF + KB * BN * 4;
   // barrier indices
   static constexpr int B_QFULL = 0;
   static constexpr int B_KFULL = 1;
@@ -130,7 +139,9 @@ struct Cfg {
   static constexpr int B_VEMPTY = B_VFULL + VS;
   static constexpr int B_CFULL = B_VEMPTY + VS;
   static constexpr int B_CEMPTY = B_CFULL + CS;
-  static constexpr int B_SFULL = B_CEMPTY + CS;   // S_q ready (and the previous P_q V done)
+  static constexpr int B_KBFULL = B_CEMPTY + CS;
+  static constexpr int B_KBEMPTY = B_KBFULL + KB;
+  static constexpr int B_SFULL = B_KBEMPTY + KB;  // S_q ready (and the previous P_q V done)
   static constexpr int B_PFULL = B_SFULL + NQ;    // P_q written and o_q rescaled
   static constexpr int B_OFULL = B_PFULL + NQ;    // last P_q V done
   static constexpr int B_DRAIN = B_OFULL + NQ;
@@ -150,7 +161,7 @@ struct Cfg {
   static constexpr int MMA_WARP = CTRL_WARP0;
   static constexpr int LOAD_WARP = CTRL_WARP0 + 1;   // Q and K
   static constexpr int VLOAD_WARP = CTRL_WARP0 + 2;  // V
-  static constexpr int CLOAD_WARP = CTRL_WARP0 + 3;  // dense bias
+  static constexpr int CLOAD_WARP = CTRL_WARP0 + 3;  // dense or per-key bias
   static constexpr int NUM_WARPS = 4 * NQ + 4;
   static constexpr int THREADS = 32 * NUM_WARPS;
   // Register budgets per warpgroup (setmaxnreg, two query tiles only): the softmax
@@ -181,14 +192,20 @@ struct Cfg {
 enum { ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_CLOAD = 4, ROLE_DRAIN = 5 };
 
 struct Watchdog {
-  volatile int *abort_flag;
-  unsigned int *status;
-  unsigned long long timeout_ns;
+  // The abort flag lives in shared memory; the status word and the timeout are read from
+  // the kernel parameters only on the slow path, so the common case holds one register.
+  uint32_t abort_addr;
+  const KernelParams &p;
 
+  __device__ bool aborted() const {
+    int v;
+    asm volatile("ld.volatile.shared.b32 %0, [%1];" : "=r"(v) : "r"(abort_addr) : "memory");
+    return v != 0;
+  }
   __device__ void trip(int role, int bar) {
-    *abort_flag = 1;
-    atomicCAS(status, 0u, 0x80000000u | (static_cast<unsigned>(role) << 24) |
-                              (static_cast<unsigned>(bar & 0xFFFF) << 8));
+    asm volatile("st.volatile.shared.b32 [%0], %1;" ::"r"(abort_addr), "r"(1) : "memory");
+    atomicCAS(p.status, 0u, 0x80000000u | (static_cast<unsigned>(role) << 24) |
+                                (static_cast<unsigned>(bar & 0xFFFF) << 8));
   }
 
   // Bounded wait of one thread; false on timeout or when another role aborted.
@@ -198,8 +215,8 @@ struct Watchdog {
     for (uint32_t spin = 1;; ++spin) {
       if (mbar_try_wait(bar_addr, parity)) return true;
       if ((spin & 15u) == 0) {
-        if (!drain && *abort_flag) return false;
-        if (global_timer_ns() - t0 > timeout_ns) {
+        if (!drain && aborted()) return false;
+        if (global_timer_ns() - t0 > p.timeout_ns) {
           trip(drain ? ROLE_DRAIN : role, bar);
           return false;
         }
@@ -222,25 +239,41 @@ struct Watchdog {
 
 // Per-CTA schedule: which query tiles it owns and which K/V tiles each one visits.
 // Iteration `it` visits K/V tile j = hi_max - it; query tile q takes part in
-// iterations [first_it[q], n_it), i.e. K/V tiles hi_q down to 0.
-template <int NQ, int MODE>
+// iterations [first_it(q), n_it), i.e. K/V tiles hi(q) down to 0. With a causal mask
+// a query tile's last K/V tile is the one holding the last key its last row may see;
+// a query tile whose rows may see no key at all (Nq > Nk) takes part in none.
+__device__ __forceinline__ int floor_div(int a, int b) { return a >= 0 ? a / b : -((b - 1 - a) / b); }
+
+template <int NQ, bool CAUSAL>
 struct Schedule {
+  static_assert(NQ == 1 || NQ == 2, "one or two query tiles per CTA");
   int bh, cta_q, n_exist, hi_max, n_it;
+  int nkv, off;
+  int first0, first1;  // first_it of query tiles 0 and 1
 
   __device__ Schedule(const KernelParams &p) {
     bh = blockIdx.x / p.ctas_per_head;
     // Within a head, the CTA with the most causal work starts first.
     cta_q = p.ctas_per_head - 1 - static_cast<int>(blockIdx.x % p.ctas_per_head);
-    n_exist = cmin(NQ, p.num_tiles - cta_q * NQ);
-    hi_max = (MODE == MODE_CAUSAL) ? cta_q * NQ + n_exist - 1 : p.num_tiles - 1;
-    n_it = hi_max + 1;
-  }
-  // First iteration query tile q takes part in; n_it when the tile does not exist.
-  __device__ int first_it(int q) const {
-    const int hi_q = (MODE == MODE_CAUSAL) ? cta_q * NQ + q : hi_max;
-    return (q < n_exist) ? hi_max - hi_q : n_it;
+    n_exist = cmin(NQ, p.nq_tiles - cta_q * NQ);
+    nkv = p.nkv_tiles;
+    off = p.causal_off;
+    const int hi0 = hi(p.Nq, 0);
+    const int hi1 = NQ == 2 ? hi(p.Nq, 1) : -1;
+    hi_max = n_exist == 2 ? hi1 : hi0;  // hi grows with the query tile
+    n_it = hi_max >= 0 ? hi_max + 1 : 0;
+    first0 = hi0 >= 0 ? hi_max - hi0 : n_it;
+    first1 = (n_exist == 2 && hi1 >= 0) ? hi_max - hi1 : n_it;
   }
   __device__ int q_tile(int q) const { return cta_q * NQ + q; }
+  // Last K/V tile query tile q visits (negative: none).
+  __device__ int hi(int nq, int q) const {
+    if (!CAUSAL) return nkv - 1;
+    const int last_row = cmin(q_tile(q) * BM + BM - 1, nq - 1);
+    return cmin(floor_div(last_row + off, BN), nkv - 1);
+  }
+  // First iteration query tile q takes part in; n_it when it takes part in none.
+  __device__ int first_it(int q) const { return q == 0 ? first0 : first1; }
 };
 
 // Row maximum of 128 values with eight independent three-input max chains.
@@ -256,12 +289,12 @@ __device__ __forceinline__ float row_max128(const float (&x)[BN]) {
   return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
 }
 
-template <int D, int DV, int MODE, bool C_TMA>
-__global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
+template <int D, int DV, bool CAUSAL, int BIAS>
+__global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
-                    const KernelParams p) {
-  using CF = Cfg<D, DV, MODE, C_TMA>;
+                    const __grid_constant__ KernelParams p) {
+  using CF = Cfg<D, DV, CAUSAL, BIAS>;
   constexpr int NQ = CF::NQ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -277,8 +310,8 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
 #ifdef ETA_PHASE_TRACE
   int trace_n = 0;
 #endif
-  const Schedule<NQ, MODE> sch(p);
-  Watchdog wd{abort_flag, p.status, p.timeout_ns};
+  const Schedule<NQ, CAUSAL> sch(p);
+  Watchdog wd{sbase + CF::ABORT_OFF, p};
 
   // ------------------------------------------------------------------ set-up
   if (threadIdx.x == 0) {
@@ -294,6 +327,15 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
     for (int s = 0; s < CF::CS; ++s) {
       mbar_init(BAR(CF::B_CFULL + s), 1);
       mbar_init(BAR(CF::B_CEMPTY + s), 4);  // one arrival per softmax warp
+    }
+    if constexpr (CF::KEY) {
+      // Every softmax warpgroup that visits any K/V tile releases every slot once.
+      int consumers = 0;
+      for (int q = 0; q < NQ; ++q) consumers += sch.first_it(q) < sch.n_it ? 4 : 0;
+      for (int s = 0; s < CF::KB; ++s) {
+        mbar_init(BAR(CF::B_KBFULL + s), 1);
+        mbar_init(BAR(CF::B_KBEMPTY + s), consumers > 0 ? consumers : 1);
+      }
     }
     for (int q = 0; q < NQ; ++q) {
       mbar_init(BAR(CF::B_SFULL + q), 1);
@@ -324,13 +366,28 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
     const int qt = sch.q_tile(q);
     const int q_row = qt * BM + row;
     const bool exists = q < sch.n_exist;
+    const bool has_keys = sch.first_it(q) < sch.n_it;  // some K/V tile is visible to this tile
     const float sl2 = p.scale_log2;
     float m2 = -INFINITY;  // running max m_t, in log2(e)-scaled units
     float l = 0.0f;        // running sum l_t
     uint32_t s_phase = 0;
     bool ok = true;
     int cpos = 0;  // dense-bias ring position
-    if (exists) {
+    if constexpr (CF::KEY) {
+      // Per-key bias slots of iterations this query tile skips are released at once.
+      if (has_keys)
+        for (int it = 0; it < sch.first_it(q); ++it) {
+          __syncwarp();
+          mbar_arrive_elect(BAR(CF::B_KBEMPTY + it % CF::KB));
+        }
+    }
+    // Tiles j >= j_mask need an elementwise mask: those that reach past the causal limit
+    // of the tile's first row, and the last tile when Nk is not a multiple of 128. lim is
+    // the last key this row may see (the causal limit i + (Nk - Nq), or the last key).
+    int j_mask = CAUSAL ? floor_div(qt * BM + sch.off + 1, BN) : INT_MAX;
+    if (p.Nk % BN != 0) j_mask = cmin(j_mask, sch.nkv - 1);
+    const int lim = CAUSAL ? cmin(q_row + sch.off, p.Nk - 1) : p.Nk - 1;
+    if (exists && has_keys) {
       for (int it = sch.first_it(q); it < sch.n_it; ++it) {
         const int j = sch.hi_max - it;
         ok = wd.wait(BAR(CF::B_SFULL + q), s_phase, ROLE_SOFTMAX, CF::B_SFULL + q);
@@ -361,7 +418,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
 
         if constexpr (CF::DENSE) {
           // x = (scale * S + C) * log2(e): the bias joins after the scaling, unscaled.
-          if constexpr (C_TMA) {
+          if constexpr (CF::C_RING) {
 #pragma unroll
             for (int cc = 0; cc < BN / CCHUNK; ++cc) {
               const int slot = cpos % CF::CS;
@@ -386,32 +443,47 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
             }
             if (!ok) break;
           } else {
-            const bool row_ok = q_row < p.N;
-            const float *crow = p.C + (static_cast<size_t>(sch.bh) * p.N + (row_ok ? q_row : 0)) *
-                                          static_cast<size_t>(p.N);
+            const bool row_ok = q_row < p.Nq;
+            const float *crow = p.C + (static_cast<size_t>(sch.bh) * p.Nq + (row_ok ? q_row : 0)) *
+                                          static_cast<size_t>(p.Nk);
 #pragma unroll
             for (int c = 0; c < BN; ++c) {
               const int kv = j * BN + c;
-              const float cv = (row_ok && kv < p.N) ? __ldg(crow + kv) : 0.0f;
+              const float cv = (row_ok && kv < p.Nk) ? __ldg(crow + kv) : 0.0f;
               x[c] = fmaf(x[c], sl2, cv * LOG2E);
             }
           }
         }
-
-        // Forbidden keys: above the causal diagonal, and past the end of the sequence.
-        const bool diag = (MODE == MODE_CAUSAL) && (j == qt);
-        const bool tail = (j == p.num_tiles - 1) && (p.N % BN != 0);
-        if (diag || tail) {
+        if constexpr (CF::KEY) {
+          // x = (scale * S + c_j) * log2(e), c_j the same for every row: broadcast reads.
+          const int slot = it % CF::KB;
+          ok = wd.wait(BAR(CF::B_KBFULL + slot), (it / CF::KB) & 1, ROLE_SOFTMAX, CF::B_KBFULL + slot);
+          if (!ok) break;
+          const float4 *kb = reinterpret_cast<const float4 *>(smem + CF::KB_OFF + slot * BN * 4);
 #pragma unroll
-          for (int c = 0; c < BN; ++c) {
-            const int kv = j * BN + c;
-            if ((diag && kv > q_row) || kv >= p.N) x[c] = -INFINITY;
+          for (int u = 0; u < BN / 4; ++u) {
+            const float4 cv = kb[u];
+            float b0, b1, b2, b3;
+            mul2(b0, b1, cv.x, cv.y, LOG2E, LOG2E);
+            mul2(b2, b3, cv.z, cv.w, LOG2E, LOG2E);
+            fma2(x[4 * u + 0], x[4 * u + 1], x[4 * u + 0], x[4 * u + 1], sl2, sl2, b0, b1);
+            fma2(x[4 * u + 2], x[4 * u + 3], x[4 * u + 2], x[4 * u + 3], sl2, sl2, b2, b3);
           }
+          __syncwarp();
+          mbar_arrive_elect(BAR(CF::B_KBEMPTY + slot));
+        }
+
+        // Forbidden keys: past the causal limit, and past the end of the keys.
+        if (j >= j_mask) {
+          const int lim_j = lim - j * BN;
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c > lim_j) x[c] = -INFINITY;
         }
 
         // b_t and m_t = max(m_{t-1}, b_t); alpha_t = exp(m_{t-1} - m_t).
         const float b = row_max128(x);
-        const float m_new = CF::DENSE ? fmaxf(m2, b) : fmaxf(m2, b * sl2);
+        const float m_new = CF::BIASED ? fmaxf(m2, b) : fmaxf(m2, b * sl2);
         // No allowed key seen yet: every p is 0 and alpha is irrelevant; use 0 as reference.
         const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
         const float alpha = (m_new == m2) ? 1.0f : ex2_approx(m2 - m_use);
@@ -438,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
           for (int c2 = 0; c2 < 16; ++c2) {
             const int c = 32 * qq + 2 * c2;
             float a0, a1;
-            if constexpr (CF::DENSE) {
+            if constexpr (CF::BIASED) {
               add2(a0, a1, x[c], x[c + 1], neg_m, neg_m);
             } else {
               fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg_m, neg_m);
@@ -478,19 +550,28 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
         m2 = m_new;
       }
 
-      // ------------------------------------------------ epilogue: O = o_T / l_T, LSE
-      if (ok) ok = wd.wait(BAR(CF::B_OFULL + q), 0, ROLE_SOFTMAX, CF::B_OFULL + q);
+    }
+    // ------------------------------------------------ epilogue: O = o_T / l_T, LSE
+    // A query tile that may see no key (Nq > Nk with a causal mask) has no o: its rows
+    // get the defined result of a row without an allowed key, O = 0 and LSE = -inf.
+    if (exists && ok) {
+      if (has_keys) ok = wd.wait(BAR(CF::B_OFULL + q), 0, ROLE_SOFTMAX, CF::B_OFULL + q);
       ETA_TRACE(6);
       if (ok) {
-        tc_fence_after();
-        const bool row_ok = q_row < p.N;
+        if (has_keys) tc_fence_after();
+        const bool row_ok = q_row < p.Nq;
         const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;  // no allowed key: O = 0
-        const size_t orow = (static_cast<size_t>(sch.bh) * p.N + (row_ok ? q_row : 0)) * DV;
+        const size_t orow = (static_cast<size_t>(sch.bh) * p.Nq + (row_ok ? q_row : 0)) * DV;
 #pragma unroll
         for (int cc = 0; cc < DV / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(t_o + 32 * cc, o);
-          tmem_wait_ld(o);
+          if (has_keys) {
+            tmem_ld32(t_o + 32 * cc, o);
+            tmem_wait_ld(o);
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) o[c] = 0u;
+          }
           float f[32];
 #pragma unroll
           for (int c = 0; c < 32; c += 2)
@@ -517,7 +598,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
         }
         if (row_ok && p.LSE != nullptr) {
           // LSE_i = m_i + ln l_i, from the log2-scaled running max.
-          p.LSE[static_cast<size_t>(sch.bh) * p.N + q_row] =
+          p.LSE[static_cast<size_t>(sch.bh) * p.Nq + q_row] =
               (l > 0.0f) ? (m2 + lg2_approx(l)) * LN2 : -INFINITY;
         }
       }
@@ -593,7 +674,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
         mma_commit_elect(BAR(CF::B_KEMPTY + kslot));
         if (it > 0) mma_commit_elect(BAR(CF::B_VEMPTY + vprev));
       }
-      if (ok) {
+      if (ok && sch.n_it > 0) {
         const int last = sch.n_it - 1;
         const int vslot = last % CF::VS;
         ok = wd.wait(BAR(CF::B_VFULL + vslot), (last / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
@@ -666,29 +747,53 @@ __global__ void __launch_bounds__(Cfg<D, DV, MODE, C_TMA>::THREADS, 1)
       for (int s = 0; s < CF::VS; ++s)
         if (last[s] >= 0)
           wd.wait1(BAR(CF::B_VFULL + s), (last[s] / CF::VS) & 1, ROLE_DRAIN, CF::B_VFULL + s, true);
-    } else if (warp == CF::CLOAD_WARP && lane == 0) {
-      // ============================================================== TMA: dense bias
+    } else if (warp == CF::CLOAD_WARP) {
       if constexpr (CF::C_RING) {
-        tma_prefetch_desc(&tmC);
-        int issued = 0;  // chunks issued, in ring order
-        bool ok = true;
-        for (int it = 0; ok && it < sch.n_it; ++it) {
-          const int j = sch.hi_max - it;
-          for (int cc = 0; cc < BN / CCHUNK; ++cc) {
-            const int slot = issued % CF::CS;
-            ok = wd.wait1(BAR(CF::B_CEMPTY + slot), ((issued / CF::CS) & 1) ^ 1, ROLE_CLOAD,
-                          CF::B_CEMPTY + slot, false);
-            if (!ok) break;
-            mbar_arrive_expect_tx(BAR(CF::B_CFULL + slot), CCHUNK_BYTES);
-            tma_load_3d(sbase + CF::C_OFF + slot * CCHUNK_BYTES, &tmC, j * BN + cc * CCHUNK,
-                        sch.q_tile(0) * BM, sch.bh, BAR(CF::B_CFULL + slot));
-            ++issued;
+        // ============================================================ TMA: dense bias
+        if (lane == 0) {
+          tma_prefetch_desc(&tmC);
+          int issued = 0;  // chunks issued, in ring order
+          bool ok = true;
+          for (int it = 0; ok && it < sch.n_it; ++it) {
+            const int j = sch.hi_max - it;
+            for (int cc = 0; cc < BN / CCHUNK; ++cc) {
+              const int slot = issued % CF::CS;
+              ok = wd.wait1(BAR(CF::B_CEMPTY + slot), ((issued / CF::CS) & 1) ^ 1, ROLE_CLOAD,
+                            CF::B_CEMPTY + slot, false);
+              if (!ok) break;
+              mbar_arrive_expect_tx(BAR(CF::B_CFULL + slot), CCHUNK_BYTES);
+              tma_load_3d(sbase + CF::C_OFF + slot * CCHUNK_BYTES, &tmC, j * BN + cc * CCHUNK,
+                          sch.q_tile(0) * BM, sch.bh, BAR(CF::B_CFULL + slot));
+              ++issued;
+            }
+          }
+          // Chunks are issued consecutively: the last fill of each slot follows from the count.
+          for (int s = 0; s < CF::CS && s < issued; ++s) {
+            const int lastpos = s + ((issued - 1 - s) / CF::CS) * CF::CS;
+            wd.wait1(BAR(CF::B_CFULL + s), (lastpos / CF::CS) & 1, ROLE_DRAIN, CF::B_CFULL + s, true);
           }
         }
-        // Chunks are issued consecutively, so the last fill of each slot follows from the count.
-        for (int s = 0; s < CF::CS && s < issued; ++s) {
-          const int lastpos = s + ((issued - 1 - s) / CF::CS) * CF::CS;
-          wd.wait1(BAR(CF::B_CFULL + s), (lastpos / CF::CS) & 1, ROLE_DRAIN, CF::B_CFULL + s, true);
+      } else if constexpr (CF::KEY) {
+        // ============================================================ per-key bias
+        // The whole warp copies the 128 biases of each K/V tile (4 per lane, zero past
+        // the last key) into the next slot of a small ring; every softmax warp that
+        // visits the tile releases the slot.
+        for (int it = 0; it < sch.n_it; ++it) {
+          const int j = sch.hi_max - it;
+          const int slot = it % CF::KB;
+          if (!wd.wait(BAR(CF::B_KBEMPTY + slot), ((it / CF::KB) & 1) ^ 1, ROLE_CLOAD,
+                       CF::B_KBEMPTY + slot))
+            break;
+          const int k0 = j * BN + 4 * lane;
+          const float *src = p.ckey + static_cast<size_t>(sch.bh) * p.Nk;
+          float4 v;
+          v.x = (k0 + 0 < p.Nk) ? __ldg(src + k0 + 0) : 0.0f;
+          v.y = (k0 + 1 < p.Nk) ? __ldg(src + k0 + 1) : 0.0f;
+          v.z = (k0 + 2 < p.Nk) ? __ldg(src + k0 + 2) : 0.0f;
+          v.w = (k0 + 3 < p.Nk) ? __ldg(src + k0 + 3) : 0.0f;
+          reinterpret_cast<float4 *>(smem + CF::KB_OFF + slot * BN * 4)[lane] = v;
+          __syncwarp();
+          mbar_arrive_elect(BAR(CF::B_KBFULL + slot));
         }
       }
     }
@@ -709,13 +814,15 @@ struct LaunchArgs {
   cudaStream_t stream;
 };
 
-// Number of query tiles one CTA owns for a given mode (the host sizes the grid with it).
-constexpr int q_tiles_per_cta(int mode) { return mode == MODE_DENSE ? 1 : 2; }
+// Number of query tiles one CTA owns (the host sizes the grid with it).
+constexpr int q_tiles_per_cta(int bias) {
+  return (bias == BIAS_DENSE_TMA || bias == BIAS_DENSE_DIRECT) ? 1 : 2;
+}
 
-template <int D, int DV, int MODE, bool C_TMA>
+template <int D, int DV, bool CAUSAL, int BIAS>
 cudaError_t launch_attn(const LaunchArgs &a) {
-  using CF = Cfg<D, DV, MODE, C_TMA>;
-  auto kern = attn_fwd_kernel<D, DV, MODE, C_TMA>;
+  using CF = Cfg<D, DV, CAUSAL, BIAS>;
+  auto kern = attn_fwd_kernel<D, DV, CAUSAL, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_TOTAL);
   if (e != cudaSuccess) return e;
   if constexpr (CF::SPLIT_REGS) {

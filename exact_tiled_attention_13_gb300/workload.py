@@ -42,10 +42,12 @@ class DeviceWorkload:
         self.K_h = pinned(self.host["K"].view(np.int16), torch.bfloat16)
         self.V_h = pinned(self.host["V"].view(np.int16), torch.bfloat16)
         self.C_h = None if self.host["C"] is None else pinned(self.host["C"], None)
+        self.ck_h = None if self.host.get("ckey") is None else pinned(self.host["ckey"], None)
         self.Q = self.Q_h.to(device)
         self.K = self.K_h.to(device)
         self.V = self.V_h.to(device)
         self.C = None if self.C_h is None else self.C_h.to(device)
+        self.ckey = None if self.ck_h is None else self.ck_h.to(device)
         odt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
         self.O = torch.empty(w.BH, w.N, w.dv, dtype=odt, device=device)
         self.LSE = torch.empty(w.BH, w.N, dtype=torch.float32, device=device)
@@ -55,12 +57,14 @@ class DeviceWorkload:
     def launch(self, stream=None):
         import exact_tiled_attention_13_gb300 as eta
 
-        eta.attn_fwd(self.Q, self.K, self.V, self.w.mode, self.C, self.w.scale, self.O, self.LSE,
-                     stream=stream)
+        eta.attn_fwd_ex(self.Q, self.K, self.V, self.w.mode, self.C, self.ckey, self.w.scale,
+                        self.O, self.LSE, stream=stream)
 
     def h2d_bytes(self) -> int:
         n = sum(t.numel() * t.element_size() for t in (self.Q_h, self.K_h, self.V_h))
-        return n + (0 if self.C_h is None else self.C_h.numel() * self.C_h.element_size())
+        for t in (self.C_h, self.ck_h):
+            n += 0 if t is None else t.numel() * t.element_size()
+        return n
 
     def d2h_bytes(self) -> int:
         return self.O.numel() * self.O.element_size() + self.LSE.numel() * 4
@@ -74,15 +78,17 @@ class DeviceWorkload:
         self.V.copy_(self.V_h, non_blocking=True)
         if self.C is not None:
             self.C.copy_(self.C_h, non_blocking=True)
-        eta.attn_fwd(self.Q, self.K, self.V, self.w.mode, self.C, self.w.scale, self.O, self.LSE,
-                     stream=stream)
+        if self.ckey is not None:
+            self.ckey.copy_(self.ck_h, non_blocking=True)
+        eta.attn_fwd_ex(self.Q, self.K, self.V, self.w.mode, self.C, self.ckey, self.w.scale,
+                        self.O, self.LSE, stream=stream)
         self.O_h.copy_(self.O, non_blocking=True)
         self.LSE_h.copy_(self.LSE, non_blocking=True)
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args(argv)
     import torch

@@ -38,10 +38,12 @@
 extern "C" {
 #endif
 
-/* Mask / bias modes (argument `mode`). */
-#define ATTN_MASK_NONE 0  /* C = 0 */
-#define ATTN_MASK_CAUSAL 1 /* C_ij = -inf for key j > query i, else 0 (square, shared indexing) */
-#define ATTN_BIAS_DENSE 2 /* C read from a dense fp32 [BH][N][N] array */
+/* Mask / bias terms (argument `mode`, a bit set; C is the sum of the selected terms). */
+#define ATTN_MASK_NONE 0   /* C = 0 */
+#define ATTN_MASK_CAUSAL 1 /* -inf for key j > query i + (Nk - Nq), else 0 (Nq = Nk: j > i) */
+#define ATTN_BIAS_DENSE 2  /* a dense fp32 [BH][Nq][Nk] array C */
+#define ATTN_BIAS_KEY 4    /* a per-key fp32 [BH][Nk] vector c, the same for every query row
+                              (attn_fwd_ex only; key padding is c_j = -inf) */
 
 /* Output element types (argument `out_dtype`). */
 #define ATTN_OUT_BF16 0
@@ -64,8 +66,9 @@ extern "C" {
  *   Q     bf16, contiguous row-major [BH][N][d]      queries
  *   K     bf16, contiguous row-major [BH][N][d]      keys
  *   V     bf16, contiguous row-major [BH][N][d_v]    values
- *   mode  ATTN_MASK_NONE, ATTN_MASK_CAUSAL or ATTN_BIAS_DENSE
- *   C     fp32, contiguous row-major [BH][N][N] when mode == ATTN_BIAS_DENSE, else NULL.
+ *   mode  ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, or
+ *         ATTN_MASK_CAUSAL | ATTN_BIAS_DENSE (causal mask and dense bias together)
+ *   C     fp32, contiguous row-major [BH][N][N] when mode has ATTN_BIAS_DENSE, else NULL.
  *         Entries are finite or -inf; C is added after the scaling and is not scaled.
  *   BH    number of heads (batch times heads), >= 1
  *   N     sequence length (queries = keys), >= 0; N == 0 is a successful no-op in which
@@ -94,6 +97,24 @@ extern "C" {
  */
 ATTN_API int attn_fwd(const void *Q, const void *K, const void *V, int mode, const float *C, int BH, int N,
              int d, int d_v, float scale, void *O, int out_dtype, float *LSE, void *stream);
+
+/*
+ * attn_fwd_ex -- the same operation with Nq queries and Nk keys per head, and the
+ * per-key bias term. Everything not listed here is as for attn_fwd.
+ *   Q     bf16 [BH][Nq][d];  K bf16 [BH][Nk][d];  V bf16 [BH][Nk][d_v]
+ *   mode  bit set of ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, ATTN_BIAS_KEY (DENSE and KEY
+ *         together are rejected: add the vector into C instead)
+ *   C     fp32 [BH][Nq][Nk] with ATTN_BIAS_DENSE, else NULL
+ *   ckey  fp32 [BH][Nk] with ATTN_BIAS_KEY, else NULL; 4-byte aligned; finite or -inf
+ *   Nq    >= 0 (0: no-op); Nk >= 1 when Nq >= 1
+ *   O     [BH][Nq][d_v];  LSE fp32 [BH][Nq] or NULL
+ * The causal mask aligns the last query with the last key: query i may see keys
+ * j <= i + (Nk - Nq). With Nq > Nk the first Nq - Nk queries see no key and get the
+ * defined result O_i = 0, LSE_i = -inf.
+ */
+ATTN_API int attn_fwd_ex(const void *Q, const void *K, const void *V, int mode, const float *C,
+                         const float *ckey, int BH, int Nq, int Nk, int d, int d_v, float scale,
+                         void *O, int out_dtype, float *LSE, void *stream);
 
 /* Static English text for a return code (never NULL). */
 ATTN_API const char *attn_strerror(int code);

@@ -134,6 +134,10 @@ WORKLOADS = {
                 p_mask=0.3),
     5: Workload("b1h16_n16384_d128_nomask_qk_x4", 1, 16, 16384, 128, 128, MODE_NONE, "f32",
                 qk_mult=4.0),
+    # Workload 4's key padding as a per-key vector (bias c_j ~ N(0,1), -inf with p = 0.3)
+    # instead of a dense N x N array.
+    6: Workload("b1h8_n4096_d64_dv128_key_bias_keypad", 1, 8, 4096, 64, 128, MODE_KEY, "f32",
+                p_mask=0.3),
 }
 
 

@@ -47,7 +47,11 @@ def run_gpu(case, out_f32=True, stream=None, with_lse=True, fill=float("nan"), d
     O = torch.full((BH, N, dv), fill, dtype=torch.float32 if out_f32 else torch.bfloat16,
                    device=Q.device)
     LSE = torch.full((BH, N), fill, dtype=torch.float32, device=Q.device) if with_lse else None
-    eta.attn_fwd(Q, K, V, case["mode"], C, case["scale"], O, LSE, stream=stream)
+    if case.get("ckey") is None:
+        eta.attn_fwd(Q, K, V, case["mode"], C, case["scale"], O, LSE, stream=stream)
+    else:
+        ckey = torch.from_numpy(np.ascontiguousarray(case["ckey"])).to(Q.device)
+        eta.attn_fwd_ex(Q, K, V, case["mode"], C, ckey, case["scale"], O, LSE, stream=stream)
     torch.cuda.synchronize()
     code, word = eta.attn_device_status(None)
     assert code == eta.ATTN_OK, f"device watchdog tripped: {word:#x}"

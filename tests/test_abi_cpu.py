@@ -121,3 +121,37 @@ def test_fault_injection_setting():
     assert eta.attn_set_fault_injection(eta.ATTN_FAULT_SKIP_FIRST_K) == eta.ATTN_OK
     assert eta.attn_set_fault_injection(eta.ATTN_FAULT_NONE) == eta.ATTN_OK
     assert eta.attn_set_fault_injection(7) == eta.ATTN_ERR_INVALID_ARG
+
+
+KP = 0x700000
+GOOD_EX = dict(Q=QP, K=KP, V=VP, mode=0, C=None, ckey=None, BH=2, Nq=48, Nk=64, d=64, d_v=64,
+               scale=0.125, O=OP, out_dtype=1, LSE=LP, stream=None)
+
+
+def call_ex(**over):
+    a = dict(GOOD_EX)
+    a.update(over)
+    return eta.attn_fwd_ex_raw(a["Q"], a["K"], a["V"], a["mode"], a["C"], a["ckey"], a["BH"],
+                               a["Nq"], a["Nk"], a["d"], a["d_v"], a["scale"], a["O"],
+                               a["out_dtype"], a["LSE"], a["stream"])
+
+
+@pytest.mark.parametrize("over", [
+    dict(mode=8), dict(mode=6, C=CP, ckey=KP), dict(mode=4, ckey=None), dict(mode=0, ckey=KP),
+    dict(mode=5, ckey=KP + 2), dict(Nk=0), dict(Nq=-1), dict(Nk=-3), dict(mode=2, C=None),
+    dict(O=KP), dict(LSE=KP + 128),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_invalid_arguments_ex(over):
+    assert call_ex(**over) == eta.ATTN_ERR_INVALID_ARG
+
+
+def test_ex_zero_queries_is_noop_and_key_mode_needs_ex():
+    assert call_ex(Nq=0, Q=None, K=None, V=None, O=None, LSE=None) == eta.ATTN_OK
+    # attn_fwd has no per-key vector argument.
+    assert call(mode=4) == eta.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
+def test_valid_ex_call_without_gpu_reports_no_device():
+    assert call_ex() == eta.ATTN_ERR_NO_DEVICE
+    assert call_ex(mode=5, ckey=KP) == eta.ATTN_ERR_NO_DEVICE

@@ -1,0 +1,84 @@
+"""attn_fwd_ex on the GPU against the oracle: queries and keys of their own lengths,
+the causal mask aligned at the last key (both signs of Nk - Nq), the per-key bias
+vector (aligned and ragged), and the causal mask combined with a bias."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_helpers import compare
+
+pytestmark = pytest.mark.gpu
+
+NONE, CAUSAL, DENSE, KEY = synth.MODE_NONE, synth.MODE_CAUSAL, synth.MODE_DENSE, synth.MODE_KEY
+
+# (BH, Nq, Nk, d, dv, mode, out_f32, p_mask)
+CASES = [
+    (2, 100, 300, 64, 64, CAUSAL, True, 0.0),
+    (1, 300, 100, 128, 128, CAUSAL, True, 0.0),
+    (2, 256, 640, 128, 128, CAUSAL, False, 0.0),
+    (1, 1, 1000, 128, 128, NONE, True, 0.0),
+    (3, 1, 700, 64, 128, CAUSAL, True, 0.0),
+    (1, 7, 513, 64, 128, CAUSAL | KEY, True, 0.3),
+    (2, 384, 384, 128, 128, KEY, True, 0.3),
+    (1, 129, 257, 64, 64, KEY, False, 0.5),
+    (1, 200, 200, 64, 128, CAUSAL | DENSE, True, 0.3),
+    (1, 130, 131, 128, 64, CAUSAL | DENSE, True, 0.2),
+    (2, 512, 256, 128, 128, NONE, True, 0.0),
+    (1, 1000, 2000, 128, 128, CAUSAL | KEY, False, 0.3),
+    (1, 640, 384, 64, 64, CAUSAL | KEY, True, 0.2),
+]
+
+
+def _id(c):
+    BH, Nq, Nk, d, dv, mode, f32, pm = c
+    return f"bh{BH}-nq{Nq}-nk{Nk}-d{d}-dv{dv}-{synth.MODE_NAMES[mode]}-{'f32' if f32 else 'bf16'}"
+
+
+def run_ex(c, out_f32=True):
+    import torch
+
+    import exact_tiled_attention_13_gb300 as eta
+
+    def dev_bits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    Q, K, V = dev_bits(c["Q"]), dev_bits(c["K"]), dev_bits(c["V"])
+    C = None if c["C"] is None else torch.from_numpy(c["C"]).cuda()
+    ck = None if c["ckey"] is None else torch.from_numpy(c["ckey"]).cuda()
+    BH, Nq = Q.shape[:2]
+    dv = V.shape[2]
+    O = torch.full((BH, Nq, dv), float("nan"), device="cuda",
+                   dtype=torch.float32 if out_f32 else torch.bfloat16)
+    L = torch.full((BH, Nq), float("nan"), device="cuda", dtype=torch.float32)
+    eta.attn_fwd_ex(Q, K, V, c["mode"], C, ck, c["scale"], O, L)
+    torch.cuda.synchronize()
+    code, word = eta.attn_device_status(None)
+    assert code == eta.ATTN_OK, f"watchdog {word:#x}"
+    return O.float().cpu().numpy().astype(np.float64), L.cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("case", CASES, ids=_id)
+def test_ex_parity(case):
+    BH, Nq, Nk, d, dv, mode, out_f32, p_mask = case
+    c = synth.random_case_ex(3000 + Nq + Nk + mode, BH, Nq, Nk, d, dv, mode, 1.0, p_mask)
+    O, L = run_ex(c, out_f32)
+    O_ref, L_ref, _ = oracle.attention_ex(c["Q"], c["K"], c["V"], mode, c["C"], c["ckey"],
+                                          c["scale"])
+    compare(O, L, O_ref, L_ref, out_bf16=not out_f32, label=_id(case))
+
+
+def test_square_ex_matches_attn_fwd_bitwise():
+    import torch
+
+    import exact_tiled_attention_13_gb300 as eta
+    from gpu_helpers import device_inputs
+
+    c = synth.random_case(31, 2, 500, 128, 128, CAUSAL)
+    Q, K, V, _ = device_inputs(c)
+    O1 = torch.empty(2, 500, 128, device="cuda")
+    O2 = torch.empty(2, 500, 128, device="cuda")
+    eta.attn_fwd(Q, K, V, CAUSAL, None, c["scale"], O1)
+    eta.attn_fwd_ex(Q, K, V, CAUSAL, None, None, c["scale"], O2)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2)
