@@ -13,11 +13,12 @@ from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_ERR_CUDA, ATTN_ERR_DEVIC
                    ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_FAULT_NONE, ATTN_FAULT_SKIP_FIRST_K,
                    ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK, ATTN_OUT_BF16, ATTN_OUT_F32,
                    AttnError, attn_device_status, attn_fwd_ex_raw, attn_fwd_raw,
-                   attn_set_fault_injection,
+                   attn_fwd_splitkv_plan, attn_fwd_splitkv_raw, attn_set_fault_injection,
                    attn_set_wait_timeout_ns, attn_version, library_path, load, strerror)
 
 __all__ = [
-    "attn_fwd", "attn_fwd_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
+    "attn_fwd", "attn_fwd_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "attn_fwd_splitkv",
+    "attn_fwd_splitkv_raw", "attn_fwd_splitkv_plan", "splitkv_workspace", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
     "attn_set_fault_injection", "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
     "ATTN_BIAS_DENSE", "ATTN_BIAS_KEY", "ATTN_OUT_BF16", "ATTN_OUT_F32",
 ]
@@ -74,13 +75,8 @@ def attn_fwd(Q, K, V, mode, C, scale, O, LSE=None, stream=None):
     return O, LSE
 
 
-def attn_fwd_ex(Q, K, V, mode, C, ckey, scale, O, LSE=None, stream=None):
-    """attn_fwd with Nq queries and Nk keys and the per-key bias term, through the C ABI.
-
-    Q: bf16 [BH, Nq, d]; K: bf16 [BH, Nk, d]; V: bf16 [BH, Nk, d_v]; mode: bit set of
-    ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, ATTN_BIAS_KEY; C: fp32 [BH, Nq, Nk] or None;
-    ckey: fp32 [BH, Nk] or None; O: bf16/fp32 [BH, Nq, d_v]; LSE: fp32 [BH, Nq] or None.
-    """
+def _marshal_ex(Q, K, V, C, ckey, O, LSE):
+    """Shape/dtype checks of the Nq x Nk entry points; returns the integers they take."""
     import torch
 
     for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O)):
@@ -110,8 +106,51 @@ def attn_fwd_ex(Q, K, V, mode, C, ckey, scale, O, LSE=None, stream=None):
         if LSE.dtype != torch.float32 or tuple(LSE.shape) != (BH, Nq) or not LSE.is_contiguous():
             raise ValueError("LSE must be a contiguous fp32 [BH, Nq] tensor")
         lse_ptr = LSE.data_ptr()
+    return BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr
+
+
+def attn_fwd_ex(Q, K, V, mode, C, ckey, scale, O, LSE=None, stream=None):
+    """attn_fwd with Nq queries and Nk keys and the per-key bias term, through the C ABI.
+
+    Q: bf16 [BH, Nq, d]; K: bf16 [BH, Nk, d]; V: bf16 [BH, Nk, d_v]; mode: bit set of
+    ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, ATTN_BIAS_KEY; C: fp32 [BH, Nq, Nk] or None;
+    ckey: fp32 [BH, Nk] or None; O: bf16/fp32 [BH, Nq, d_v]; LSE: fp32 [BH, Nq] or None.
+    """
+    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE)
     code = attn_fwd_ex_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), mode, c_ptr, k_ptr, BH, Nq, Nk,
                            d, dv, scale, O.data_ptr(), out_dtype, lse_ptr, _stream_handle(stream))
     if code != ATTN_OK:
         raise AttnError(code, "attn_fwd_ex")
+    return O, LSE
+
+
+def splitkv_workspace(mode, BH, Nq, Nk, d, d_v, n_splits=0, device="cuda"):
+    """A workspace tensor (uint8) of the size attn_fwd_splitkv_plan reports, or None when
+    the plan has one key range. The caller keeps it for as long as the launches using
+    it may run."""
+    import torch
+
+    code, splits, nbytes = attn_fwd_splitkv_plan(mode, BH, Nq, Nk, d, d_v, n_splits)
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd_splitkv_plan")
+    return None if nbytes == 0 else torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def attn_fwd_splitkv(Q, K, V, mode, C, ckey, scale, O, LSE=None, workspace=None, n_splits=0,
+                     stream=None):
+    """attn_fwd_ex with each head's keys split into ranges run as separate blocks and merged
+    by a second kernel (include/attn.h, attn_fwd_splitkv). `workspace`: a contiguous CUDA
+    tensor of at least the planned bytes (see splitkv_workspace), or None when the plan
+    has one range; n_splits = 0 lets the library choose."""
+    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE)
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        if not workspace.is_contiguous():
+            raise ValueError("workspace must be contiguous")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    code = attn_fwd_splitkv_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), mode, c_ptr, k_ptr, BH,
+                                Nq, Nk, d, dv, scale, n_splits, ws_ptr, ws_bytes, O.data_ptr(),
+                                out_dtype, lse_ptr, _stream_handle(stream))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd_splitkv")
     return O, LSE

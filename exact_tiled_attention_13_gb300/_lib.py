@@ -35,6 +35,14 @@ SIGNATURES = {
     "attn_fwd_ex": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P,
                                    ctypes.c_int, _P, _P]),
+    "attn_fwd_splitkv": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_float, ctypes.c_int, _P, ctypes.c_ulonglong, _P,
+                                        ctypes.c_int, _P, _P]),
+    "attn_fwd_splitkv_plan": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_ulonglong)]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
@@ -92,6 +100,23 @@ def attn_fwd_ex_raw(Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, O, out_dt
     """attn_fwd_ex with plain integers as pointers; returns its code unchanged."""
     return load().attn_fwd_ex(Q, K, V, int(mode), C, ckey, int(BH), int(Nq), int(Nk), int(d),
                               int(d_v), float(scale), O, int(out_dtype), LSE, stream)
+
+
+def attn_fwd_splitkv_raw(Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, n_splits, workspace,
+                         workspace_bytes, O, out_dtype, LSE, stream) -> int:
+    """attn_fwd_splitkv with plain integers as pointers; returns its code unchanged."""
+    return load().attn_fwd_splitkv(Q, K, V, int(mode), C, ckey, int(BH), int(Nq), int(Nk), int(d),
+                                   int(d_v), float(scale), int(n_splits), workspace,
+                                   int(workspace_bytes), O, int(out_dtype), LSE, stream)
+
+
+def attn_fwd_splitkv_plan(mode, BH, Nq, Nk, d, d_v, n_splits=0):
+    """(code, key ranges, workspace bytes) of attn_fwd_splitkv for these arguments."""
+    splits = ctypes.c_int(0)
+    nbytes = ctypes.c_ulonglong(0)
+    code = load().attn_fwd_splitkv_plan(int(mode), int(BH), int(Nq), int(Nk), int(d), int(d_v),
+                                        int(n_splits), ctypes.byref(splits), ctypes.byref(nbytes))
+    return code, splits.value, nbytes.value
 
 
 def attn_device_status(stream=None):

@@ -20,23 +20,36 @@ MiB = 1 << 20
 GiB = 1 << 30
 
 
-def flops(BH: int, N: int, d: int, dv: int, causal: bool) -> float:
-    """Algorithmic FLOPs of one forward pass: 2 * BH * N^2 * (d + dv), halved when causal."""
-    f = 2.0 * BH * N * N * (d + dv)
-    return f / 2.0 if causal else f
+def allowed_pairs(N: int, causal: bool, Nk: int | None = None) -> float:
+    """(query, key) pairs that take part, per head. Without a mask Nq * Nk. With the causal
+    mask (query i sees keys j <= i + Nk - Nq) the continuous count Nq Nk - Nq^2 / 2 when
+    Nq <= Nk and Nk^2 / 2 otherwise; for Nq = Nk both give the usual N^2 / 2."""
+    Nq, Nk = N, (N if Nk is None else Nk)
+    if not causal:
+        return float(Nq) * Nk
+    if Nq <= Nk:
+        return float(Nq) * Nk - 0.5 * float(Nq) * Nq
+    return 0.5 * float(Nk) * Nk
+
+
+def flops(BH: int, N: int, d: int, dv: int, causal: bool, Nk: int | None = None) -> float:
+    """Algorithmic FLOPs of one forward pass: 2 (d + dv) per allowed (query, key) pair,
+    i.e. 2 BH N^2 (d + dv), halved when causal, for N queries and N keys."""
+    return 2.0 * BH * allowed_pairs(N, causal, Nk) * (d + dv)
 
 
 def required_bytes(BH: int, N: int, d: int, dv: int, out_bytes: int, lse: bool = True,
-                   dense_bias: bool = False, key_bias: bool = False) -> int:
-    """Bytes of reading Q, K, V (bf16) and the bias (fp32 C [N, N] or vector [N]) once and
-    writing O and LSE once."""
-    b = BH * N * (d + d + dv) * BF16 + BH * N * dv * out_bytes
+                   dense_bias: bool = False, key_bias: bool = False, Nk: int | None = None) -> int:
+    """Bytes of reading Q (N rows), K and V (Nk rows, default N) in bf16 and the bias (fp32
+    C [N, Nk] or vector [Nk]) once and writing O and LSE once."""
+    Nk = N if Nk is None else Nk
+    b = BH * N * d * BF16 + BH * Nk * (d + dv) * BF16 + BH * N * dv * out_bytes
     if lse:
         b += BH * N * F32
     if dense_bias:
-        b += BH * N * N * F32
+        b += BH * N * Nk * F32
     if key_bias:
-        b += BH * N * F32
+        b += BH * Nk * F32
     return b
 
 

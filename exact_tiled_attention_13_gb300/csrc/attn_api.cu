@@ -12,6 +12,7 @@
 
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
+#include "attn_merge_kernel.cuh"
 
 namespace eta {
 
@@ -180,93 +181,271 @@ extern "C" int attn_set_fault_injection(int fault) {
   return ATTN_OK;
 }
 
-extern "C" int attn_fwd_ex(const void *Q, const void *K, const void *V, int mode, const float *C,
-                           const float *ckey, int BH, int Nq, int Nk, int d, int d_v, float scale,
-                           void *O, int out_dtype, float *LSE, void *stream) {
-  // ---- arguments (no CUDA call before these pass)
+namespace eta {
+namespace {
+
+// One forward problem as the entry points receive it.
+struct Problem {
+  const void *Q, *K, *V;
+  int mode;
+  const float *C, *ckey;
+  int BH, Nq, Nk, d, d_v;
+  float scale;
+  void *O;
+  int out_dtype;
+  float *LSE;
+  void *stream;
+  bool causal() const { return (mode & ATTN_MASK_CAUSAL) != 0; }
+  bool dense() const { return (mode & ATTN_BIAS_DENSE) != 0; }
+  bool key() const { return (mode & ATTN_BIAS_KEY) != 0; }
+  int bias() const {
+    if (dense()) return (Nk % 4 == 0) ? BIAS_DENSE_TMA : BIAS_DENSE_DIRECT;
+    return key() ? BIAS_KEY : BIAS_NONE;
+  }
+  int nkv_tiles() const { return (Nk + BN - 1) / BN; }
+  int ctas_per_head() const {
+    const int nqc = q_tiles_per_cta(bias());
+    return ((Nq + BM - 1) / BM + nqc - 1) / nqc;
+  }
+  size_t o_bytes() const {
+    return static_cast<size_t>(BH) * Nq * d_v * (out_dtype == ATTN_OUT_F32 ? 4 : 2);
+  }
+  size_t lse_bytes() const { return LSE ? static_cast<size_t>(BH) * Nq * 4 : 0; }
+};
+
+constexpr int kEmpty = 1;  // check_shape: a valid call with nothing to do
+
+// Checks of mode, sizes and scale (no pointer is looked at).
+int check_shape(int mode, int BH, int Nq, int Nk, int d, int d_v, int out_dtype, float scale) {
   if (mode & ~(ATTN_MASK_CAUSAL | ATTN_BIAS_DENSE | ATTN_BIAS_KEY)) return ATTN_ERR_INVALID_ARG;
-  const bool causal = (mode & ATTN_MASK_CAUSAL) != 0;
-  const bool dense = (mode & ATTN_BIAS_DENSE) != 0;
-  const bool key = (mode & ATTN_BIAS_KEY) != 0;
-  if (dense && key) return ATTN_ERR_INVALID_ARG;
+  if ((mode & ATTN_BIAS_DENSE) && (mode & ATTN_BIAS_KEY)) return ATTN_ERR_INVALID_ARG;
   if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
   if (BH < 1 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if ((d != 64 && d != 128) || (d_v != 64 && d_v != 128)) return ATTN_ERR_UNSUPPORTED;
-  if (Nq == 0) return ATTN_OK;  // empty buffers may be null
+  if (Nq == 0) return kEmpty;                // empty buffers may be null
   if (Nk == 0) return ATTN_ERR_INVALID_ARG;  // every row would lack an allowed key
-  if (!Q || !K || !V || !O) return ATTN_ERR_INVALID_ARG;
-  if (dense != (C != nullptr) || key != (ckey != nullptr)) return ATTN_ERR_INVALID_ARG;
-  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) ||
-      (C && !aligned(C, 16)) || (ckey && !aligned(ckey, 4)) || (LSE && !aligned(LSE, 4)))
-    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
 
-  const size_t qrows = static_cast<size_t>(BH) * static_cast<size_t>(Nq);
-  const size_t krows = static_cast<size_t>(BH) * static_cast<size_t>(Nk);
-  const size_t o_bytes = qrows * d_v * (out_dtype == ATTN_OUT_F32 ? 4 : 2);
-  const size_t lse_bytes = LSE ? qrows * 4 : 0;
-  const void *ins[5] = {Q, K, V, C, ckey};
-  const size_t in_bytes[5] = {qrows * d * 2, krows * d * 2, krows * d_v * 2,
-                              C ? qrows * static_cast<size_t>(Nk) * 4 : 0, ckey ? krows * 4 : 0};
+// Pointer checks that need no CUDA call: presence, alignment, overlaps.
+int check_pointers(const Problem &a) {
+  if (!a.Q || !a.K || !a.V || !a.O) return ATTN_ERR_INVALID_ARG;
+  if (a.dense() != (a.C != nullptr) || a.key() != (a.ckey != nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(a.Q, 16) || !aligned(a.K, 16) || !aligned(a.V, 16) || !aligned(a.O, 16) ||
+      (a.C && !aligned(a.C, 16)) || (a.ckey && !aligned(a.ckey, 4)) || (a.LSE && !aligned(a.LSE, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t qrows = static_cast<size_t>(a.BH) * static_cast<size_t>(a.Nq);
+  const size_t krows = static_cast<size_t>(a.BH) * static_cast<size_t>(a.Nk);
+  const void *ins[5] = {a.Q, a.K, a.V, a.C, a.ckey};
+  const size_t in_bytes[5] = {qrows * a.d * 2, krows * a.d * 2, krows * a.d_v * 2,
+                              a.C ? qrows * static_cast<size_t>(a.Nk) * 4 : 0,
+                              a.ckey ? krows * 4 : 0};
   for (int i = 0; i < 5; ++i) {
-    if (ranges_overlap(O, o_bytes, ins[i], in_bytes[i]) || ranges_overlap(LSE, lse_bytes, ins[i], in_bytes[i]))
+    if (ranges_overlap(a.O, a.o_bytes(), ins[i], in_bytes[i]) ||
+        ranges_overlap(a.LSE, a.lse_bytes(), ins[i], in_bytes[i]))
       return ATTN_ERR_INVALID_ARG;
   }
-  if (ranges_overlap(O, o_bytes, LSE, lse_bytes)) return ATTN_ERR_INVALID_ARG;
+  if (ranges_overlap(a.O, a.o_bytes(), a.LSE, a.lse_bytes())) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// Launches the attention kernel. With n_splits > 1 each CTA covers `split_tiles` K/V
+// tiles of its head and writes fp32 partials to O_dst / LSE_dst instead of O / LSE.
+int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int split_tiles,
+                   void *O_dst, float *LSE_dst, int out_f32) {
+  int rc;
+  if ((rc = get_encoder()) != ATTN_OK) return rc;
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  const uint64_t nq = static_cast<uint64_t>(a.Nq), nk = static_cast<uint64_t>(a.Nk),
+                 bh = static_cast<uint64_t>(a.BH);
+  if (encode_3d(&la.tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.Q, a.d, nq, bh, SW_CHUNK, BM) != ATTN_OK ||
+      encode_3d(&la.tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.d, nk, bh, SW_CHUNK, BN) != ATTN_OK ||
+      encode_3d(&la.tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.V, a.d_v, nk, bh, SW_CHUNK, BN) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  // The dense bias goes through TMA when its rows are 16-byte multiples; otherwise the
+  // softmax warps read it directly.
+  const int bias = a.bias();
+  if (bias == BIAS_DENSE_TMA &&
+      encode_3d(&la.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.C, nk, nq, bh, CCHUNK, BM) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+
+  la.p.BH = a.BH;
+  la.p.Nq = a.Nq;
+  la.p.Nk = a.Nk;
+  la.p.nq_tiles = (a.Nq + BM - 1) / BM;
+  la.p.nkv_tiles = a.nkv_tiles();
+  la.p.causal_off = a.Nk - a.Nq;
+  la.p.ctas_per_head = a.ctas_per_head();
+  la.p.n_splits = n_splits;
+  la.p.split_tiles = split_tiles;
+  la.p.scale_log2 = a.scale * LOG2E;
+  la.p.out_f32 = out_f32;
+  la.p.O = O_dst;
+  la.p.LSE = LSE_dst;
+  la.p.C = a.C;
+  la.p.ckey = a.ckey;
+  la.p.status = watchdog;
+  la.p.timeout_ns = g_timeout_ns.load();
+  la.p.fault = g_fault.load();
+  la.stream = static_cast<cudaStream_t>(a.stream);
+  if (static_cast<uint64_t>(a.BH) * la.p.ctas_per_head * n_splits > 0x7FFFFFFFull)
+    return ATTN_ERR_INVALID_ARG;
+
+  cudaError_t e;
+  const bool causal = a.causal();
+  if (a.d == 64 && a.d_v == 64) e = dispatch<64, 64>(causal, bias, la);
+  else if (a.d == 64) e = dispatch<64, 128>(causal, bias, la);
+  else if (a.d_v == 64) e = dispatch<128, 64>(causal, bias, la);
+  else e = dispatch<128, 128>(causal, bias, la);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
+  }
+  return ATTN_OK;
+}
+
+constexpr int kMaxSplits = 1024;
+
+// Number of key ranges for a split launch and the K/V tiles of each. A request of
+// n_splits ranges is rounded to whole tiles: split_tiles = ceil(nkv / n_splits), and
+// only ceil(nkv / split_tiles) ranges are non-empty. n_splits == 0 chooses the count
+// for `sms` multiprocessors: the one that minimises waves x tiles per range, plus a
+// small charge per range for writing and merging its partials.
+void split_plan(const Problem &a, int n_splits, int sms, int *splits, int *split_tiles) {
+  const int nkv = a.nkv_tiles();
+  if (n_splits <= 0) {
+    const long long base = static_cast<long long>(a.BH) * a.ctas_per_head();
+    int best = 1;
+    double best_cost = 1e300;
+    for (int s = 1; s <= nkv && s <= kMaxSplits; ++s) {
+      const int chunk = (nkv + s - 1) / s;
+      const int eff = (nkv + chunk - 1) / chunk;
+      if (eff != s) continue;  // the same ranges as a smaller request
+      const long long waves = (base * eff + sms - 1) / sms;
+      const double cost = static_cast<double>(waves) * chunk + 0.125 * eff;
+      if (cost < best_cost) {
+        best_cost = cost;
+        best = s;
+      }
+    }
+    n_splits = best;
+  }
+  if (n_splits > nkv) n_splits = nkv;
+  *split_tiles = (nkv + n_splits - 1) / n_splits;
+  *splits = (nkv + *split_tiles - 1) / *split_tiles;
+}
+
+unsigned long long split_workspace_bytes(const Problem &a, int splits) {
+  if (splits <= 1) return 0;
+  return static_cast<unsigned long long>(splits) * a.BH * a.Nq * (a.d_v + 1) * 4ull;
+}
+
+int sm_count(int dev, int *sms) {
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace eta
+
+extern "C" int attn_fwd_ex(const void *Q, const void *K, const void *V, int mode, const float *C,
+                           const float *ckey, int BH, int Nq, int Nk, int d, int d_v, float scale,
+                           void *O, int out_dtype, float *LSE, void *stream) {
+  // ---- arguments (no CUDA call before these pass)
+  int rc = check_shape(mode, BH, Nq, Nk, d, d_v, out_dtype, scale);
+  if (rc == kEmpty) return ATTN_OK;
+  if (rc != ATTN_OK) return rc;
+  const Problem a{Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, O, out_dtype, LSE, stream};
+  if ((rc = check_pointers(a)) != ATTN_OK) return rc;
 
   // ---- device
   int dev = -1;
   unsigned int *watchdog = nullptr;
-  int rc = current_device(&dev, &watchdog);
-  if (rc != ATTN_OK) return rc;
+  if ((rc = current_device(&dev, &watchdog)) != ATTN_OK) return rc;
   const void *ptrs[7] = {Q, K, V, O, C, ckey, LSE};
   for (const void *ptr : ptrs)
     if (ptr && device_pointer_ok(ptr, dev) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
-  if ((rc = get_encoder()) != ATTN_OK) return rc;
+  return launch_forward(a, watchdog, 1, a.nkv_tiles(), O, LSE, out_dtype == ATTN_OUT_F32 ? 1 : 0);
+}
 
-  LaunchArgs a;
-  std::memset(&a, 0, sizeof(a));
-  const uint64_t nq = static_cast<uint64_t>(Nq), nk = static_cast<uint64_t>(Nk),
-                 bh = static_cast<uint64_t>(BH);
-  if (encode_3d(&a.tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, d, nq, bh, SW_CHUNK, BM) != ATTN_OK ||
-      encode_3d(&a.tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, d, nk, bh, SW_CHUNK, BN) != ATTN_OK ||
-      encode_3d(&a.tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, V, d_v, nk, bh, SW_CHUNK, BN) != ATTN_OK)
-    return ATTN_ERR_CUDA;
-  // The dense bias goes through TMA when its rows are 16-byte multiples; otherwise the
-  // softmax warps read it directly.
-  int bias = BIAS_NONE;
-  if (dense) bias = (Nk % 4 == 0) ? BIAS_DENSE_TMA : BIAS_DENSE_DIRECT;
-  if (key) bias = BIAS_KEY;
-  if (bias == BIAS_DENSE_TMA &&
-      encode_3d(&a.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, nk, nq, bh, CCHUNK, BM) != ATTN_OK)
-    return ATTN_ERR_CUDA;
+extern "C" int attn_fwd_splitkv_plan(int mode, int BH, int Nq, int Nk, int d, int d_v,
+                                     int n_splits, int *splits, unsigned long long *workspace_bytes) {
+  if (splits) *splits = 0;
+  if (workspace_bytes) *workspace_bytes = 0;
+  if (!splits || !workspace_bytes || n_splits < 0) return ATTN_ERR_INVALID_ARG;
+  int rc = check_shape(mode, BH, Nq, Nk, d, d_v, ATTN_OUT_F32, 1.0f);
+  if (rc == kEmpty) {
+    *splits = 1;
+    return ATTN_OK;
+  }
+  if (rc != ATTN_OK) return rc;
+  const Problem a{nullptr, nullptr, nullptr, mode, nullptr, nullptr, BH, Nq, Nk, d, d_v,
+                  1.0f, nullptr, ATTN_OUT_F32, nullptr, nullptr};
+  int sms = 0;
+  if (n_splits == 0) {
+    int dev = -1;
+    unsigned int *watchdog = nullptr;
+    if ((rc = current_device(&dev, &watchdog)) != ATTN_OK) return rc;
+    if ((rc = sm_count(dev, &sms)) != ATTN_OK) return rc;
+  }
+  int tiles = 0;
+  split_plan(a, n_splits, sms, splits, &tiles);
+  *workspace_bytes = split_workspace_bytes(a, *splits);
+  return ATTN_OK;
+}
 
-  const int nq_tiles = (Nq + BM - 1) / BM;
-  const int nqc = q_tiles_per_cta(bias);
-  a.p.BH = BH;
-  a.p.Nq = Nq;
-  a.p.Nk = Nk;
-  a.p.nq_tiles = nq_tiles;
-  a.p.nkv_tiles = (Nk + BN - 1) / BN;
-  a.p.causal_off = Nk - Nq;
-  a.p.ctas_per_head = (nq_tiles + nqc - 1) / nqc;
-  a.p.scale_log2 = scale * LOG2E;
-  a.p.out_f32 = out_dtype == ATTN_OUT_F32 ? 1 : 0;
-  a.p.O = O;
-  a.p.LSE = LSE;
-  a.p.C = C;
-  a.p.ckey = ckey;
-  a.p.status = watchdog;
-  a.p.timeout_ns = g_timeout_ns.load();
-  a.p.fault = g_fault.load();
-  a.stream = static_cast<cudaStream_t>(stream);
-  if (static_cast<uint64_t>(BH) * a.p.ctas_per_head > 0x7FFFFFFFull) return ATTN_ERR_INVALID_ARG;
+extern "C" int attn_fwd_splitkv(const void *Q, const void *K, const void *V, int mode,
+                                const float *C, const float *ckey, int BH, int Nq, int Nk, int d,
+                                int d_v, float scale, int n_splits, void *workspace,
+                                unsigned long long workspace_bytes, void *O, int out_dtype,
+                                float *LSE, void *stream) {
+  // ---- arguments (no CUDA call before these pass)
+  if (n_splits < 0) return ATTN_ERR_INVALID_ARG;
+  int rc = check_shape(mode, BH, Nq, Nk, d, d_v, out_dtype, scale);
+  if (rc == kEmpty) return ATTN_OK;
+  if (rc != ATTN_OK) return rc;
+  const Problem a{Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, O, out_dtype, LSE, stream};
+  if ((rc = check_pointers(a)) != ATTN_OK) return rc;
 
-  cudaError_t e;
-  if (d == 64 && d_v == 64) e = dispatch<64, 64>(causal, bias, a);
-  else if (d == 64) e = dispatch<64, 128>(causal, bias, a);
-  else if (d_v == 64) e = dispatch<128, 64>(causal, bias, a);
-  else e = dispatch<128, 128>(causal, bias, a);
+  // ---- device and plan
+  int dev = -1;
+  unsigned int *watchdog = nullptr;
+  if ((rc = current_device(&dev, &watchdog)) != ATTN_OK) return rc;
+  int sms = 0;
+  if (n_splits == 0 && (rc = sm_count(dev, &sms)) != ATTN_OK) return rc;
+  int splits = 1, tiles = 0;
+  split_plan(a, n_splits, sms, &splits, &tiles);
+  const unsigned long long need = split_workspace_bytes(a, splits);
+  if (splits > 1) {
+    if (!workspace || !aligned(workspace, 16) || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+    const void *bufs[7] = {Q, K, V, C, ckey, O, LSE};
+    const size_t qrows = static_cast<size_t>(BH) * Nq, krows = static_cast<size_t>(BH) * Nk;
+    const size_t sizes[7] = {qrows * d * 2, krows * d * 2, krows * d_v * 2,
+                             C ? qrows * static_cast<size_t>(Nk) * 4 : 0, ckey ? krows * 4 : 0,
+                             a.o_bytes(), a.lse_bytes()};
+    for (int i = 0; i < 7; ++i)
+      if (ranges_overlap(workspace, need, bufs[i], sizes[i])) return ATTN_ERR_INVALID_ARG;
+  }
+  const void *ptrs[8] = {Q, K, V, O, C, ckey, LSE, splits > 1 ? workspace : nullptr};
+  for (const void *ptr : ptrs)
+    if (ptr && device_pointer_ok(ptr, dev) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
+
+  const int out_f32 = out_dtype == ATTN_OUT_F32 ? 1 : 0;
+  if (splits == 1) return launch_forward(a, watchdog, 1, a.nkv_tiles(), O, LSE, out_f32);
+
+  // Partials: O_part [splits][BH][Nq][d_v] fp32, then L_part [splits][BH][Nq] fp32.
+  float *O_part = static_cast<float *>(workspace);
+  float *L_part = O_part + static_cast<size_t>(splits) * BH * Nq * d_v;
+  if ((rc = launch_forward(a, watchdog, splits, tiles, O_part, L_part, 1)) != ATTN_OK) return rc;
+  const long long rows = static_cast<long long>(BH) * Nq;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d_v == 64 ? launch_merge<64>(O_part, L_part, splits, rows, O, out_f32, LSE, st)
+                                  : launch_merge<128>(O_part, L_part, splits, rows, O, out_f32, LSE, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return ATTN_ERR_LAUNCH;

@@ -83,10 +83,12 @@ struct KernelParams {
   int nkv_tiles;      // ceil(Nk / 128)
   int causal_off;     // Nk - Nq: query i may see keys j <= i + causal_off
   int ctas_per_head;  // ceil(nq_tiles / NQ)
+  int n_splits;       // key ranges per head (1: the whole key sequence)
+  int split_tiles;    // K/V tiles per key range
   float scale_log2;   // scale * log2(e)
   int out_f32;        // O element type: 1 fp32, 0 bf16
-  void *O;
-  float *LSE;
+  void *O;    // with n_splits > 1: fp32 partial outputs [n_splits][BH][Nq][d_v]
+  float *LSE; // with n_splits > 1: partial LSE [n_splits][BH][Nq]
   const float *C;           // dense bias [BH][Nq][Nk], read directly when it cannot go through TMA
   const float *ckey;        // per-key bias [BH][Nk]
   unsigned int *status;     // watchdog word (device memory)
@@ -248,29 +250,38 @@ template <int NQ, bool CAUSAL>
 struct Schedule {
   static_assert(NQ == 1 || NQ == 2, "one or two query tiles per CTA");
   int bh, cta_q, n_exist, hi_max, n_it;
-  int nkv, off;
   int first0, first1;  // first_it of query tiles 0 and 1
 
   __device__ Schedule(const KernelParams &p) {
-    bh = blockIdx.x / p.ctas_per_head;
+    // Grid order: head, then key range, then query tiles, so the CTAs that share a
+    // head's K/V tiles run side by side.
+    const int per_head = p.ctas_per_head * p.n_splits;
+    bh = blockIdx.x / per_head;
+    const int r = static_cast<int>(blockIdx.x % per_head);
+    const int split = r / p.ctas_per_head;
     // Within a head, the CTA with the most causal work starts first.
-    cta_q = p.ctas_per_head - 1 - static_cast<int>(blockIdx.x % p.ctas_per_head);
+    cta_q = p.ctas_per_head - 1 - r % p.ctas_per_head;
     n_exist = cmin(NQ, p.nq_tiles - cta_q * NQ);
-    nkv = p.nkv_tiles;
-    off = p.causal_off;
-    const int hi0 = hi(p.Nq, 0);
-    const int hi1 = NQ == 2 ? hi(p.Nq, 1) : -1;
+    const int lo = split * p.split_tiles;  // this CTA's K/V tiles: lo .. top
+    const int top = cmin(lo + p.split_tiles, p.nkv_tiles) - 1;
+    const int hi0 = hi(p, 0, top);
+    const int hi1 = NQ == 2 ? hi(p, 1, top) : lo - 1;
     hi_max = n_exist == 2 ? hi1 : hi0;  // hi grows with the query tile
-    n_it = hi_max >= 0 ? hi_max + 1 : 0;
-    first0 = hi0 >= 0 ? hi_max - hi0 : n_it;
-    first1 = (n_exist == 2 && hi1 >= 0) ? hi_max - hi1 : n_it;
+    n_it = hi_max >= lo ? hi_max - lo + 1 : 0;
+    if (CAUSAL) {
+      first0 = hi0 >= lo ? hi_max - hi0 : n_it;
+      first1 = (n_exist == 2 && hi1 >= lo) ? hi_max - hi1 : n_it;
+    } else {  // every query tile visits the whole range (n_it is 0 for an empty range)
+      first0 = 0;
+      first1 = n_exist == 2 ? 0 : n_it;
+    }
   }
   __device__ int q_tile(int q) const { return cta_q * NQ + q; }
-  // Last K/V tile query tile q visits (negative: none).
-  __device__ int hi(int nq, int q) const {
-    if (!CAUSAL) return nkv - 1;
-    const int last_row = cmin(q_tile(q) * BM + BM - 1, nq - 1);
-    return cmin(floor_div(last_row + off, BN), nkv - 1);
+  // Last K/V tile query tile q visits, at most `top` (below the range's first: none).
+  __device__ int hi(const KernelParams &p, int q, int top) const {
+    if (!CAUSAL) return top;
+    const int last_row = cmin(q_tile(q) * BM + BM - 1, p.Nq - 1);
+    return cmin(floor_div(last_row + p.causal_off, BN), top);
   }
   // First iteration query tile q takes part in; n_it when it takes part in none.
   __device__ int first_it(int q) const { return q == 0 ? first0 : first1; }
@@ -384,9 +395,9 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     // Tiles j >= j_mask need an elementwise mask: those that reach past the causal limit
     // of the tile's first row, and the last tile when Nk is not a multiple of 128. lim is
     // the last key this row may see (the causal limit i + (Nk - Nq), or the last key).
-    int j_mask = CAUSAL ? floor_div(qt * BM + sch.off + 1, BN) : INT_MAX;
-    if (p.Nk % BN != 0) j_mask = cmin(j_mask, sch.nkv - 1);
-    const int lim = CAUSAL ? cmin(q_row + sch.off, p.Nk - 1) : p.Nk - 1;
+    int j_mask = CAUSAL ? floor_div(qt * BM + p.causal_off + 1, BN) : INT_MAX;
+    if (p.Nk % BN != 0) j_mask = cmin(j_mask, p.nkv_tiles - 1);
+    const int lim = CAUSAL ? cmin(q_row + p.causal_off, p.Nk - 1) : p.Nk - 1;
     if (exists && has_keys) {
       for (int it = sch.first_it(q); it < sch.n_it; ++it) {
         const int j = sch.hi_max - it;
@@ -561,7 +572,11 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         if (has_keys) tc_fence_after();
         const bool row_ok = q_row < p.Nq;
         const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;  // no allowed key: O = 0
-        const size_t orow = (static_cast<size_t>(sch.bh) * p.Nq + (row_ok ? q_row : 0)) * DV;
+        // Key range `split` of a split launch writes its own slice of the partials.
+        const int split = static_cast<int>(blockIdx.x % (p.ctas_per_head * p.n_splits)) /
+                          p.ctas_per_head;
+        const size_t lrow = (static_cast<size_t>(split) * p.BH + sch.bh) * p.Nq + (row_ok ? q_row : 0);
+        const size_t orow = lrow * DV;
 #pragma unroll
         for (int cc = 0; cc < DV / 32; ++cc) {
           uint32_t o[32];
@@ -598,7 +613,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         }
         if (row_ok && p.LSE != nullptr) {
           // LSE_i = m_i + ln l_i, from the log2-scaled running max.
-          p.LSE[static_cast<size_t>(sch.bh) * p.Nq + q_row] =
+          p.LSE[lrow] =
               (l > 0.0f) ? (m2 + lg2_approx(l)) * LN2 : -INFINITY;
         }
       }
@@ -833,7 +848,8 @@ cudaError_t launch_attn(const LaunchArgs &a) {
     if (e != cudaSuccess) return e;
     if (attr.numRegs * CF::THREADS < CF::REGS_NEEDED) return cudaErrorLaunchOutOfResources;
   }
-  const unsigned grid = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ctas_per_head);
+  const unsigned grid = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ctas_per_head) *
+                        static_cast<unsigned>(a.p.n_splits);
   kern<<<grid, CF::THREADS, CF::SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmC, a.p);
   return cudaGetLastError();
 }

@@ -3,7 +3,7 @@
     python -m exact_tiled_attention_13_gb300.workload --workload 3 --iters 3
 
 generates the seeded inputs of the workload, copies them to cuda:0, launches
-attn_fwd `--iters` times on the current stream and synchronises. It is the command
+the forward pass `--iters` times on the current stream and synchronises. It is the command
 the profiler summaries under profiles/ were taken with.
 """
 from __future__ import annotations
@@ -48,6 +48,14 @@ class DeviceWorkload:
         self.V = self.V_h.to(device)
         self.C = None if self.C_h is None else self.C_h.to(device)
         self.ckey = None if self.ck_h is None else self.ck_h.to(device)
+        self.workspace = None
+        self.launches_per_step = 1
+        if w.split_kv:
+            import exact_tiled_attention_13_gb300 as eta
+
+            self.workspace = eta.splitkv_workspace(w.mode, w.BH, w.N, w.Nkv, w.d, w.dv, 0,
+                                                   device=device)
+            self.launches_per_step = 1 if self.workspace is None else 2
         odt = torch.float32 if w.out_dtype == "f32" else torch.bfloat16
         self.O = torch.empty(w.BH, w.N, w.dv, dtype=odt, device=device)
         self.LSE = torch.empty(w.BH, w.N, dtype=torch.float32, device=device)
@@ -57,8 +65,13 @@ class DeviceWorkload:
     def launch(self, stream=None):
         import exact_tiled_attention_13_gb300 as eta
 
-        eta.attn_fwd_ex(self.Q, self.K, self.V, self.w.mode, self.C, self.ckey, self.w.scale,
-                        self.O, self.LSE, stream=stream)
+        if self.w.split_kv:
+            eta.attn_fwd_splitkv(self.Q, self.K, self.V, self.w.mode, self.C, self.ckey,
+                                 self.w.scale, self.O, self.LSE, workspace=self.workspace,
+                                 stream=stream)
+        else:
+            eta.attn_fwd_ex(self.Q, self.K, self.V, self.w.mode, self.C, self.ckey, self.w.scale,
+                            self.O, self.LSE, stream=stream)
 
     def h2d_bytes(self) -> int:
         n = sum(t.numel() * t.element_size() for t in (self.Q_h, self.K_h, self.V_h))
@@ -80,15 +93,14 @@ class DeviceWorkload:
             self.C.copy_(self.C_h, non_blocking=True)
         if self.ckey is not None:
             self.ckey.copy_(self.ck_h, non_blocking=True)
-        eta.attn_fwd_ex(self.Q, self.K, self.V, self.w.mode, self.C, self.ckey, self.w.scale,
-                        self.O, self.LSE, stream=stream)
+        self.launch(stream)
         self.O_h.copy_(self.O, non_blocking=True)
         self.LSE_h.copy_(self.LSE, non_blocking=True)
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5, 6])
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args(argv)
     import torch

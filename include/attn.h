@@ -116,6 +116,50 @@ ATTN_API int attn_fwd_ex(const void *Q, const void *K, const void *V, int mode, 
                          const float *ckey, int BH, int Nq, int Nk, int d, int d_v, float scale,
                          void *O, int out_dtype, float *LSE, void *stream);
 
+/*
+ * attn_fwd_splitkv -- the attn_fwd_ex operation with each head's keys cut into ranges of
+ * whole 128-key tiles that run as separate thread blocks, for shapes with few query
+ * tiles and many keys (decoding, a short query block against a long key cache), where
+ * one block per query tile would leave most of the GPU idle. Each range stores its
+ * normalised partial output and log-sum-exp in `workspace`; a second kernel merges the
+ * ranges in increasing order by rescaling them to the common maximum (the blockwise
+ * softmax statistics of "AI Infra ch. 5", section 5.4, and the alpha rescaling of
+ * "Compilers and kernels", section "FlashAttention rewrites the algorithm around IO").
+ * Arguments as for attn_fwd_ex, plus:
+ *   n_splits  requested number of key ranges, >= 0. It is rounded to whole tiles
+ *             (ceil(Nk/128) / ceil(ceil(Nk/128) / n_splits) ranges) and capped at the
+ *             number of key tiles. 0 lets the library choose for the current device.
+ *   workspace device memory of at least the size attn_fwd_splitkv_plan reports for the
+ *             same arguments, 16-byte aligned, overlapping no input or output. The
+ *             caller owns it; its contents on entry do not matter and are overwritten.
+ *             It must stay untouched until the work on `stream` completes. When the
+ *             plan has one range the kernel writes O directly and the workspace is
+ *             not used (it may then be NULL).
+ *   workspace_bytes its size in bytes.
+ * Two kernels are launched on `stream` (one when the plan has one range). The result
+ * is deterministic for a given number of ranges (fixed merge order, no atomics); a
+ * different number of ranges may differ in rounding, within the tolerance of the
+ * method. Errors as for attn_fwd_ex; a missing, misaligned, too small or overlapping
+ * workspace is ATTN_ERR_INVALID_ARG.
+ */
+ATTN_API int attn_fwd_splitkv(const void *Q, const void *K, const void *V, int mode,
+                              const float *C, const float *ckey, int BH, int Nq, int Nk, int d,
+                              int d_v, float scale, int n_splits, void *workspace,
+                              unsigned long long workspace_bytes, void *O, int out_dtype,
+                              float *LSE, void *stream);
+
+/*
+ * attn_fwd_splitkv_plan -- the number of key ranges attn_fwd_splitkv will use for
+ * these arguments (`*splits`) and the workspace bytes it needs (`*workspace_bytes`,
+ * splits x BH x Nq x (d_v + 1) x 4 bytes: fp32 partial O and LSE per range; 0 when
+ * splits is 1). n_splits == 0 (automatic) reads the current device's multiprocessor
+ * count; any other value involves no CUDA call. Returns ATTN_OK, or the argument
+ * error attn_fwd_splitkv would return for the same shape, mode and n_splits
+ * (ATTN_ERR_INVALID_ARG also for NULL out-pointers).
+ */
+ATTN_API int attn_fwd_splitkv_plan(int mode, int BH, int Nq, int Nk, int d, int d_v, int n_splits,
+                                   int *splits, unsigned long long *workspace_bytes);
+
 /* Static English text for a return code (never NULL). */
 ATTN_API const char *attn_strerror(int code);
 

@@ -115,10 +115,16 @@ class Workload:
     out_dtype: str  # "bf16" or "f32"
     qk_mult: float = 1.0
     p_mask: float = 0.0
+    Nk: int = 0             # keys per head; 0: as many as queries (N)
+    split_kv: bool = False  # launched as a split forward pass (key ranges + merge)
 
     @property
     def BH(self) -> int:
         return self.B * self.H
+
+    @property
+    def Nkv(self) -> int:
+        return self.Nk or self.N
 
     @property
     def scale(self) -> float:
@@ -138,6 +144,10 @@ WORKLOADS = {
     # instead of a dense N x N array.
     6: Workload("b1h8_n4096_d64_dv128_key_bias_keypad", 1, 8, 4096, 64, 128, MODE_KEY, "f32",
                 p_mask=0.3),
+    # A 128-query block at the end of a 65536-key sequence (causal mask aligned at the
+    # last key), 8 heads: one query tile per head, so the keys are split into ranges.
+    7: Workload("b1h8_nq128_nk65536_d128_causal_splitkv", 1, 8, 128, 128, 128, MODE_CAUSAL,
+                "bf16", Nk=65536, split_kv=True),
 }
 
 
@@ -189,17 +199,19 @@ def key_bias(seed_c: int, seed_mask: int, BH: int, Nk: int, p_mask: float, std: 
 
 def make_inputs(w: Workload, workload_id: int, base: int = BASE_SEED) -> dict:
     """Seeded inputs of workload `w`: Q, K, V as bf16 bit arrays, C fp32 or None."""
-    BH, N = w.BH, w.N
+    BH, N, Nk = w.BH, w.N, w.Nkv
     Q = bf16_tensor(seed_for(workload_id, "Q", base), (BH, N, w.d), w.qk_mult)
-    K = bf16_tensor(seed_for(workload_id, "K", base), (BH, N, w.d), w.qk_mult)
-    V = bf16_tensor(seed_for(workload_id, "V", base), (BH, N, w.dv))
+    K = bf16_tensor(seed_for(workload_id, "K", base), (BH, Nk, w.d), w.qk_mult)
+    V = bf16_tensor(seed_for(workload_id, "V", base), (BH, Nk, w.dv))
     C = ckey = None
     if w.mode & MODE_DENSE:
+        if Nk != N:
+            raise ValueError("the dense-bias recipe is square (Nq = Nk)")
         C = dense_bias(seed_for(workload_id, "C", base), seed_for(workload_id, "mask", base),
                        BH, N, w.p_mask)
     if w.mode & MODE_KEY:
         ckey = key_bias(seed_for(workload_id, "ckey", base), seed_for(workload_id, "mask", base),
-                        BH, N, w.p_mask)
+                        BH, Nk, w.p_mask)
     return {"Q": Q, "K": K, "V": V, "C": C, "ckey": ckey, "scale": w.scale, "mode": w.mode}
 
 

@@ -155,3 +155,59 @@ def test_ex_zero_queries_is_noop_and_key_mode_needs_ex():
 def test_valid_ex_call_without_gpu_reports_no_device():
     assert call_ex() == eta.ATTN_ERR_NO_DEVICE
     assert call_ex(mode=5, ckey=KP) == eta.ATTN_ERR_NO_DEVICE
+
+
+# ---------------------------------------------------------------- split forward pass
+WP = 0x900000
+
+
+def call_split(n_splits=3, workspace=WP, workspace_bytes=1 << 30, **over):
+    a = dict(GOOD_EX)
+    a.update(over)
+    return eta.attn_fwd_splitkv_raw(a["Q"], a["K"], a["V"], a["mode"], a["C"], a["ckey"], a["BH"],
+                                    a["Nq"], a["Nk"], a["d"], a["d_v"], a["scale"], n_splits,
+                                    workspace, workspace_bytes, a["O"], a["out_dtype"], a["LSE"],
+                                    a["stream"])
+
+
+@pytest.mark.parametrize("nk,req,splits", [
+    (64, 1, 1), (64, 5, 1), (1000, 1, 1), (1000, 3, 3), (1000, 5, 4), (1000, 8, 8),
+    (1000, 100, 8), (65536, 19, 19), (65536, 7, 7), (129, 2, 2), (129, 3, 2),
+])
+def test_splitkv_plan_rounds_to_whole_tiles(nk, req, splits):
+    code, s, nbytes = eta.attn_fwd_splitkv_plan(1, 4, 100, nk, 128, 64, req)
+    assert code == eta.ATTN_OK
+    assert s == splits
+    # ceil(tiles / ceil(tiles / req)) ranges; fp32 partial O and LSE per range and row.
+    tiles = -(-nk // 128)
+    assert s == -(-tiles // -(-tiles // min(req, tiles)))
+    assert nbytes == (0 if s == 1 else s * 4 * 100 * (64 + 1) * 4)
+
+
+def test_splitkv_plan_rejects_what_the_call_rejects():
+    assert eta.attn_fwd_splitkv_plan(8, 1, 1, 1, 64, 64, 2)[0] == eta.ATTN_ERR_INVALID_ARG
+    assert eta.attn_fwd_splitkv_plan(0, 1, 1, 0, 64, 64, 2)[0] == eta.ATTN_ERR_INVALID_ARG
+    assert eta.attn_fwd_splitkv_plan(0, 1, 1, 1, 96, 64, 2)[0] == eta.ATTN_ERR_UNSUPPORTED
+    assert eta.attn_fwd_splitkv_plan(0, 1, 1, 1, 64, 64, -1)[0] == eta.ATTN_ERR_INVALID_ARG
+    assert eta.attn_fwd_splitkv_plan(0, 1, 0, 5, 64, 64, 2)[:2] == (eta.ATTN_OK, 1)
+
+
+@pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
+def test_splitkv_automatic_plan_needs_a_device():
+    assert eta.attn_fwd_splitkv_plan(0, 1, 1, 4096, 64, 64, 0)[0] == eta.ATTN_ERR_NO_DEVICE
+
+
+@pytest.mark.parametrize("over", [
+    dict(n_splits=-1), dict(mode=8), dict(Nk=0), dict(O=KP), dict(mode=4, ckey=None),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_invalid_arguments_splitkv(over):
+    assert call_split(**over) == eta.ATTN_ERR_INVALID_ARG
+
+
+def test_splitkv_zero_queries_is_noop():
+    assert call_split(Nq=0, Q=None, K=None, V=None, O=None, LSE=None, workspace=None) == eta.ATTN_OK
+
+
+@pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
+def test_valid_splitkv_call_without_gpu_reports_no_device():
+    assert call_split(Nk=1000) == eta.ATTN_ERR_NO_DEVICE

@@ -1,22 +1,34 @@
-"""The synthetic benchmark workloads at full size, launched exactly as bench.py
-launches them, against the oracle on sampled rows (the oracle computes rows one by
-one), plus properties that hold at any size (every output written and finite)."""
+"""The synthetic benchmark workloads at full size, launched exactly as bench.py launches
+them (exact_tiled_attention_13_gb300.workload.DeviceWorkload), against the oracle on
+sampled rows (the oracle computes rows one by one), plus properties that hold at any
+size (every output written and finite)."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_helpers import compare, run_gpu, sample_rows
+from gpu_helpers import compare, sample_rows
 
 pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("wid", sorted(synth.WORKLOADS))
 def test_workload_sampled_parity(wid):
-    w = synth.WORKLOADS[wid]
-    c = synth.make_inputs(w, wid)
-    out_f32 = w.out_dtype == "f32"
-    O, L = run_gpu(c, out_f32=out_f32)
+    import torch
+
+    import exact_tiled_attention_13_gb300 as eta
+    from exact_tiled_attention_13_gb300.workload import DeviceWorkload
+
+    wl = DeviceWorkload(wid)
+    w, c = wl.w, wl.host
+    wl.O.fill_(float("nan"))
+    wl.LSE.fill_(float("nan"))
+    wl.launch()
+    torch.cuda.synchronize()
+    code, word = eta.attn_device_status(None)
+    assert code == eta.ATTN_OK, f"device watchdog tripped: {word:#x}"
+    O = wl.O.float().cpu().numpy().astype(np.float64)
+    L = wl.LSE.cpu().numpy().astype(np.float64)
     assert np.isfinite(O).all() and np.isfinite(L).all(), "unwritten (NaN) or non-finite output"
     if w.BH * w.N <= 4096:
         rows = np.arange(w.BH * w.N, dtype=np.int64)
@@ -26,5 +38,5 @@ def test_workload_sampled_parity(wid):
     O_ref, L_ref, _ = oracle.attention_ex(c["Q"], c["K"], c["V"], w.mode, c["C"], c["ckey"],
                                           w.scale, rows=rows)
     stats = compare(O.reshape(-1, w.dv)[rows], L.reshape(-1)[rows], O_ref, L_ref,
-                    out_bf16=not out_f32, label=w.name)
+                    out_bf16=w.out_dtype != "f32", label=w.name)
     print(w.name, len(rows), "rows", stats)
