@@ -24,6 +24,7 @@ SOURCES = [
     "attn_inst_d64_dv128.cu",
     "attn_inst_d128_dv64.cu",
     "attn_inst_d128_dv128.cu",
+    "attn_static_scratch.cu",
 ]
 HEADERS = ["attn_fwd_kernel.cuh", "attn_merge_kernel.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

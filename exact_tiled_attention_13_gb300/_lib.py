@@ -22,6 +22,8 @@ ATTN_ERR_UNSUPPORTED_DEVICE = -4
 ATTN_ERR_LAUNCH = -5
 ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_CUDA = -7
+ATTN_ERR_SCRATCH_LIMIT = -8
+ATTN_STATIC_SCRATCH_BYTES = 33554432
 
 ATTN_FAULT_NONE = 0
 ATTN_FAULT_SKIP_FIRST_K = 1
@@ -43,6 +45,10 @@ SIGNATURES = {
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                              ctypes.c_int, ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_ulonglong)]),
+    "attn_fwd_splitkv_static": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_float, ctypes.c_int, _P,
+                                               ctypes.c_int, _P, _P]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
@@ -108,6 +114,15 @@ def attn_fwd_splitkv_raw(Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, n_sp
     return load().attn_fwd_splitkv(Q, K, V, int(mode), C, ckey, int(BH), int(Nq), int(Nk), int(d),
                                    int(d_v), float(scale), int(n_splits), workspace,
                                    int(workspace_bytes), O, int(out_dtype), LSE, stream)
+
+
+def attn_fwd_splitkv_static_raw(Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, n_splits, O,
+                                out_dtype, LSE, stream) -> int:
+    """attn_fwd_splitkv_static (partials in the library's fixed array) with plain integers
+    as pointers; returns its code unchanged."""
+    return load().attn_fwd_splitkv_static(Q, K, V, int(mode), C, ckey, int(BH), int(Nq), int(Nk),
+                                          int(d), int(d_v), float(scale), int(n_splits), O,
+                                          int(out_dtype), LSE, stream)
 
 
 def attn_fwd_splitkv_plan(mode, BH, Nq, Nk, d, d_v, n_splits=0):

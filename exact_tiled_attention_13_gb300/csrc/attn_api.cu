@@ -167,6 +167,8 @@ extern "C" const char *attn_strerror(int code) {
     case ATTN_ERR_LAUNCH: return "kernel launch rejected by the CUDA runtime";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a kernel pipeline wait timed out (watchdog tripped)";
     case ATTN_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case ATTN_ERR_SCRATCH_LIMIT:
+      return "the split plan needs more scratch than the library's fixed array (ATTN_STATIC_SCRATCH_BYTES)";
     default: return "unknown error code";
   }
 }

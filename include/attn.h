@@ -58,6 +58,8 @@ extern "C" {
 #define ATTN_ERR_LAUNCH (-5)             /* the kernel launch was rejected by the CUDA runtime */
 #define ATTN_ERR_DEVICE_TIMEOUT (-6)     /* a kernel gave up on a pipeline wait (see attn_device_status) */
 #define ATTN_ERR_CUDA (-7)               /* another CUDA runtime or driver call failed */
+#define ATTN_ERR_SCRATCH_LIMIT (-8)      /* attn_fwd_splitkv_static: the problem needs more scratch
+                                            than ATTN_STATIC_SCRATCH_BYTES */
 
 /*
  * attn_fwd -- O = softmax(Q K^T * scale + C) V and LSE for BH heads, on `stream`.
@@ -159,6 +161,32 @@ ATTN_API int attn_fwd_splitkv(const void *Q, const void *K, const void *V, int m
  */
 ATTN_API int attn_fwd_splitkv_plan(int mode, int BH, int Nq, int Nk, int d, int d_v, int n_splits,
                                    int *splits, unsigned long long *workspace_bytes);
+
+/*
+ * attn_fwd_splitkv_static -- attn_fwd_splitkv for callers that cannot allocate device
+ * memory (the pages have no counterpart: this is a deployment variant of the split
+ * forward pass, not a step of the method). It takes the arguments of attn_fwd_splitkv
+ * without the workspace and keeps its partials in a fixed array inside the library,
+ * ATTN_STATIC_SCRATCH_BYTES (32 MiB) per device. It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   - A problem whose plan (attn_fwd_splitkv_plan with the same arguments) needs more
+ *     than ATTN_STATIC_SCRATCH_BYTES is rejected with ATTN_ERR_SCRATCH_LIMIT before any
+ *     CUDA call (n_splits > 0) or after reading the device's multiprocessor count
+ *     (n_splits == 0). Pass a smaller n_splits to fit; one range needs no scratch.
+ *   - Every call on a device shares the one array. Nothing in it needs to start at
+ *     zero (each call writes every partial it reads), but two calls whose work may
+ *     overlap on the GPU (different streams, or host threads without ordering between
+ *     them) race on it and may return wrong results: order such calls on one stream.
+ *   - The first call on each device looks up the array's address (cudaGetSymbolAddress),
+ *     which loads the library's device code on that device; make that first call with
+ *     the device current and before any stream capture begins.
+ * Returns what attn_fwd_splitkv returns, or ATTN_ERR_SCRATCH_LIMIT.
+ */
+#define ATTN_STATIC_SCRATCH_BYTES 33554432
+ATTN_API int attn_fwd_splitkv_static(const void *Q, const void *K, const void *V, int mode,
+                                     const float *C, const float *ckey, int BH, int Nq, int Nk,
+                                     int d, int d_v, float scale, int n_splits, void *O,
+                                     int out_dtype, float *LSE, void *stream);
 
 /* Static English text for a return code (never NULL). */
 ATTN_API const char *attn_strerror(int code);
