@@ -11,7 +11,9 @@ compilers-kernels), section "FlashAttention rewrites the algorithm around IO":
 S = Q K^T * scale + C, m_i = max_j S_ij, l_i = sum_j exp(S_ij - m_i),
 P = exp(S - m) / l, O = P V; LSE_i = m_i + ln l_i is reported beside O.
 Second, test-only path: the blockwise online recurrence of the same section and
-the (m, l, u) form of "AI Infra ch. 5", section 5.3, Example 5-6.
+the (m, l, u) form of "AI Infra ch. 5", section 5.3, Example 5-6. Backward pass: the
+gradients dQ, dK, dV of that definition by the chain rule, recomputing S and P from
+the kept row statistics (the same section's remark on the backward pass).
 
 Every function is pinned by the ``-m "not gpu"`` tests in tests/test_oracle_pins.py
 (invariants, closed forms, special cases, the pages' worked numbers and brute force).
@@ -84,6 +86,9 @@ def _bind(path: str):
     lib.oracle_online_step.restype = None
     lib.oracle_online_merge.argtypes = [dbl, dbl, p, dbl, dbl, p, i64, p, p, p]
     lib.oracle_online_merge.restype = None
+    lib.oracle_attention_bwd.argtypes = [p, p, p, p, ctypes.c_int, p, p, i64, i64, i64, i64, i64,
+                                         dbl, p, i64, p, i64, p, i64, p, p, p, ctypes.c_int]
+    lib.oracle_attention_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -175,6 +180,44 @@ class Oracle:
             LSE = LSE.reshape(BH, Nq)
         return O, LSE, used
 
+    def attention_bwd(self, Q, K, V, dO, mode, C, ckey, scale, heads=None, qrows=None,
+                      krows=None, nthreads=0):
+        """Gradients of O = softmax(scale Q K^T + C) V for the loss gradient dO (bf16 bits
+        [BH, Nq, dv]): returns (dQ, dK, dV, threads), fp64, shaped [nheads, nq_sel, d],
+        [nheads, nk_sel, d], [nheads, nk_sel, dv] for the selected heads, query rows (dQ)
+        and keys (dK, dV); None selects all of them."""
+        Q, K, V, dO = _bits(Q, 3), _bits(K, 3), _bits(V, 3), _bits(dO, 3)
+        BH, Nq, d = Q.shape
+        Nk, dv = K.shape[1], V.shape[2]
+        if K.shape != (BH, Nk, d) or V.shape[:2] != (BH, Nk) or dO.shape != (BH, Nq, dv):
+            raise ValueError("inconsistent Q/K/V/dO shapes")
+        Cc = kk = None
+        if mode & MODE_DENSE:
+            Cc = np.ascontiguousarray(C, dtype=np.float32)
+            if Cc.shape != (BH, Nq, Nk):
+                raise ValueError("C must be [BH, Nq, Nk]")
+        if mode & MODE_KEY:
+            kk = np.ascontiguousarray(ckey, dtype=np.float32)
+            if kk.shape != (BH, Nk):
+                raise ValueError("ckey must be [BH, Nk]")
+
+        def sel(a, n):
+            return (None, n) if a is None else (np.ascontiguousarray(a, dtype=np.int64), len(a))
+
+        h_arr, nh = sel(heads, BH)
+        q_arr, nq = sel(qrows, Nq)
+        k_arr, nk = sel(krows, Nk)
+        dQ = np.empty((nh, nq, d))
+        dK = np.empty((nh, nk, d))
+        dV = np.empty((nh, nk, dv))
+        used = self.lib.oracle_attention_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(dO), int(mode),
+                                             _ptr(Cc), _ptr(kk), BH, Nq, Nk, d, dv, float(scale),
+                                             _ptr(h_arr), nh, _ptr(q_arr), nq, _ptr(k_arr), nk,
+                                             _ptr(dQ), _ptr(dK), _ptr(dV), int(nthreads))
+        if used < 0:
+            raise ValueError("oracle_attention_bwd rejected its arguments")
+        return dQ, dK, dV, used
+
     def attention_head(self, Q, K, V, mode, C, scale):
         """S, P (fp64 [N, N]), O ([N, dv]) and LSE ([N]) of one head, all materialised."""
         Q, K, V = _bits(Q, 2), _bits(K, 2), _bits(V, 2)
@@ -251,6 +294,10 @@ def attention(*args, **kwargs):
 
 def attention_ex(*args, **kwargs):
     return default().attention_ex(*args, **kwargs)
+
+
+def attention_bwd(*args, **kwargs):
+    return default().attention_bwd(*args, **kwargs)
 
 
 def attention_head(*args, **kwargs):

@@ -365,3 +365,265 @@ void oracle_online_merge(double m1, double l1, const double *u1, double m2, doub
         u[c] = a1 * u1[c] + a2 * u2[c];
     *m = mm;
 }
+
+/* ------------------------------------------------------------------------------
+ * Backward pass (test infrastructure, like everything above).
+ *
+ * The pages state that the backward pass of the tiled method recomputes the local
+ * score and probability blocks from Q, K and the kept softmax statistics instead of
+ * storing them ("Compilers and kernels", section "FlashAttention rewrites the
+ * algorithm around IO", the paragraph after the recurrence). The gradients themselves
+ * are those of the forward display; for a loss whose gradient with respect to O is dO,
+ * the chain rule through O = P V, the row softmax P = softmax(S) and
+ * S = scale Q K^T + C gives
+ *
+ *     dV   = P^T dO
+ *     dP   = dO V^T
+ *     D_i  = sum_j P_ij dP_ij
+ *     dS_ij = P_ij (dP_ij - D_i)        (the softmax Jacobian, row by row)
+ *     dQ   = scale dS K,    dK = scale dS^T Q.
+ *
+ * The oracle evaluates them in two passes per head. Pass 1, per query row i: the row
+ * of S and P by the definition (attention_row), the row of dP, D_i, and dQ_i; it keeps
+ * m_i, l_i and D_i. Pass 2, per key j: S_ij and P_ij = exp(S_ij - m_i) / l_i for every
+ * query row i again, then dV_j and dK_j. A row with no allowed key has P = 0, so it
+ * contributes nothing (its output is the constant 0).
+ * ------------------------------------------------------------------------------ */
+
+typedef struct {
+    const problem_t *p;
+    const uint16_t *dO; /* bf16 bits [BH][Nq][dv] */
+    int64_t bh;
+    const int64_t *qrows; /* rows of this head for dQ, or NULL for all */
+    int64_t nq_sel;
+    const int64_t *krows; /* keys of this head for dK, dV, or NULL for all */
+    int64_t nk_sel;
+    double *m, *l, *D; /* [Nq] each: row max, row sum, D_i */
+    double *dQ;        /* [nq_sel][d] */
+    double *dK, *dV;   /* [nk_sel][d], [nk_sel][dv] */
+    int pass;
+    int64_t next, total;
+    int failed;
+    pthread_mutex_t lock;
+} bwd_job_t;
+
+/* Pass 1 for query row i: m_i, l_i, D_i, and dQ_i when `dq` is not NULL. */
+static int bwd_row(const bwd_job_t *job, int64_t i, double *S_row, double *P_row, double *O_row,
+                   double *dP_row, double *dq)
+{
+    const problem_t *p = job->p;
+    const int64_t bh = job->bh, Nk = p->Nk, d = p->d, dv = p->dv;
+    double lse;
+    attention_row(p, bh, i, S_row, P_row, O_row, &lse);
+    double m = -INFINITY;
+    for (int64_t j = 0; j < Nk; j++)
+        if (S_row[j] > m)
+            m = S_row[j];
+    double l = 0.0; /* l_i = sum_j exp(S_ij - m_i), kept for pass 2 */
+    for (int64_t j = 0; m != -INFINITY && j < Nk; j++) {
+        const double e = exp(S_row[j] - m);
+        l += e;
+    }
+    job->m[i] = m;
+    job->l[i] = l;
+
+    const uint16_t *go = job->dO + (bh * p->Nq + i) * dv;
+    double D = 0.0;
+    for (int64_t j = 0; j < Nk; j++) {
+        const uint16_t *v = p->V + (bh * Nk + j) * dv;
+        double acc = 0.0;
+        for (int64_t c = 0; c < dv; c++)
+            acc += bf16_value(go[c]) * bf16_value(v[c]);
+        dP_row[j] = acc;
+        D += P_row[j] * acc;
+    }
+    job->D[i] = D;
+    if (dq) {
+        for (int64_t c = 0; c < d; c++)
+            dq[c] = 0.0;
+        for (int64_t j = 0; j < Nk; j++) {
+            const double ds = P_row[j] * (dP_row[j] - D);
+            const uint16_t *k = p->K + (bh * Nk + j) * d;
+            for (int64_t c = 0; c < d; c++)
+                dq[c] += ds * bf16_value(k[c]);
+        }
+        for (int64_t c = 0; c < d; c++)
+            dq[c] *= p->scale;
+    }
+    return 0;
+}
+
+/* Pass 2 for key j: dK_j and dV_j over every query row of the head. */
+static void bwd_key(const bwd_job_t *job, int64_t j, double *dk, double *dv_out)
+{
+    const problem_t *p = job->p;
+    const int64_t bh = job->bh, Nk = p->Nk, d = p->d, dv = p->dv;
+    const uint16_t *k = p->K + (bh * Nk + j) * d;
+    const uint16_t *v = p->V + (bh * Nk + j) * dv;
+    for (int64_t c = 0; c < d; c++)
+        dk[c] = 0.0;
+    for (int64_t c = 0; c < dv; c++)
+        dv_out[c] = 0.0;
+    for (int64_t i = 0; i < p->Nq; i++) {
+        if (job->m[i] == -INFINITY)
+            continue; /* no allowed key in row i: P_i = 0 */
+        const uint16_t *q = p->Q + (bh * p->Nq + i) * d;
+        const uint16_t *go = job->dO + (bh * p->Nq + i) * dv;
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; c++)
+            dot += bf16_value(q[c]) * bf16_value(k[c]);
+        const double s = p->scale * dot + bias_value(p, bh, i, j);
+        const double P = exp(s - job->m[i]) / job->l[i];
+        double dP = 0.0;
+        for (int64_t c = 0; c < dv; c++)
+            dP += bf16_value(go[c]) * bf16_value(v[c]);
+        const double ds = P * (dP - job->D[i]);
+        for (int64_t c = 0; c < d; c++)
+            dk[c] += ds * bf16_value(q[c]);
+        for (int64_t c = 0; c < dv; c++)
+            dv_out[c] += P * bf16_value(go[c]);
+    }
+    for (int64_t c = 0; c < d; c++)
+        dk[c] *= p->scale;
+}
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job_t *job = (bwd_job_t *)arg;
+    const problem_t *p = job->p;
+    const size_t n = (size_t)(p->Nk > p->dv ? p->Nk : p->dv);
+    double *buf = (double *)malloc(sizeof(double) * (3 * (size_t)p->Nk + n));
+    if (!buf) {
+        pthread_mutex_lock(&job->lock);
+        job->failed = 1;
+        pthread_mutex_unlock(&job->lock);
+        return NULL;
+    }
+    double *S_row = buf, *P_row = buf + p->Nk, *dP_row = buf + 2 * p->Nk, *O_row = buf + 3 * p->Nk;
+    for (;;) {
+        pthread_mutex_lock(&job->lock);
+        int64_t r = job->next;
+        job->next += 8;
+        pthread_mutex_unlock(&job->lock);
+        if (r >= job->total)
+            break;
+        int64_t end = r + 8 < job->total ? r + 8 : job->total;
+        for (; r < end; r++) {
+            if (job->pass == 1) {
+                /* every row i for m, l, D; dQ for the selected ones (pass 1 runs rows
+                   in order, the selection is matched below) */
+                bwd_row(job, r, S_row, P_row, O_row, dP_row, NULL);
+            } else if (job->pass == 2) {
+                int64_t i = job->qrows ? job->qrows[r] : r;
+                bwd_row(job, i, S_row, P_row, O_row, dP_row, job->dQ + r * p->d);
+            } else {
+                int64_t j = job->krows ? job->krows[r] : r;
+                bwd_key(job, j, job->dK + r * p->d, job->dV + r * p->dv);
+            }
+        }
+    }
+    free(buf);
+    return NULL;
+}
+
+static int bwd_run(bwd_job_t *job, int pass, int64_t total, int nthreads)
+{
+    job->pass = pass;
+    job->next = 0;
+    job->total = total;
+    int64_t units = (total + 7) / 8;
+    if (nthreads > units)
+        nthreads = units > 0 ? (int)units : 1;
+    pthread_t *tid = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    int started = 0;
+    for (int t = 0; tid && t < nthreads; t++) {
+        if (pthread_create(&tid[t], NULL, bwd_worker, job) != 0)
+            break;
+        started++;
+    }
+    if (started == 0)
+        bwd_worker(job);
+    for (int t = 0; t < started; t++)
+        pthread_join(tid[t], NULL);
+    free(tid);
+    return started > 0 ? started : 1;
+}
+
+/*
+ * Gradients dQ, dK, dV of the attention output for the loss gradient dO.
+ *   Q, K, V, mode, C, ckey, BH, Nq, Nk, d, dv, scale: as oracle_attention_ex
+ *   dO      : bf16 bit patterns, row-major [BH][Nq][dv]
+ *   heads   : heads to evaluate (nheads of them), or NULL for all BH
+ *   qrows   : query rows (within a head) whose dQ is wanted, or NULL for all Nq
+ *   krows   : keys (within a head) whose dK and dV are wanted, or NULL for all Nk
+ *   dQ      : fp64 [nheads][nq_sel][d];  dK: [nheads][nk_sel][d];  dV: [nheads][nk_sel][dv]
+ *   nthreads: worker threads; <= 0 means every online core
+ * Every head is evaluated on its own, rows and keys in a fixed order, so the result
+ * does not depend on the thread count or on the selection.
+ * Returns the number of threads used, or -1 on bad arguments / allocation failure.
+ */
+int oracle_attention_bwd(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                         const uint16_t *dO, int mode, const float *C, const float *ckey,
+                         int64_t BH, int64_t Nq, int64_t Nk, int64_t d, int64_t dv, double scale,
+                         const int64_t *heads, int64_t nheads, const int64_t *qrows,
+                         int64_t nq_sel, const int64_t *krows, int64_t nk_sel, double *dQ,
+                         double *dK, double *dV, int nthreads)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV || BH < 1 || Nq < 1 || Nk < 1 || d < 1 ||
+        dv < 1)
+        return -1;
+    if (mode & ~(ORACLE_CAUSAL | ORACLE_DENSE | ORACLE_KEY))
+        return -1;
+    if (((mode & ORACLE_DENSE) && !C) || ((mode & ORACLE_KEY) && !ckey))
+        return -1;
+    if (!heads)
+        nheads = BH;
+    if (!qrows)
+        nq_sel = Nq;
+    if (!krows)
+        nk_sel = Nk;
+    for (int64_t h = 0; heads && h < nheads; h++)
+        if (heads[h] < 0 || heads[h] >= BH)
+            return -1;
+    for (int64_t r = 0; qrows && r < nq_sel; r++)
+        if (qrows[r] < 0 || qrows[r] >= Nq)
+            return -1;
+    for (int64_t r = 0; krows && r < nk_sel; r++)
+        if (krows[r] < 0 || krows[r] >= Nk)
+            return -1;
+    if (nthreads <= 0) {
+        long n = sysconf(_SC_NPROCESSORS_ONLN);
+        nthreads = n > 0 ? (int)n : 1;
+    }
+
+    problem_t p = {Q, K, V, C, ckey, mode, BH, Nq, Nk, d, dv, scale};
+    double *stats = (double *)malloc(sizeof(double) * 3 * (size_t)Nq);
+    if (!stats)
+        return -1;
+    bwd_job_t job;
+    memset(&job, 0, sizeof job);
+    job.p = &p;
+    job.dO = dO;
+    job.qrows = qrows;
+    job.nq_sel = nq_sel;
+    job.krows = krows;
+    job.nk_sel = nk_sel;
+    job.m = stats;
+    job.l = stats + Nq;
+    job.D = stats + 2 * Nq;
+    pthread_mutex_init(&job.lock, NULL);
+    int used = 1;
+    for (int64_t h = 0; h < nheads; h++) {
+        job.bh = heads ? heads[h] : h;
+        job.dQ = dQ + h * nq_sel * d;
+        job.dK = dK + h * nk_sel * d;
+        job.dV = dV + h * nk_sel * dv;
+        int u = bwd_run(&job, 1, Nq, nthreads); /* m, l, D of every row */
+        used = u > used ? u : used;
+        bwd_run(&job, 2, nq_sel, nthreads);     /* dQ of the selected rows */
+        bwd_run(&job, 3, nk_sel, nthreads);     /* dK, dV of the selected keys */
+    }
+    pthread_mutex_destroy(&job.lock);
+    free(stats);
+    return job.failed ? -1 : used;
+}

@@ -527,6 +527,155 @@ def pin_bruteforce_rectangular(orc):
             assert abs(L[0, i] - float(mpmath.log(tot))) <= 1e-13 * max(1.0, abs(float(mpmath.log(tot))))
 
 
+# ---------------------------------------------------------------- backward pass
+KEY = synth.MODE_KEY
+
+
+def _bwd_case(seed, BH, Nq, Nk, d, dv, mode, p_mask=0.0):
+    c = _case_ex(seed, BH, Nq, Nk, d, dv, mode, p_mask)
+    c["dO"] = synth.bf16_tensor(seed + 17, (BH, Nq, dv))
+    return c
+
+
+def _bwd(orc, c, **kw):
+    return orc.attention_bwd(c["Q"], c["K"], c["V"], c["dO"], c["mode"], c["C"], c["ckey"],
+                             c["scale"], **kw)
+
+
+def pin_bwd_finite_differences(orc):
+    """Every gradient entry equals the central difference of the loss sum(dO * O) in
+    60-digit arithmetic (step 1e-20), on tiny problems of every mask kind, queries
+    and keys of their own lengths: <= 1e-11 relative."""
+    import mpmath
+
+    mpmath.mp.dps = 60
+    h = mpmath.mpf("1e-20")
+    for seed, Nq, Nk, mode, p_mask in ((11, 3, 4, NONE, 0.0), (12, 3, 4, CAUSAL, 0.0),
+                                       (13, 4, 3, CAUSAL, 0.0), (14, 3, 4, DENSE, 0.3),
+                                       (15, 3, 5, KEY | CAUSAL, 0.3)):
+        d, dv = 3, 2
+        c = _bwd_case(seed, 1, Nq, Nk, d, dv, mode, p_mask)
+        dQ, dK, dV, _ = _bwd(orc, c)
+        Qv, Kv, Vv, G = (_vals(c[k])[0] for k in ("Q", "K", "V", "dO"))
+        sc = mpmath.mpf(c["scale"])
+
+        def loss(Qm, Km, Vm):
+            tot = mpmath.mpf(0)
+            for i in range(Nq):
+                w = []
+                for j in range(Nk):
+                    if (mode & CAUSAL) and j > i + (Nk - Nq):
+                        w.append(None)
+                        continue
+                    sij = sc * mpmath.fsum(Qm[i][k] * Km[j][k] for k in range(d))
+                    if mode & DENSE:
+                        cij = float(c["C"][0, i, j])
+                        if cij == -math.inf:
+                            w.append(None)
+                            continue
+                        sij += mpmath.mpf(cij)
+                    if mode & KEY:
+                        cj = float(c["ckey"][0, j])
+                        if cj == -math.inf:
+                            w.append(None)
+                            continue
+                        sij += mpmath.mpf(cj)
+                    w.append(sij)
+                live = [x for x in w if x is not None]
+                if not live:
+                    continue
+                e = [mpmath.exp(x) if x is not None else mpmath.mpf(0) for x in w]
+                z = mpmath.fsum(e)
+                for col in range(dv):
+                    o = mpmath.fsum(e[j] * Vm[j][col] for j in range(Nk)) / z
+                    tot += mpmath.mpf(float(G[i, col])) * o
+            return tot
+
+        base = {"Q": [[mpmath.mpf(float(x)) for x in r] for r in Qv],
+                "K": [[mpmath.mpf(float(x)) for x in r] for r in Kv],
+                "V": [[mpmath.mpf(float(x)) for x in r] for r in Vv]}
+        for name, grad in (("Q", dQ[0]), ("K", dK[0]), ("V", dV[0])):
+            for r in range(grad.shape[0]):
+                for col in range(grad.shape[1]):
+                    plus = {k: [list(row) for row in v] for k, v in base.items()}
+                    minus = {k: [list(row) for row in v] for k, v in base.items()}
+                    plus[name][r][col] += h
+                    minus[name][r][col] -= h
+                    fd = float((loss(plus["Q"], plus["K"], plus["V"]) -
+                                loss(minus["Q"], minus["K"], minus["V"])) / (2 * h))
+                    assert abs(grad[r, col] - fd) <= 1e-11 * max(1.0, abs(fd)), (
+                        name, seed, r, col, grad[r, col], fd)
+
+
+def pin_bwd_key_gradients_sum_to_zero(orc):
+    """Adding one vector to every key adds a constant to each row of S (softmax does not
+    change), so the key gradients of a head sum to zero, for every mask kind."""
+    for seed, Nq, Nk, mode, pm in ((21, 40, 40, NONE, 0.0), (22, 33, 70, CAUSAL, 0.0),
+                                   (23, 50, 30, CAUSAL, 0.0), (24, 20, 45, DENSE, 0.3),
+                                   (25, 31, 64, KEY | CAUSAL, 0.3)):
+        c = _bwd_case(seed, 2, Nq, Nk, 16, 8, mode, pm)
+        dQ, dK, dV, _ = _bwd(orc, c)
+        scale = np.abs(dK).max()
+        assert np.abs(dK.sum(axis=1)).max() <= 1e-12 * max(1.0, scale) * Nk, (seed, dK.sum(axis=1))
+
+
+def pin_bwd_value_gradients_sum_to_dO(orc):
+    """Rows of P sum to 1, so sum_j dV_j = sum over rows with an allowed key of dO_i."""
+    for seed, Nq, Nk, mode in ((31, 40, 40, NONE), (32, 50, 30, CAUSAL), (33, 17, 64, KEY)):
+        c = _bwd_case(seed, 2, Nq, Nk, 16, 8, mode, 0.3 if mode & KEY else 0.0)
+        dQ, dK, dV, _ = _bwd(orc, c)
+        G = _vals(c["dO"])
+        live = np.ones((2, Nq), dtype=bool)
+        if mode & CAUSAL and Nq > Nk:
+            live[:, :Nq - Nk] = False  # rows that see no key
+        want = (G * live[:, :, None]).sum(axis=1)
+        assert np.abs(dV.sum(axis=1) - want).max() <= 1e-12 * Nq, seed
+
+
+def pin_bwd_uniform_weights(orc):
+    """Q = 0 and no mask: P_ij = 1/Nk, so dV_j = mean_i-free sum_i dO_i / Nk, dK = 0, and
+    dQ_i = scale / Nk * sum_j (dO_i . (v_j - vbar)) k_j (closed form)."""
+    c = _bwd_case(41, 1, 12, 20, 8, 6, NONE)
+    c["Q"] = np.zeros_like(c["Q"])
+    dQ, dK, dV, _ = _bwd(orc, c)
+    K, V, G = _vals(c["K"])[0], _vals(c["V"])[0], _vals(c["dO"])[0]
+    Nk = K.shape[0]
+    assert np.abs(dV[0] - G.sum(axis=0)[None, :] / Nk).max() <= 1e-14
+    assert np.abs(dK).max() == 0.0
+    vbar = V.mean(axis=0)
+    want = c["scale"] / Nk * ((G @ (V - vbar).T) @ K)
+    assert np.abs(dQ[0] - want).max() <= 1e-13
+
+
+def pin_bwd_single_and_no_key_rows(orc):
+    """A row with one allowed key has a one-hot P, so dS_i = 0 and dQ_i = 0; a row with no
+    allowed key (Nq > Nk, causal) has the constant output 0 and gradient 0 everywhere."""
+    c = _bwd_case(51, 1, 20, 20, 8, 8, CAUSAL)
+    dQ, dK, dV, _ = _bwd(orc, c)
+    assert np.all(dQ[0, 0] == 0.0)  # query 0 sees key 0 only
+    c = _bwd_case(52, 1, 30, 10, 8, 8, CAUSAL)
+    dQ, dK, dV, _ = _bwd(orc, c)
+    assert np.all(dQ[0, :20] == 0.0) and np.all(dQ[0, 20] == 0.0)  # none, then one key
+    # The keyless rows' dO does not reach dV or dK.
+    c2 = dict(c)
+    c2["dO"] = c["dO"].copy()
+    c2["dO"][0, :20] = synth.bf16_tensor(999, (20, 8))
+    _, dK2, dV2, _ = _bwd(orc, c2)
+    assert np.array_equal(dK, dK2) and np.array_equal(dV, dV2)
+
+
+def pin_bwd_selection_and_threads(orc):
+    """Selected heads, query rows and keys, and any thread count, give the same bits."""
+    c = _bwd_case(61, 3, 37, 45, 8, 16, CAUSAL | KEY, 0.2)
+    dQ, dK, dV, _ = _bwd(orc, c, nthreads=1)
+    heads, qr, kr = [2, 0], [36, 0, 17], [44, 3, 3, 10]
+    sQ, sK, sV, _ = _bwd(orc, c, heads=heads, qrows=qr, krows=kr, nthreads=3)
+    assert np.array_equal(sQ, dQ[heads][:, qr]) and np.array_equal(sK, dK[heads][:, kr])
+    assert np.array_equal(sV, dV[heads][:, kr])
+    tQ, tK, tV, _ = _bwd(orc, c, nthreads=7)
+    assert np.array_equal(tQ, dQ) and np.array_equal(tK, dK) and np.array_equal(tV, dV)
+
+
 ALL_PINS = [
     pin_p_rows_sum_to_one,
     pin_constant_v,
@@ -550,4 +699,10 @@ ALL_PINS = [
     pin_causal_offset,
     pin_bias_terms_add,
     pin_bruteforce_rectangular,
+    pin_bwd_finite_differences,
+    pin_bwd_key_gradients_sum_to_zero,
+    pin_bwd_value_gradients_sum_to_dO,
+    pin_bwd_uniform_weights,
+    pin_bwd_single_and_no_key_rows,
+    pin_bwd_selection_and_threads,
 ]

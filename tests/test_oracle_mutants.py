@@ -50,6 +50,22 @@ MUTANTS = {
     "step_r_not_applied_to_l": ("*l = r * *l + p;", "*l = *l + p;"),
     "step_p_relative_to_old_max": ("double p = exp(s - m_new);", "double p = exp(s - *m);"),
     "merge_weights_swapped": ("*l = a1 * l1 + a2 * l2;", "*l = a2 * l1 + a1 * l2;"),
+    "bwd_row_D_dropped": ("const double ds = P_row[j] * (dP_row[j] - D);",
+                          "const double ds = P_row[j] * dP_row[j];"),
+    "bwd_key_D_dropped": ("const double ds = P * (dP - job->D[i]);", "const double ds = P * dP;"),
+    "bwd_D_not_weighted_by_P": ("D += P_row[j] * acc;", "D += acc;"),
+    "bwd_dQ_scale_dropped": ("dq[c] *= p->scale;", "dq[c] *= 1.0;"),
+    "bwd_dK_scale_dropped": ("dk[c] *= p->scale;", "dk[c] *= 1.0;"),
+    "bwd_dK_from_keys": ("dk[c] += ds * bf16_value(q[c]);", "dk[c] += ds * bf16_value(k[c]);"),
+    "bwd_dQ_from_queries": ("dq[c] += ds * bf16_value(k[c]);",
+                            "dq[c] += ds * bf16_value(p->Q[(bh * p->Nq + i) * d + c]);"),
+    "bwd_dV_from_dP": ("dv_out[c] += P * bf16_value(go[c]);", "dv_out[c] += dP * bf16_value(go[c]);"),
+    "bwd_key_pass_bias_dropped": ("const double s = p->scale * dot + bias_value(p, bh, i, j);",
+                                  "const double s = p->scale * dot;"),
+    "bwd_key_pass_unnormalised": ("const double P = exp(s - job->m[i]) / job->l[i];",
+                                  "const double P = exp(s - job->m[i]);"),
+    "bwd_dP_with_keys": ("acc += bf16_value(go[c]) * bf16_value(v[c]);",
+                         "acc += bf16_value(go[c]) * bf16_value(p->K[(bh * Nk + j) * d + c % d]);"),
 }
 
 _CHILD = r"""
