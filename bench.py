@@ -207,6 +207,12 @@ def recorded_traffic(workload_id: int):
 
 def workload_figures(w):
     causal = bool(w.mode & synth.MODE_CAUSAL)
+    if w.backward:
+        F = accounting.bwd_flops(w.BH, w.N, w.d, w.dv, causal, Nk=w.Nkv)
+        B = accounting.bwd_required_bytes(w.BH, w.N, w.d, w.dv, 4 if w.out_dtype == "f32" else 2,
+                                          dense_bias=bool(w.mode & synth.MODE_DENSE),
+                                          key_bias=bool(w.mode & synth.MODE_KEY), Nk=w.Nkv)
+        return F, B
     F = accounting.flops(w.BH, w.N, w.d, w.dv, causal, Nk=w.Nkv)
     B = accounting.required_bytes(w.BH, w.N, w.d, w.dv, 4 if w.out_dtype == "f32" else 2, lse=True,
                                   dense_bias=bool(w.mode & synth.MODE_DENSE),
@@ -225,6 +231,9 @@ def config_dict(w, world):
         cfg["N_q"], cfg["N_k"] = w.N, w.Nkv
     if w.split_kv:
         cfg["split_kv"] = "key ranges chosen by the library for this GPU, then a merge kernel"
+    if w.backward:
+        cfg["pass"] = ("backward: dQ, dK, dV (fp32) from Q, K, V, O, LSE of one forward pass "
+                       "and a seeded bf16 dO; FLOPs of the five products, recomputation not counted")
     return cfg
 
 
@@ -233,8 +242,13 @@ def needs_flush(w) -> bool:
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+def sample_units(w) -> int:
+    """Units of the CPU sample: query rows (forward) or whole heads (backward)."""
+    return w.BH if w.backward else w.BH * w.N
+
+
 def oracle_rows(w, nrows: int) -> np.ndarray:
-    total = w.BH * w.N
+    total = sample_units(w)
     nrows = max(1, min(nrows, total))
     return np.unique(np.linspace(0, total - 1, nrows).astype(np.int64))
 
@@ -242,6 +256,12 @@ def oracle_rows(w, nrows: int) -> np.ndarray:
 def time_oracle(w, inputs, rows):
     import oracle
 
+    if w.backward:  # rows: the heads to evaluate in full
+        t0 = time.perf_counter()
+        _, _, _, threads = oracle.attention_bwd(inputs["Q"], inputs["K"], inputs["V"], inputs["dO"],
+                                                w.mode, inputs["C"], inputs.get("ckey"), w.scale,
+                                                heads=rows)
+        return time.perf_counter() - t0, threads
     t0 = time.perf_counter()
     _, _, threads = oracle.attention_ex(inputs["Q"], inputs["K"], inputs["V"], w.mode, inputs["C"],
                                         inputs.get("ckey"), w.scale, rows=rows)
@@ -250,21 +270,27 @@ def time_oracle(w, inputs, rows):
 
 def cpu_rows_for_seconds(w, inputs, seconds: float) -> int:
     """Rows the oracle finishes in about `seconds` on this host (calibrated on a small sample)."""
-    probe = oracle_rows(w, 64)
+    probe = oracle_rows(w, 1 if w.backward else 64)
     dt, _ = time_oracle(w, inputs, probe)
     rate = len(probe) / max(dt, 1e-6)
-    return int(max(16, min(w.BH * w.N, rate * seconds)))
+    return int(max(1 if w.backward else 16, min(sample_units(w), rate * seconds)))
 
 
 def cpu_baseline(w, inputs, nrows):
     F, _ = workload_figures(w)
     rows = oracle_rows(w, nrows)
     dt, threads = time_oracle(w, inputs, rows)
-    flops = F * len(rows) / (w.BH * w.N)  # the workload's average algorithmic FLOPs per row
+    flops = F * len(rows) / sample_units(w)  # the workload's average algorithmic FLOPs per unit
+    if w.backward:
+        sample = (f"{len(rows)} of the workload's {w.BH} heads in full (dQ, dK, dV), fp64 C oracle "
+                  f"recomputing each row of S and P; FLOPs counted as the per-head average; "
+                  f"{dt:.1f} s wall")
+    else:
+        sample = (f"{len(rows)} query rows evenly strided over all {w.BH} heads x {w.N} rows of the "
+                  f"workload, fp64 C oracle with each row of S and P materialised; FLOPs counted "
+                  f"as the workload's per-row average; {dt:.1f} s wall")
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{len(rows)} query rows evenly strided over all {w.BH} heads x {w.N} rows "
-                      f"of the workload, fp64 C oracle with each row of S and P materialised; "
-                      f"FLOPs counted as the workload's per-row average; {dt:.1f} s wall"}
+            "sample": sample}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -276,7 +302,8 @@ def run_reference(args):
     inputs = synth.make_inputs(w, args.workload)
     F, _ = workload_figures(w)
     total_steps = args.steps + args.warmup
-    rows_per_step = max(8, cpu_rows_for_seconds(w, inputs, 90.0) // max(1, total_steps))
+    rows_per_step = max(1 if w.backward else 8,
+                        cpu_rows_for_seconds(w, inputs, 90.0) // max(1, total_steps))
     rows = oracle_rows(w, rows_per_step)
     for _ in range(args.warmup):
         time_oracle(w, inputs, rows)
@@ -285,11 +312,12 @@ def run_reference(args):
     for _ in range(args.steps):
         _, threads = time_oracle(w, inputs, rows)
     dt = (time.perf_counter() - t0) / args.steps
-    flops = F * len(rows) / (w.BH * w.N)
+    flops = F * len(rows) / sample_units(w)
     value = flops / dt / 1e12
-    sample = (f"{len(rows)} query rows per step, evenly strided over the workload's {w.BH} heads; "
+    unit_name = "whole heads (dQ, dK, dV)" if w.backward else "query rows"
+    sample = (f"{len(rows)} {unit_name} per step, evenly strided over the workload's {w.BH} heads; "
               f"fp64 C oracle materialising each row of S and P; FLOPs counted as the workload's "
-              f"per-row average")
+              f"per-unit average")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -397,8 +425,8 @@ def run_ours(args):
                 "roofline_time_ms": accounting.roofline_time_s(F, B, peaks["bf16_tflops"] * 1e12,
                                                                peaks["hbm_gbs"] * 1e9) * 1e3}
     if wl.launches_per_step > 1:
-        roofline["note"] = ("kernel_ms spans the step's attention and merge launches "
-                            "(timed together; the attention kernel dominates)")
+        roofline["note"] = (f"kernel_ms spans the step's {wl.launches_per_step} launches, timed "
+                            f"together (the attention kernels dominate)")
 
     line = None
     if rank == 0:

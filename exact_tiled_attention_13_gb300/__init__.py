@@ -12,13 +12,15 @@ from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_ERR_CUDA, ATTN_ERR_DEVIC
                    ATTN_ERR_LAUNCH, ATTN_ERR_NO_DEVICE, ATTN_ERR_UNSUPPORTED,
                    ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_FAULT_NONE, ATTN_FAULT_SKIP_FIRST_K,
                    ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK, ATTN_OUT_BF16, ATTN_OUT_F32,
-                   AttnError, attn_device_status, attn_fwd_ex_raw, attn_fwd_raw,
+                   AttnError, attn_bwd_raw, attn_bwd_workspace_bytes, attn_device_status,
+                   attn_fwd_ex_raw, attn_fwd_raw,
                    attn_fwd_splitkv_plan, attn_fwd_splitkv_raw, attn_set_fault_injection,
                    attn_set_wait_timeout_ns, attn_version, library_path, load, strerror)
 
 __all__ = [
     "attn_fwd", "attn_fwd_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "attn_fwd_splitkv",
-    "attn_fwd_splitkv_raw", "attn_fwd_splitkv_plan", "splitkv_workspace", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
+    "attn_fwd_splitkv_raw", "attn_fwd_splitkv_plan", "splitkv_workspace", "attn_bwd",
+    "attn_bwd_raw", "attn_bwd_workspace_bytes", "bwd_workspace", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
     "attn_set_fault_injection", "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
     "ATTN_BIAS_DENSE", "ATTN_BIAS_KEY", "ATTN_OUT_BF16", "ATTN_OUT_F32",
 ]
@@ -154,3 +156,38 @@ def attn_fwd_splitkv(Q, K, V, mode, C, ckey, scale, O, LSE=None, workspace=None,
     if code != ATTN_OK:
         raise AttnError(code, "attn_fwd_splitkv")
     return O, LSE
+
+
+def bwd_workspace(BH, Nq, device="cuda"):
+    """A workspace tensor (uint8) of the size attn_bwd needs."""
+    import torch
+
+    code, nbytes = attn_bwd_workspace_bytes(BH, Nq)
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_bwd_workspace_bytes")
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device=device)
+
+
+def attn_bwd(Q, K, V, O, dO, LSE, mode, C, ckey, scale, dQ, dK, dV, workspace, stream=None):
+    """Gradients dQ, dK, dV (fp32, written in place) of the forward pass that produced O and
+    LSE from Q, K, V, mode, C, ckey and scale, for the loss gradient dO (bf16, shaped like
+    O), through the C ABI (include/attn.h, attn_bwd). `workspace`: see bwd_workspace."""
+    import torch
+
+    BH, Nq, Nk, d, dv, o_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE)
+    if LSE is None:
+        raise ValueError("the backward pass needs the forward LSE")
+    if dO.dtype != torch.bfloat16 or tuple(dO.shape) != (BH, Nq, dv) or not dO.is_contiguous():
+        raise ValueError("dO must be a contiguous bf16 [BH, Nq, d_v] tensor")
+    for name, t, shape in (("dQ", dQ, (BH, Nq, d)), ("dK", dK, (BH, Nk, d)), ("dV", dV, (BH, Nk, dv))):
+        if t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 {list(shape)} tensor")
+    if not workspace.is_contiguous():
+        raise ValueError("workspace must be contiguous")
+    code = attn_bwd_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), o_dtype,
+                        dO.data_ptr(), lse_ptr, mode, c_ptr, k_ptr, BH, Nq, Nk, d, dv, scale,
+                        dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(), workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_bwd")
+    return dQ, dK, dV

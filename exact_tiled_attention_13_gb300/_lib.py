@@ -49,6 +49,12 @@ SIGNATURES = {
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_float, ctypes.c_int, _P,
                                                ctypes.c_int, _P, _P]),
+    "attn_bwd": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P,
+                                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, ctypes.c_ulonglong,
+                                _P]),
+    "attn_bwd_workspace_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int,
+                                                ctypes.POINTER(ctypes.c_ulonglong)]),
     "attn_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_device_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_timeout_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
@@ -132,6 +138,21 @@ def attn_fwd_splitkv_plan(mode, BH, Nq, Nk, d, d_v, n_splits=0):
     code = load().attn_fwd_splitkv_plan(int(mode), int(BH), int(Nq), int(Nk), int(d), int(d_v),
                                         int(n_splits), ctypes.byref(splits), ctypes.byref(nbytes))
     return code, splits.value, nbytes.value
+
+
+def attn_bwd_raw(Q, K, V, O, o_dtype, dO, LSE, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, dQ, dK,
+                 dV, workspace, workspace_bytes, stream) -> int:
+    """attn_bwd with plain integers as pointers; returns its code unchanged."""
+    return load().attn_bwd(Q, K, V, O, int(o_dtype), dO, LSE, int(mode), C, ckey, int(BH), int(Nq),
+                           int(Nk), int(d), int(d_v), float(scale), dQ, dK, dV, workspace,
+                           int(workspace_bytes), stream)
+
+
+def attn_bwd_workspace_bytes(BH, Nq):
+    """(code, bytes) of the workspace attn_bwd needs."""
+    nbytes = ctypes.c_ulonglong(0)
+    code = load().attn_bwd_workspace_bytes(int(BH), int(Nq), ctypes.byref(nbytes))
+    return code, nbytes.value
 
 
 def attn_device_status(stream=None):

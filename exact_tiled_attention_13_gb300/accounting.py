@@ -53,6 +53,27 @@ def required_bytes(BH: int, N: int, d: int, dv: int, out_bytes: int, lse: bool =
     return b
 
 
+def bwd_flops(BH: int, N: int, d: int, dv: int, causal: bool, Nk: int | None = None) -> float:
+    """Algorithmic FLOPs of one backward pass: the five products S = Q K^T (d), dP = dO V^T
+    (dv), dV = P^T dO (dv), dK = dS^T Q (d) and dQ = dS K (d), 2 (3 d + 2 dv) per allowed
+    pair. Recomputing S and dP a second time (the dQ kernel) is not counted."""
+    return 2.0 * BH * allowed_pairs(N, causal, Nk) * (3 * d + 2 * dv)
+
+
+def bwd_required_bytes(BH: int, N: int, d: int, dv: int, o_bytes: int, dense_bias: bool = False,
+                       key_bias: bool = False, Nk: int | None = None) -> int:
+    """Bytes of reading Q, K, V, dO (bf16), O (its dtype), LSE and the bias once and writing
+    dQ, dK, dV (fp32) once."""
+    Nk = N if Nk is None else Nk
+    b = BH * N * d * BF16 + BH * Nk * (d + dv) * BF16 + BH * N * dv * (BF16 + o_bytes) + BH * N * F32
+    b += BH * N * d * F32 + BH * Nk * (d + dv) * F32
+    if dense_bias:
+        b += BH * N * Nk * F32
+    if key_bias:
+        b += BH * Nk * F32
+    return b
+
+
 def materialized_intermediate_bytes(N: int, elem_bytes: int = F32) -> dict:
     """Sizes of S and P for one head and the traffic of writing and re-reading both."""
     s = N * N * elem_bytes

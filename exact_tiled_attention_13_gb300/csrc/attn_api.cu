@@ -13,6 +13,7 @@
 #include "attn.h"
 #include "attn_fwd_kernel.cuh"
 #include "attn_merge_kernel.cuh"
+#include "attn_bwd_kernel.cuh"
 
 namespace eta {
 
@@ -29,6 +30,17 @@ ETA_DECLARE(128, 64)
 ETA_DECLARE(128, 128)
 #undef ETA_DECLARE
 #undef ETA_DECLARE_C
+#define ETA_DECLARE_BWD_C(D, DV, C)                                                       \
+  extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_NONE>(const BwdLaunchArgs &);  \
+  extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_DENSE>(const BwdLaunchArgs &); \
+  extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_KEY>(const BwdLaunchArgs &);
+#define ETA_DECLARE_BWD(D, DV) ETA_DECLARE_BWD_C(D, DV, false) ETA_DECLARE_BWD_C(D, DV, true)
+ETA_DECLARE_BWD(64, 64)
+ETA_DECLARE_BWD(64, 128)
+ETA_DECLARE_BWD(128, 64)
+ETA_DECLARE_BWD(128, 128)
+#undef ETA_DECLARE_BWD
+#undef ETA_DECLARE_BWD_C
 
 namespace {
 
@@ -148,6 +160,19 @@ cudaError_t dispatch_bias(int bias, const LaunchArgs &a) {
 template <int D, int DV>
 cudaError_t dispatch(bool causal, int bias, const LaunchArgs &a) {
   return causal ? dispatch_bias<D, DV, true>(bias, a) : dispatch_bias<D, DV, false>(bias, a);
+}
+
+template <int D, int DV, bool C>
+cudaError_t dispatch_bwd_bias(int bias, const BwdLaunchArgs &a) {
+  switch (bias) {
+    case BWD_BIAS_DENSE: return launch_bwd<D, DV, C, BWD_BIAS_DENSE>(a);
+    case BWD_BIAS_KEY: return launch_bwd<D, DV, C, BWD_BIAS_KEY>(a);
+    default: return launch_bwd<D, DV, C, BWD_BIAS_NONE>(a);
+  }
+}
+template <int D, int DV>
+cudaError_t dispatch_bwd(bool causal, int bias, const BwdLaunchArgs &a) {
+  return causal ? dispatch_bwd_bias<D, DV, true>(bias, a) : dispatch_bwd_bias<D, DV, false>(bias, a);
 }
 
 }  // namespace
@@ -485,6 +510,133 @@ extern "C" int attn_device_status(void *stream, unsigned int *detail) {
       return ATTN_ERR_CUDA;
     }
     return ATTN_ERR_DEVICE_TIMEOUT;
+  }
+  return ATTN_OK;
+}
+
+// ------------------------------------------------------------------ backward pass
+namespace eta {
+namespace {
+unsigned long long bwd_workspace_bytes(int BH, int Nq) {
+  const unsigned long long nqp = static_cast<unsigned long long>((Nq + BM - 1) / BM) * BM;
+  return 2ull * static_cast<unsigned long long>(BH) * nqp * 4ull;
+}
+}  // namespace
+}  // namespace eta
+
+extern "C" int attn_bwd_workspace_bytes(int BH, int Nq, unsigned long long *bytes) {
+  if (bytes) *bytes = 0;
+  if (!bytes || BH < 1 || Nq < 0) return ATTN_ERR_INVALID_ARG;
+  *bytes = bwd_workspace_bytes(BH, Nq);
+  return ATTN_OK;
+}
+
+extern "C" int attn_bwd(const void *Q, const void *K, const void *V, const void *O, int o_dtype,
+                        const void *dO, const float *LSE, int mode, const float *C,
+                        const float *ckey, int BH, int Nq, int Nk, int d, int d_v, float scale,
+                        float *dQ, float *dK, float *dV, void *workspace,
+                        unsigned long long workspace_bytes, void *stream) {
+  // ---- arguments (no CUDA call before these pass)
+  int rc = check_shape(mode, BH, Nq, Nk, d, d_v, o_dtype, scale);
+  if (rc < 0) return rc;
+  if (Nk == 0) return Nq == 0 ? ATTN_OK : ATTN_ERR_INVALID_ARG;
+  const bool no_queries = Nq == 0;
+  const size_t qrows = static_cast<size_t>(BH) * static_cast<size_t>(Nq);
+  const size_t krows = static_cast<size_t>(BH) * static_cast<size_t>(Nk);
+  const unsigned long long need = bwd_workspace_bytes(BH, Nq);
+  if (!K || !V || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+  if (!no_queries && (!Q || !O || !dO || !LSE || !dQ || !workspace || workspace_bytes < need))
+    return ATTN_ERR_INVALID_ARG;
+  const bool dense = (mode & ATTN_BIAS_DENSE) != 0, key = (mode & ATTN_BIAS_KEY) != 0;
+  if (dense != (C != nullptr) || key != (ckey != nullptr)) return ATTN_ERR_INVALID_ARG;
+  const void *a16[9] = {Q, K, V, O, dO, C, dQ, dK, dV};
+  for (const void *ptr : a16)
+    if (ptr && !aligned(ptr, 16)) return ATTN_ERR_INVALID_ARG;
+  if ((LSE && !aligned(LSE, 4)) || (ckey && !aligned(ckey, 4)) || (workspace && !aligned(workspace, 16)))
+    return ATTN_ERR_INVALID_ARG;
+  // Outputs (dQ, dK, dV, workspace) overlap no input and no other output.
+  const void *ins[8] = {Q, K, V, O, dO, LSE, C, ckey};
+  const size_t in_bytes[8] = {qrows * d * 2, krows * d * 2, krows * d_v * 2,
+                              qrows * d_v * (o_dtype == ATTN_OUT_F32 ? 4 : 2), qrows * d_v * 2,
+                              qrows * 4, C ? qrows * static_cast<size_t>(Nk) * 4 : 0,
+                              ckey ? krows * 4 : 0};
+  const void *outs[4] = {dQ, dK, dV, no_queries ? nullptr : workspace};
+  const size_t out_bytes[4] = {qrows * d * 4, krows * d * 4, krows * d_v * 4, need};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 8; ++i)
+      if (ranges_overlap(outs[o], out_bytes[o], ins[i], in_bytes[i])) return ATTN_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < 4; ++o2)
+      if (ranges_overlap(outs[o], out_bytes[o], outs[o2], out_bytes[o2])) return ATTN_ERR_INVALID_ARG;
+  }
+
+  // ---- device
+  int dev = -1;
+  unsigned int *watchdog = nullptr;
+  if ((rc = current_device(&dev, &watchdog)) != ATTN_OK) return rc;
+  const void *ptrs[12] = {Q, K, V, O, dO, LSE, C, ckey, dQ, dK, dV, no_queries ? nullptr : workspace};
+  for (const void *ptr : ptrs)
+    if (ptr && device_pointer_ok(ptr, dev) != ATTN_OK) return ATTN_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (no_queries) {  // no query sees any key: the key and value gradients are zero
+    if (cudaMemsetAsync(dK, 0, krows * d * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(dV, 0, krows * d_v * 4, st) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    return ATTN_OK;
+  }
+  if ((rc = get_encoder()) != ATTN_OK) return rc;
+
+  BwdLaunchArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const uint64_t nq = static_cast<uint64_t>(Nq), nk = static_cast<uint64_t>(Nk),
+                 bh = static_cast<uint64_t>(BH);
+  if (encode_3d(&a.tmQ, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, Q, d, nq, bh, SW_CHUNK, BM) != ATTN_OK ||
+      encode_3d(&a.tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, d, nk, bh, SW_CHUNK, BN) != ATTN_OK ||
+      encode_3d(&a.tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, V, d_v, nk, bh, SW_CHUNK, BN) != ATTN_OK ||
+      encode_3d(&a.tmdO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dO, d_v, nq, bh, SW_CHUNK, BM) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  const int nq_tiles = (Nq + BM - 1) / BM;
+  BwdParams &pp = a.p;
+  pp.BH = BH;
+  pp.Nq = Nq;
+  pp.Nk = Nk;
+  pp.nq_tiles = nq_tiles;
+  pp.nkv_tiles = (Nk + BN - 1) / BN;
+  pp.causal_off = Nk - Nq;
+  pp.nqp = nq_tiles * BM;
+  pp.scale_log2 = scale * LOG2E;
+  pp.scale = scale;
+  float *Lp = static_cast<float *>(workspace);
+  float *Dd = Lp + static_cast<size_t>(BH) * pp.nqp;
+  pp.Lp = Lp;
+  pp.Dd = Dd;
+  pp.C = C;
+  pp.ckey = ckey;
+  pp.dQ = dQ;
+  pp.dK = dK;
+  pp.dV = dV;
+  pp.status = watchdog;
+  pp.timeout_ns = g_timeout_ns.load();
+  a.stream = st;
+  if (static_cast<uint64_t>(BH) * (pp.nkv_tiles > nq_tiles ? pp.nkv_tiles : nq_tiles) > 0x7FFFFFFFull)
+    return ATTN_ERR_INVALID_ARG;
+
+  const int out_f32 = o_dtype == ATTN_OUT_F32 ? 1 : 0;
+  const uint16_t *dO16 = static_cast<const uint16_t *>(dO);
+  cudaError_t e = d_v == 64 ? launch_bwd_prep<64>(O, out_f32, dO16, LSE, BH, Nq, pp.nqp, Lp, Dd, st)
+                            : launch_bwd_prep<128>(O, out_f32, dO16, LSE, BH, Nq, pp.nqp, Lp, Dd, st);
+  if (e == cudaSuccess) {
+    const bool causal = (mode & ATTN_MASK_CAUSAL) != 0;
+    const int bias = dense ? BWD_BIAS_DENSE : (key ? BWD_BIAS_KEY : BWD_BIAS_NONE);
+    if (d == 64 && d_v == 64) e = dispatch_bwd<64, 64>(causal, bias, a);
+    else if (d == 64) e = dispatch_bwd<64, 128>(causal, bias, a);
+    else if (d_v == 64) e = dispatch_bwd<128, 64>(causal, bias, a);
+    else e = dispatch_bwd<128, 128>(causal, bias, a);
+  }
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_LAUNCH;
   }
   return ATTN_OK;
 }

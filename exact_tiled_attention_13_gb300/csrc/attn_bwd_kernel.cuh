@@ -1,0 +1,655 @@
+// Exact attention backward pass, tile by tile, for sm_103a.
+//
+// The gradients are those of O = softmax(S) V with S = scale Q K^T + C, for a loss
+// gradient dO:
+//     dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij = dO_i . O_i,
+//     dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+// The score and probability tiles are recomputed from Q, K and the forward's kept
+// statistic LSE_i (P_ij = exp(S_ij - LSE_i)) instead of being stored, as the pages
+// say of the tiled method's backward pass ("Compilers and kernels", section
+// "FlashAttention rewrites the algorithm around IO", the paragraph after the
+// recurrence).
+//
+// Three kernels, no atomics (the result is deterministic):
+//   prep : one warp per query row: Lp_i = LSE_i log2(e) (+inf for a row with no allowed
+//          key and for the padding rows up to a whole tile, so that their p is 0) and
+//          D_i = dO_i . O_i, into a caller workspace [BH][nq_tiles * 128] each.
+//   dkdv : one CTA per (head, 128-key tile j). Keeps K_j and V_j in shared memory and
+//          streams the query tiles i that see tile j (Q_i, dO_i and their Lp, D) through a
+//          ring of slots. Per query tile, on the tensor cores with accumulators in tensor
+//          memory: S^T = K_j Q_i^T and dP^T = V_j dO_i^T; the elementwise warps (thread =
+//          key row = tensor-memory lane) form P^T = exp2(S^T scale log2e - Lp) and
+//          dS^T = P^T o (dP^T - D) in bf16 over S^T and dP^T; then dV_j += P^T dO_i and
+//          dK_j += dS^T Q_i. At the end dV_j and scale dK_j are written in fp32.
+//   dq   : one CTA per (head, 128-query tile i). Keeps Q_i and dO_i, streams the K/V tiles
+//          the tile sees: S = Q_i K_j^T, dP = dO_i V_j^T, dS = P o (dP - D) in bf16 over
+//          dP, dQ_i += dS K_j; at the end scale dQ_i in fp32.
+// Warp roles of dkdv and dq (12 warps): two elementwise warpgroups (each thread owns one
+// tensor-memory lane and half of the 128 columns), the MMA warp (whole warp, one elected
+// lane issues) and one TMA producer warp. Every wait is bounded (the forward kernel's
+// watchdog): a wait that runs out is recorded and the CTA drains and returns.
+#pragma once
+
+#include "attn_fwd_kernel.cuh"
+
+namespace eta {
+
+struct BwdParams {
+  int BH;
+  int Nq, Nk;
+  int nq_tiles, nkv_tiles;
+  int causal_off;     // Nk - Nq: query i may see keys j <= i + causal_off
+  int nqp;            // nq_tiles * 128: row stride of Lp and D
+  float scale_log2;   // scale * log2(e)
+  float scale;
+  const float *Lp;    // [BH][nqp] LSE * log2(e), +inf where p must be 0
+  const float *Dd;    // [BH][nqp] D_i = dO_i . O_i
+  const float *C;     // dense bias [BH][Nq][Nk] or null
+  const float *ckey;  // per-key bias [BH][Nk] or null
+  float *dQ;          // [BH][Nq][d]
+  float *dK;          // [BH][Nk][d]
+  float *dV;          // [BH][Nk][d_v]
+  unsigned int *status;
+  unsigned long long timeout_ns;
+};
+
+using BwdWatchdog = WatchdogT<BwdParams>;
+
+// ------------------------------------------------------------------------ prep
+// O: [rows][DV] bf16 (out_f32 = 0) or fp32; dO: [rows][DV] bf16; LSE: [rows].
+template <int DV>
+__global__ void __launch_bounds__(256)
+    attn_bwd_prep_kernel(const void *__restrict__ O, int out_f32, const uint16_t *__restrict__ dO,
+                         const float *__restrict__ LSE, int BH, int Nq, int nqp, float *Lp,
+                         float *Dd) {
+  constexpr int W = DV / 32;
+  const long long prow = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
+  if (prow >= static_cast<long long>(BH) * nqp) return;
+  const int lane = threadIdx.x % 32;
+  const int bh = static_cast<int>(prow / nqp);
+  const int i = static_cast<int>(prow % nqp);
+  float acc = 0.0f;
+  float lp = INFINITY;
+  if (i < Nq) {
+    const long long row = static_cast<long long>(bh) * Nq + i;
+    const uint16_t *g = dO + row * DV + lane * W;
+    float o[W], gv[W];
+#pragma unroll
+    for (int c = 0; c < W; ++c) gv[c] = __uint_as_float(static_cast<uint32_t>(g[c]) << 16);
+    if (out_f32) {
+      const float *src = static_cast<const float *>(O) + row * DV + lane * W;
+#pragma unroll
+      for (int c = 0; c < W; ++c) o[c] = src[c];
+    } else {
+      const uint16_t *src = static_cast<const uint16_t *>(O) + row * DV + lane * W;
+#pragma unroll
+      for (int c = 0; c < W; ++c) o[c] = __uint_as_float(static_cast<uint32_t>(src[c]) << 16);
+    }
+#pragma unroll
+    for (int c = 0; c < W; ++c) acc = fmaf(gv[c], o[c], acc);
+    const float lse = LSE[row];
+    lp = lse == -INFINITY ? INFINITY : lse * LOG2E;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (lane == 0) {
+    Lp[prow] = lp;
+    Dd[prow] = i < Nq ? acc : 0.0f;
+  }
+}
+
+// ------------------------------------------------------------------------ shared pieces
+// Bias sources of the backward kernels.
+enum { BWD_BIAS_NONE = 0, BWD_BIAS_DENSE = 1, BWD_BIAS_KEY = 2 };
+
+template <int D, int DV, bool CAUSAL, int BIAS>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "d must be 64 or 128");
+  static_assert(DV == 64 || DV == 128, "d_v must be 64 or 128");
+  static constexpr int Q_TILE = BM * D * 2;   // also a K tile (128 rows x d)
+  static constexpr int DO_TILE = BM * DV * 2; // also a V tile (128 rows x d_v)
+  static constexpr int LD_BYTES = 2 * BM * 4; // Lp and D of one query tile
+  static constexpr int BUDGET = 224 * 1024;
+  // dkdv: K_j, V_j resident; ring of (Q_i, dO_i, Lp_i, D_i) slots.
+  static constexpr int A_SLOT = Q_TILE + DO_TILE + LD_BYTES;
+  static constexpr int A_QS = cmin(3, (BUDGET - Q_TILE - DO_TILE) / A_SLOT);
+  static constexpr int A_K_OFF = 0;
+  static constexpr int A_V_OFF = Q_TILE;
+  static constexpr int A_SLOT_OFF = Q_TILE + DO_TILE;
+  static constexpr int A_BAR_OFF = A_SLOT_OFF + A_QS * A_SLOT;
+  // dq: Q_i, dO_i resident; ring of (K_j, V_j) slots.
+  static constexpr int B_SLOT = Q_TILE + DO_TILE;
+  static constexpr int B_KS = cmin(3, (BUDGET - Q_TILE - DO_TILE) / B_SLOT);
+  static constexpr int B_Q_OFF = 0;
+  static constexpr int B_DO_OFF = Q_TILE;
+  static constexpr int B_SLOT_OFF = Q_TILE + DO_TILE;
+  static constexpr int B_BAR_OFF = B_SLOT_OFF + B_KS * B_SLOT;
+  static_assert(A_QS >= 2 && B_KS >= 2, "need two ring slots");
+  static_assert(A_SLOT % 1024 == 0 && B_SLOT % 1024 == 0, "slots keep 1024-byte alignment");
+
+  // barriers (the same layout serves both kernels; RING = ring slots)
+  static constexpr int RING = A_QS > B_KS ? A_QS : B_KS;
+  static constexpr int BAR_FIXED = 0;               // K_j/V_j (dkdv) or Q_i/dO_i (dq)
+  static constexpr int BAR_FULL = 1;                // ring slot filled
+  static constexpr int BAR_EMPTY = BAR_FULL + RING; // ring slot released
+  static constexpr int BAR_SFULL = BAR_EMPTY + RING;
+  static constexpr int BAR_PFULL = BAR_SFULL + 1;   // 8 elementwise warps arrive
+  static constexpr int BAR_ACC = BAR_PFULL + 1;
+  static constexpr int BAR_DRAIN = BAR_ACC + 1;
+  static constexpr int NUM_BARS = BAR_DRAIN + 1;
+  static constexpr int BAR_BYTES = NUM_BARS * 8;
+  static constexpr int TAIL_BYTES = BAR_BYTES + 8;  // + tensor-memory address + abort flag
+  static constexpr int A_SMEM = A_BAR_OFF + TAIL_BYTES + 1024;
+  static constexpr int B_SMEM = B_BAR_OFF + TAIL_BYTES + 1024;
+  static_assert(A_SMEM <= 232448 && B_SMEM <= 232448, "shared memory over the per-CTA limit");
+  // At least 120 KB each, so one CTA holds an SM (the CTA allocates all tensor memory).
+  static constexpr int A_SMEM_TOTAL = A_SMEM > 120 * 1024 ? A_SMEM : 120 * 1024;
+  static constexpr int B_SMEM_TOTAL = B_SMEM > 120 * 1024 ? B_SMEM : 120 * 1024;
+
+  // tensor memory
+  static constexpr int S_COL = 0;     // S^T (dkdv) or S (dq); P^T packed over it
+  static constexpr int DP_COL = 128;  // dP^T or dP; dS^T / dS packed over it
+  static constexpr int ACC0_COL = 256;        // dV (dkdv) or dQ (dq)
+  static constexpr int ACC1_COL = 256 + DV;   // dK (dkdv)
+  static constexpr int TMEM_COLS = 512;
+
+  static constexpr int NUM_WARPS = 12;
+  static constexpr int THREADS = 32 * NUM_WARPS;
+  static constexpr int MMA_WARP = 8;
+  static constexpr int LOAD_WARP = 9;
+
+  static constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, false);
+  static constexpr uint32_t IDESC_NV = idesc_bf16_f32(128, DV, true);  // dV += P^T dO
+  static constexpr uint32_t IDESC_ND = idesc_bf16_f32(128, D, true);   // dK, dQ
+};
+
+// K-major operand step ks (16 elements of the contraction) inside 128-row boxes of 64
+// columns: 32 bytes within a 128-byte row, a new box every 4 steps.
+__device__ __forceinline__ uint32_t kmajor_step(int ks) {
+  return static_cast<uint32_t>(((ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32) >> 4);
+}
+// Packed bf16 A operand in tensor memory for step ks (16 columns of the contraction):
+// elementwise warpgroup g owns contraction columns [64g, 64g + 64) and stores them,
+// two per 32-bit column, at [64g, 64g + 32).
+__device__ __forceinline__ uint32_t packed_col(int ks) {
+  return static_cast<uint32_t>(64 * (ks / 4) + 8 * (ks % 4));
+}
+
+// Loads a 32-column chunk of two tensor-memory matrices.
+__device__ __forceinline__ void ld_pair(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
+                                        uint32_t (&b)[32]) {
+  tmem_ld32(ta, a);
+  tmem_ld32(tb, b);
+  tmem_wait_ld(a);
+  tmem_wait_ld(b);
+}
+
+// Writes a 128 x W fp32 accumulator row (this thread's lane) from tensor memory to
+// global memory, columns [c0, c0 + n) in 32-column chunks, times `mul`.
+__device__ __forceinline__ void store_acc_row(uint32_t tcol, int c0, int n, float mul, float *dst,
+                                              bool row_ok) {
+  for (int cc = c0; cc < c0 + n; cc += 32) {
+    uint32_t r[32];
+    tmem_ld32(tcol + cc, r);
+    tmem_wait_ld(r);
+    if (row_ok) {
+      float4 *d4 = reinterpret_cast<float4 *>(dst + cc);
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        d4[v] = make_float4(__uint_as_float(r[4 * v]) * mul, __uint_as_float(r[4 * v + 1]) * mul,
+                            __uint_as_float(r[4 * v + 2]) * mul, __uint_as_float(r[4 * v + 3]) * mul);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_zero_row(int n, float *dst, bool row_ok) {
+  if (!row_ok) return;
+  float4 *d4 = reinterpret_cast<float4 *>(dst);
+  for (int v = 0; v < n / 4; ++v) d4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// ------------------------------------------------------------------------ dK, dV
+template <int D, int DV, bool CAUSAL, int BIAS>
+__global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
+    attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                         const __grid_constant__ BwdParams p) {
+  using CF = BwdCfg<D, DV, CAUSAL, BIAS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + CF::A_BAR_OFF;
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + CF::A_BAR_OFF + CF::BAR_BYTES);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::A_BAR_OFF + CF::BAR_BYTES + 4);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // This CTA: head bh, key tile j; the query tiles that see it are i_lo .. nq_tiles - 1.
+  const int bh = blockIdx.x / p.nkv_tiles;
+  const int j = static_cast<int>(blockIdx.x % p.nkv_tiles);
+  int i_lo = 0;
+  if (CAUSAL) {
+    // The first query that sees key 128 j is q0 = 128 j - (Nk - Nq); none when q0 >= Nq.
+    const int q0 = j * BN - p.causal_off;
+    i_lo = q0 >= p.Nq ? p.nq_tiles : (q0 <= 0 ? 0 : q0 / BM);
+  }
+  const int n_it = p.nq_tiles - i_lo;
+  BwdWatchdog wd{sbase + CF::A_BAR_OFF + CF::BAR_BYTES + 4, p};
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(CF::BAR_FIXED), 1);
+    for (int s = 0; s < CF::A_QS; ++s) {
+      mbar_init(BAR(CF::BAR_FULL + s), 1);
+      mbar_init(BAR(CF::BAR_EMPTY + s), 1);
+    }
+    mbar_init(BAR(CF::BAR_SFULL), 1);
+    mbar_init(BAR(CF::BAR_PFULL), 8);
+    mbar_init(BAR(CF::BAR_ACC), 1);
+    mbar_init(BAR(CF::BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == CF::MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_ptr), CF::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp < 8) {
+    // ============================================================ elementwise
+    const int g = warp / 4;  // columns (queries) [64 g, 64 g + 64)
+    const int r = threadIdx.x % 128;
+    const int key = j * BN + r;
+    const bool key_ok = key < p.Nk;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
+    const uint32_t t_s = tmem + lane_off + CF::S_COL;
+    const uint32_t t_dp = tmem + lane_off + CF::DP_COL;
+    float kb = 0.0f;  // per-key bias of this row, log2-scaled
+    if (BIAS == BWD_BIAS_KEY) kb = key_ok ? p.ckey[static_cast<size_t>(bh) * p.Nk + key] * LOG2E : 0.0f;
+    const bool row_dead = !key_ok || (BIAS == BWD_BIAS_KEY && kb == -INFINITY);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int i = i_lo + it;
+      const int slot = it % CF::A_QS;
+      ok = wd.wait(BAR(CF::BAR_SFULL), it & 1, ROLE_SOFTMAX, CF::BAR_SFULL);
+      if (!ok) break;
+      tc_fence_after();
+      const float *Ls = reinterpret_cast<const float *>(smem + CF::A_SLOT_OFF + slot * CF::A_SLOT +
+                                                        CF::Q_TILE + CF::DO_TILE);
+      const float *Ds = Ls + BM;
+      // Keys past the causal limit of the tile's first query need the elementwise test.
+      const bool diag = CAUSAL && (j * BN + BN - 1 > i * BM + p.causal_off);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c0 = 64 * g + 32 * h;
+        uint32_t sr[32], dr[32];
+        ld_pair(t_s + c0, t_dp + c0, sr, dr);
+        uint32_t pp[16], dd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 L4 = *reinterpret_cast<const float4 *>(Ls + c0 + c);
+          const float4 D4 = *reinterpret_cast<const float4 *>(Ds + c0 + c);
+          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
+          const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+          float pv[4], dv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int q = i * BM + c0 + c + u;
+            float x = fmaf(__uint_as_float(sr[c + u]), p.scale_log2, kb) - Lv[u];
+            if (BIAS == BWD_BIAS_DENSE)
+              x += (key_ok && q < p.Nq) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
+                                        : 0.0f;
+            if (diag && key > q + p.causal_off) x = -INFINITY;
+            if (row_dead) x = -INFINITY;
+            const float pr = ex2_approx(x);
+            pv[u] = pr;
+            dv[u] = pr * (__uint_as_float(dr[c + u]) - Dv[u]);
+          }
+          pp[c / 2] = pack_bf16(pv[0], pv[1]);
+          pp[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
+          dd[c / 2] = pack_bf16(dv[0], dv[1]);
+          dd[c / 2 + 1] = pack_bf16(dv[2], dv[3]);
+        }
+        tmem_st16(t_s + 64 * g + 16 * h, pp);
+        tmem_st16(t_dp + 64 * g + 16 * h, dd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      mbar_arrive_elect(BAR(CF::BAR_PFULL));
+    }
+    // ---------------------------------------------------------- epilogue: dV, scale dK
+    float *dv_row = p.dV + (static_cast<size_t>(bh) * p.Nk + (key_ok ? key : 0)) * DV;
+    float *dk_row = p.dK + (static_cast<size_t>(bh) * p.Nk + (key_ok ? key : 0)) * D;
+    if (ok && n_it > 0) {
+      ok = wd.wait(BAR(CF::BAR_ACC), 0, ROLE_SOFTMAX, CF::BAR_ACC);
+      if (ok) {
+        tc_fence_after();
+        store_acc_row(tmem + lane_off + CF::ACC0_COL, g * DV / 2, DV / 2, 1.0f, dv_row, key_ok);
+        store_acc_row(tmem + lane_off + CF::ACC1_COL, g * D / 2, D / 2, p.scale, dk_row, key_ok);
+      }
+    } else if (ok) {
+      store_zero_row(DV / 2, dv_row + g * DV / 2, key_ok);
+      store_zero_row(D / 2, dk_row + g * D / 2, key_ok);
+    }
+  } else if (warp == CF::MMA_WARP) {
+    // ============================================================ MMA issue
+    bool ok = n_it == 0 || wd.wait(BAR(CF::BAR_FIXED), 0, ROLE_MMA, CF::BAR_FIXED);
+    const uint64_t k_desc = smem_desc(sbase + CF::A_K_OFF, 16, 1024);
+    const uint64_t v_desc = smem_desc(sbase + CF::A_V_OFF, 16, 1024);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int slot = it % CF::A_QS;
+      const uint32_t sl = sbase + CF::A_SLOT_OFF + slot * CF::A_SLOT;
+      ok = wd.wait(BAR(CF::BAR_FULL + slot), (it / CF::A_QS) & 1, ROLE_MMA, CF::BAR_FULL + slot);
+      if (!ok) break;
+      tc_fence_after();
+      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (both operands K-major).
+      const uint64_t q_desc = smem_desc(sl, 16, 1024);
+      const uint64_t do_desc = smem_desc(sl + CF::Q_TILE, 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_ss_elect(tmem + CF::S_COL, k_desc + kmajor_step(ks), q_desc + kmajor_step(ks),
+                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < DV / 16; ++ks)
+        mma_ss_elect(tmem + CF::DP_COL, v_desc + kmajor_step(ks), do_desc + kmajor_step(ks),
+                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_SFULL));
+      ok = wd.wait(BAR(CF::BAR_PFULL), it & 1, ROLE_MMA, CF::BAR_PFULL);
+      if (!ok) break;
+      tc_fence_after();
+      // dV_j += P^T dO_i, dK_j += dS^T Q_i (A from tensor memory, B MN-major: the
+      // contraction runs over the 128 query rows of the slot's tiles).
+      const uint64_t do_mn = smem_desc(sl + CF::Q_TILE, SW_CHUNK_BYTES, 1024);
+      const uint64_t q_mn = smem_desc(sl, SW_CHUNK_BYTES, 1024);
+#pragma unroll
+      for (int ks = 0; ks < BM / 16; ++ks)
+        mma_ts_elect(tmem + CF::ACC0_COL, tmem + CF::S_COL + packed_col(ks),
+                     do_mn + ((ks * 16 * 128) >> 4), CF::IDESC_NV, (it > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < BM / 16; ++ks)
+        mma_ts_elect(tmem + CF::ACC1_COL, tmem + CF::DP_COL + packed_col(ks),
+                     q_mn + ((ks * 16 * 128) >> 4), CF::IDESC_ND, (it > 0 || ks > 0) ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_EMPTY + slot));
+    }
+    if (ok && n_it > 0) mma_commit_elect(BAR(CF::BAR_ACC));
+    mma_commit_elect(BAR(CF::BAR_DRAIN));
+    wd.drain(BAR(CF::BAR_DRAIN), 0, CF::BAR_DRAIN);
+  } else if (warp == CF::LOAD_WARP && lane == 0) {
+    // ============================================================ TMA producer
+    if (n_it > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(BAR(CF::BAR_FIXED), CF::Q_TILE + CF::DO_TILE);
+      for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+        tma_load_3d(sbase + CF::A_K_OFF + kc * SW_CHUNK_BYTES, &tmK, kc * SW_CHUNK, j * BN, bh,
+                    BAR(CF::BAR_FIXED));
+      for (int kc = 0; kc < DV / SW_CHUNK; ++kc)
+        tma_load_3d(sbase + CF::A_V_OFF + kc * SW_CHUNK_BYTES, &tmV, kc * SW_CHUNK, j * BN, bh,
+                    BAR(CF::BAR_FIXED));
+    }
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int i = i_lo + it;
+      const int slot = it % CF::A_QS;
+      if (!wd.wait1(BAR(CF::BAR_EMPTY + slot), ((it / CF::A_QS) & 1) ^ 1, ROLE_LOAD,
+                    CF::BAR_EMPTY + slot, false))
+        break;
+      const uint32_t sl = sbase + CF::A_SLOT_OFF + slot * CF::A_SLOT;
+      mbar_arrive_expect_tx(BAR(CF::BAR_FULL + slot), CF::Q_TILE + CF::DO_TILE + CF::LD_BYTES);
+      for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+        tma_load_3d(sl + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK, i * BM, bh, BAR(CF::BAR_FULL + slot));
+      for (int kc = 0; kc < DV / SW_CHUNK; ++kc)
+        tma_load_3d(sl + CF::Q_TILE + kc * SW_CHUNK_BYTES, &tmdO, kc * SW_CHUNK, i * BM, bh,
+                    BAR(CF::BAR_FULL + slot));
+      const size_t lrow = static_cast<size_t>(bh) * p.nqp + static_cast<size_t>(i) * BM;
+      bulk_load(sl + CF::Q_TILE + CF::DO_TILE, p.Lp + lrow, BM * 4, BAR(CF::BAR_FULL + slot));
+      bulk_load(sl + CF::Q_TILE + CF::DO_TILE + BM * 4, p.Dd + lrow, BM * 4, BAR(CF::BAR_FULL + slot));
+      ++issued;
+    }
+    // Copies still in flight land before the CTA exits.
+    if (n_it > 0) wd.wait1(BAR(CF::BAR_FIXED), 0, ROLE_DRAIN, CF::BAR_FIXED, true);
+    for (int s = 0; s < CF::A_QS && s < issued; ++s) {
+      const int lastpos = s + ((issued - 1 - s) / CF::A_QS) * CF::A_QS;
+      wd.wait1(BAR(CF::BAR_FULL + s), (lastpos / CF::A_QS) & 1, ROLE_DRAIN, CF::BAR_FULL + s, true);
+    }
+  }
+  __syncwarp();
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == CF::MMA_WARP) tmem_dealloc(tmem, CF::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------ dQ
+template <int D, int DV, bool CAUSAL, int BIAS>
+__global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
+    attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const __grid_constant__ BwdParams p) {
+  using CF = BwdCfg<D, DV, CAUSAL, BIAS>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + CF::B_BAR_OFF;
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + CF::B_BAR_OFF + CF::BAR_BYTES);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::B_BAR_OFF + CF::BAR_BYTES + 4);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // This CTA: head bh, query tile i; it visits key tiles 0 .. hi (none when hi < 0).
+  const int bh = blockIdx.x / p.nq_tiles;
+  const int i = static_cast<int>(blockIdx.x % p.nq_tiles);
+  int hi = p.nkv_tiles - 1;
+  if (CAUSAL) hi = cmin(floor_div(cmin(i * BM + BM - 1, p.Nq - 1) + p.causal_off, BN), hi);
+  const int n_it = hi + 1 > 0 ? hi + 1 : 0;
+  BwdWatchdog wd{sbase + CF::B_BAR_OFF + CF::BAR_BYTES + 4, p};
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(CF::BAR_FIXED), 1);
+    for (int s = 0; s < CF::B_KS; ++s) {
+      mbar_init(BAR(CF::BAR_FULL + s), 1);
+      mbar_init(BAR(CF::BAR_EMPTY + s), 1);
+    }
+    mbar_init(BAR(CF::BAR_SFULL), 1);
+    mbar_init(BAR(CF::BAR_PFULL), 8);
+    mbar_init(BAR(CF::BAR_ACC), 1);
+    mbar_init(BAR(CF::BAR_DRAIN), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == CF::MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_ptr), CF::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp < 8) {
+    // ============================================================ elementwise
+    const int g = warp / 4;  // columns (keys) [64 g, 64 g + 64)
+    const int r = threadIdx.x % 128;
+    const int q = i * BM + r;
+    const bool q_ok = q < p.Nq;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
+    const uint32_t t_s = tmem + lane_off + CF::S_COL;
+    const uint32_t t_dp = tmem + lane_off + CF::DP_COL;
+    const size_t lrow = static_cast<size_t>(bh) * p.nqp + static_cast<size_t>(q);
+    const float Lr = p.Lp[lrow];  // +inf for padding rows and rows with no allowed key
+    const float Dr = p.Dd[lrow];
+    const int lim = CAUSAL ? q + p.causal_off : INT_MAX;  // last key this row may see
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int j = it;
+      ok = wd.wait(BAR(CF::BAR_SFULL), it & 1, ROLE_SOFTMAX, CF::BAR_SFULL);
+      if (!ok) break;
+      tc_fence_after();
+      const bool mask = (CAUSAL && (j * BN + BN - 1 > i * BM + p.causal_off)) ||
+                        (j == p.nkv_tiles - 1 && (p.Nk % BN) != 0);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c0 = 64 * g + 32 * h;
+        uint32_t sr[32], dr[32];
+        ld_pair(t_s + c0, t_dp + c0, sr, dr);
+        uint32_t dd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float dv2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int key = j * BN + c0 + c + u;
+            float x = fmaf(__uint_as_float(sr[c + u]), p.scale_log2, -Lr);
+            if (BIAS == BWD_BIAS_KEY)
+              x += key < p.Nk ? __ldg(p.ckey + static_cast<size_t>(bh) * p.Nk + key) * LOG2E : 0.0f;
+            if (BIAS == BWD_BIAS_DENSE)
+              x += (q_ok && key < p.Nk) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
+                                        : 0.0f;
+            if (mask && (key > lim || key >= p.Nk)) x = -INFINITY;
+            const float pr = ex2_approx(x);
+            dv2[u] = pr * (__uint_as_float(dr[c + u]) - Dr);
+          }
+          dd[c / 2] = pack_bf16(dv2[0], dv2[1]);
+        }
+        tmem_st16(t_dp + 64 * g + 16 * h, dd);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      mbar_arrive_elect(BAR(CF::BAR_PFULL));
+    }
+    // ---------------------------------------------------------- epilogue: scale dQ
+    float *dq_row = p.dQ + (static_cast<size_t>(bh) * p.Nq + (q_ok ? q : 0)) * D;
+    if (ok && n_it > 0) {
+      ok = wd.wait(BAR(CF::BAR_ACC), 0, ROLE_SOFTMAX, CF::BAR_ACC);
+      if (ok) {
+        tc_fence_after();
+        store_acc_row(tmem + lane_off + CF::ACC0_COL, g * D / 2, D / 2, p.scale, dq_row, q_ok);
+      }
+    } else if (ok) {
+      store_zero_row(D / 2, dq_row + g * D / 2, q_ok);
+    }
+  } else if (warp == CF::MMA_WARP) {
+    // ============================================================ MMA issue
+    bool ok = n_it == 0 || wd.wait(BAR(CF::BAR_FIXED), 0, ROLE_MMA, CF::BAR_FIXED);
+    const uint64_t q_desc = smem_desc(sbase + CF::B_Q_OFF, 16, 1024);
+    const uint64_t do_desc = smem_desc(sbase + CF::B_DO_OFF, 16, 1024);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int slot = it % CF::B_KS;
+      const uint32_t sl = sbase + CF::B_SLOT_OFF + slot * CF::B_SLOT;
+      ok = wd.wait(BAR(CF::BAR_FULL + slot), (it / CF::B_KS) & 1, ROLE_MMA, CF::BAR_FULL + slot);
+      if (!ok) break;
+      tc_fence_after();
+      // S = Q_i K_j^T and dP = dO_i V_j^T (both operands K-major).
+      const uint64_t k_desc = smem_desc(sl, 16, 1024);
+      const uint64_t v_desc = smem_desc(sl + CF::Q_TILE, 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_ss_elect(tmem + CF::S_COL, q_desc + kmajor_step(ks), k_desc + kmajor_step(ks),
+                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
+#pragma unroll
+      for (int ks = 0; ks < DV / 16; ++ks)
+        mma_ss_elect(tmem + CF::DP_COL, do_desc + kmajor_step(ks), v_desc + kmajor_step(ks),
+                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_SFULL));
+      ok = wd.wait(BAR(CF::BAR_PFULL), it & 1, ROLE_MMA, CF::BAR_PFULL);
+      if (!ok) break;
+      tc_fence_after();
+      // dQ_i += dS K_j (A = dS from tensor memory, B = K_j MN-major over the 128 keys).
+      const uint64_t k_mn = smem_desc(sl, SW_CHUNK_BYTES, 1024);
+#pragma unroll
+      for (int ks = 0; ks < BN / 16; ++ks)
+        mma_ts_elect(tmem + CF::ACC0_COL, tmem + CF::DP_COL + packed_col(ks),
+                     k_mn + ((ks * 16 * 128) >> 4), CF::IDESC_ND, (it > 0 || ks > 0) ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_EMPTY + slot));
+    }
+    if (ok && n_it > 0) mma_commit_elect(BAR(CF::BAR_ACC));
+    mma_commit_elect(BAR(CF::BAR_DRAIN));
+    wd.drain(BAR(CF::BAR_DRAIN), 0, CF::BAR_DRAIN);
+  } else if (warp == CF::LOAD_WARP && lane == 0) {
+    // ============================================================ TMA producer
+    if (n_it > 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(BAR(CF::BAR_FIXED), CF::Q_TILE + CF::DO_TILE);
+      for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+        tma_load_3d(sbase + CF::B_Q_OFF + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK, i * BM, bh,
+                    BAR(CF::BAR_FIXED));
+      for (int kc = 0; kc < DV / SW_CHUNK; ++kc)
+        tma_load_3d(sbase + CF::B_DO_OFF + kc * SW_CHUNK_BYTES, &tmdO, kc * SW_CHUNK, i * BM, bh,
+                    BAR(CF::BAR_FIXED));
+    }
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int j = it;
+      const int slot = it % CF::B_KS;
+      if (!wd.wait1(BAR(CF::BAR_EMPTY + slot), ((it / CF::B_KS) & 1) ^ 1, ROLE_LOAD,
+                    CF::BAR_EMPTY + slot, false))
+        break;
+      const uint32_t sl = sbase + CF::B_SLOT_OFF + slot * CF::B_SLOT;
+      mbar_arrive_expect_tx(BAR(CF::BAR_FULL + slot), CF::Q_TILE + CF::DO_TILE);
+      for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+        tma_load_3d(sl + kc * SW_CHUNK_BYTES, &tmK, kc * SW_CHUNK, j * BN, bh, BAR(CF::BAR_FULL + slot));
+      for (int kc = 0; kc < DV / SW_CHUNK; ++kc)
+        tma_load_3d(sl + CF::Q_TILE + kc * SW_CHUNK_BYTES, &tmV, kc * SW_CHUNK, j * BN, bh,
+                    BAR(CF::BAR_FULL + slot));
+      ++issued;
+    }
+    if (n_it > 0) wd.wait1(BAR(CF::BAR_FIXED), 0, ROLE_DRAIN, CF::BAR_FIXED, true);
+    for (int s = 0; s < CF::B_KS && s < issued; ++s) {
+      const int lastpos = s + ((issued - 1 - s) / CF::B_KS) * CF::B_KS;
+      wd.wait1(BAR(CF::BAR_FULL + s), (lastpos / CF::B_KS) & 1, ROLE_DRAIN, CF::BAR_FULL + s, true);
+    }
+  }
+  __syncwarp();
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == CF::MMA_WARP) tmem_dealloc(tmem, CF::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------------ host side
+struct BwdLaunchArgs {
+  CUtensorMap tmQ, tmK, tmV, tmdO;
+  BwdParams p;
+  cudaStream_t stream;
+};
+
+template <int D, int DV, bool CAUSAL, int BIAS>
+cudaError_t launch_bwd(const BwdLaunchArgs &a) {
+  using CF = BwdCfg<D, DV, CAUSAL, BIAS>;
+  auto ka = attn_bwd_dkdv_kernel<D, DV, CAUSAL, BIAS>;
+  auto kb = attn_bwd_dq_kernel<D, DV, CAUSAL, BIAS>;
+  cudaError_t e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::A_SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::B_SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
+  const unsigned grid_a = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.nkv_tiles);
+  const unsigned grid_b = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.nq_tiles);
+  ka<<<grid_a, CF::THREADS, CF::A_SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  kb<<<grid_b, CF::THREADS, CF::B_SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
+  return cudaGetLastError();
+}
+
+template <int DV>
+cudaError_t launch_bwd_prep(const void *O, int out_f32, const uint16_t *dO, const float *LSE,
+                            int BH, int Nq, int nqp, float *Lp, float *Dd, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(BH) * nqp;
+  const long long blocks = (rows + 7) / 8;
+  attn_bwd_prep_kernel<DV><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(O, out_f32, dO, LSE, BH,
+                                                                             Nq, nqp, Lp, Dd);
+  return cudaGetLastError();
+}
+
+}  // namespace eta

@@ -193,11 +193,12 @@ struct Cfg {
 // Watchdog codes: bit 31 set, role in bits 24-27, barrier index in bits 8-23.
 enum { ROLE_SOFTMAX = 1, ROLE_MMA = 2, ROLE_LOAD = 3, ROLE_CLOAD = 4, ROLE_DRAIN = 5 };
 
-struct Watchdog {
+template <class Params>
+struct WatchdogT {
   // The abort flag lives in shared memory; the status word and the timeout are read from
   // the kernel parameters only on the slow path, so the common case holds one register.
   uint32_t abort_addr;
-  const KernelParams &p;
+  const Params &p;
 
   __device__ bool aborted() const {
     int v;
@@ -238,6 +239,8 @@ struct Watchdog {
     return __all_sync(0xFFFFFFFFu, ok);
   }
 };
+
+using Watchdog = WatchdogT<KernelParams>;
 
 // Per-CTA schedule: which query tiles it owns and which K/V tiles each one visits.
 // Iteration `it` visits K/V tile j = hi_max - it; query tile q takes part in

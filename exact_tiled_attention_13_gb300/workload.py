@@ -61,11 +61,32 @@ class DeviceWorkload:
         self.LSE = torch.empty(w.BH, w.N, dtype=torch.float32, device=device)
         self.O_h = torch.empty(self.O.shape, dtype=odt).pin_memory()
         self.LSE_h = torch.empty(self.LSE.shape, dtype=torch.float32).pin_memory()
+        if w.backward:
+            import exact_tiled_attention_13_gb300 as eta
+
+            # The forward pass once, for O and LSE; the step is the backward pass.
+            eta.attn_fwd_ex(self.Q, self.K, self.V, w.mode, self.C, self.ckey, w.scale, self.O,
+                            self.LSE)
+            self.O_h.copy_(self.O)
+            self.LSE_h.copy_(self.LSE)
+            self.dO_h = pinned(self.host["dO"].view(np.int16), torch.bfloat16)
+            self.dO = self.dO_h.to(device)
+            self.dQ = torch.empty(w.BH, w.N, w.d, dtype=torch.float32, device=device)
+            self.dK = torch.empty(w.BH, w.Nkv, w.d, dtype=torch.float32, device=device)
+            self.dV = torch.empty(w.BH, w.Nkv, w.dv, dtype=torch.float32, device=device)
+            self.grads_h = [torch.empty(t.shape, dtype=torch.float32).pin_memory()
+                            for t in (self.dQ, self.dK, self.dV)]
+            self.workspace = eta.bwd_workspace(w.BH, w.N, device=device)
+            self.launches_per_step = 3
 
     def launch(self, stream=None):
         import exact_tiled_attention_13_gb300 as eta
 
-        if self.w.split_kv:
+        if self.w.backward:
+            eta.attn_bwd(self.Q, self.K, self.V, self.O, self.dO, self.LSE, self.w.mode, self.C,
+                         self.ckey, self.w.scale, self.dQ, self.dK, self.dV, self.workspace,
+                         stream=stream)
+        elif self.w.split_kv:
             eta.attn_fwd_splitkv(self.Q, self.K, self.V, self.w.mode, self.C, self.ckey,
                                  self.w.scale, self.O, self.LSE, workspace=self.workspace,
                                  stream=stream)
@@ -73,34 +94,38 @@ class DeviceWorkload:
             eta.attn_fwd_ex(self.Q, self.K, self.V, self.w.mode, self.C, self.ckey, self.w.scale,
                             self.O, self.LSE, stream=stream)
 
+    def _inputs(self):
+        pairs = [(self.Q, self.Q_h), (self.K, self.K_h), (self.V, self.V_h), (self.C, self.C_h),
+                 (self.ckey, self.ck_h)]
+        if self.w.backward:
+            pairs += [(self.O, self.O_h), (self.LSE, self.LSE_h), (self.dO, self.dO_h)]
+        return [(d, h) for d, h in pairs if d is not None]
+
+    def _outputs(self):
+        if self.w.backward:
+            return list(zip((self.dQ, self.dK, self.dV), self.grads_h))
+        return [(self.O, self.O_h), (self.LSE, self.LSE_h)]
+
     def h2d_bytes(self) -> int:
-        n = sum(t.numel() * t.element_size() for t in (self.Q_h, self.K_h, self.V_h))
-        for t in (self.C_h, self.ck_h):
-            n += 0 if t is None else t.numel() * t.element_size()
-        return n
+        return sum(h.numel() * h.element_size() for _, h in self._inputs())
 
     def d2h_bytes(self) -> int:
-        return self.O.numel() * self.O.element_size() + self.LSE.numel() * 4
+        return sum(d.numel() * d.element_size() for d, _ in self._outputs())
 
     def end_to_end(self, stream):
         """One call the way a host-side user makes it: pinned host inputs in, host outputs out."""
         import exact_tiled_attention_13_gb300 as eta
 
-        self.Q.copy_(self.Q_h, non_blocking=True)
-        self.K.copy_(self.K_h, non_blocking=True)
-        self.V.copy_(self.V_h, non_blocking=True)
-        if self.C is not None:
-            self.C.copy_(self.C_h, non_blocking=True)
-        if self.ckey is not None:
-            self.ckey.copy_(self.ck_h, non_blocking=True)
+        for d, h in self._inputs():
+            d.copy_(h, non_blocking=True)
         self.launch(stream)
-        self.O_h.copy_(self.O, non_blocking=True)
-        self.LSE_h.copy_(self.LSE, non_blocking=True)
+        for d, h in self._outputs():
+            h.copy_(d, non_blocking=True)
 
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
-    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7])
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args(argv)
     import torch

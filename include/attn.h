@@ -188,6 +188,41 @@ ATTN_API int attn_fwd_splitkv_static(const void *Q, const void *K, const void *V
                                      int d, int d_v, float scale, int n_splits, void *O,
                                      int out_dtype, float *LSE, void *stream);
 
+/*
+ * attn_bwd -- gradients dQ, dK, dV of O = softmax(Q K^T * scale + C) V for a loss
+ * gradient dO, on `stream`. They are the derivatives of the attn_fwd_ex operation:
+ *     dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij = dO_i . O_i,
+ *     dS = P o (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,
+ * with P recomputed tile by tile from Q, K, the bias and the forward's LSE instead of
+ * being stored ("Compilers and kernels", section "FlashAttention rewrites the algorithm
+ * around IO", the remark after the recurrence that the backward pass recomputes the
+ * score and probability blocks). The bias C itself gets no gradient.
+ * Arguments (device pointers):
+ *   Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale
+ *            exactly as given to attn_fwd_ex for the forward pass
+ *   O        that forward pass's output [BH][Nq][d_v], element type o_dtype
+ *            (ATTN_OUT_BF16 or ATTN_OUT_F32)
+ *   dO       bf16 [BH][Nq][d_v], the gradient of the loss with respect to O
+ *   LSE      fp32 [BH][Nq], the forward pass's LSE (required here)
+ *   dQ       fp32 [BH][Nq][d];  dK fp32 [BH][Nk][d];  dV fp32 [BH][Nk][d_v]  (outputs)
+ *   workspace device memory of attn_bwd_workspace_bytes(BH, Nq) bytes, 16-byte aligned,
+ *            for the per-row statistics (LSE in log2 units and D); overwritten
+ * Alignment: Q, K, V, O, dO, C, dQ, dK, dV 16 bytes; LSE, ckey 4 bytes.
+ * Aliasing: dQ, dK, dV and the workspace overlap no input and no other output.
+ * Nq == 0 writes zeros to dK and dV; Nk == 0 with Nq >= 1 is rejected.
+ * Rows whose LSE is -inf (no allowed key) contribute nothing and get dQ_i = 0.
+ * Three kernels run on `stream` (row statistics, then dK/dV, then dQ); no atomics, so
+ * the result is deterministic. Errors as for attn_fwd_ex.
+ */
+ATTN_API int attn_bwd(const void *Q, const void *K, const void *V, const void *O, int o_dtype,
+                      const void *dO, const float *LSE, int mode, const float *C, const float *ckey,
+                      int BH, int Nq, int Nk, int d, int d_v, float scale, float *dQ, float *dK,
+                      float *dV, void *workspace, unsigned long long workspace_bytes, void *stream);
+
+/* attn_bwd_workspace_bytes -- the workspace attn_bwd needs: 2 x BH x ceil(Nq/128) x 128
+ * x 4 bytes. Returns ATTN_OK, or ATTN_ERR_INVALID_ARG (BH < 1, Nq < 0, NULL bytes). */
+ATTN_API int attn_bwd_workspace_bytes(int BH, int Nq, unsigned long long *bytes);
+
 /* Static English text for a return code (never NULL). */
 ATTN_API const char *attn_strerror(int code);
 

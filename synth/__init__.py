@@ -25,7 +25,7 @@ import os
 import numpy as np
 
 BASE_SEED = 20261202
-TENSOR_ID = {"Q": 0, "K": 1, "V": 2, "C": 3, "mask": 4, "ckey": 5}
+TENSOR_ID = {"Q": 0, "K": 1, "V": 2, "C": 3, "mask": 4, "ckey": 5, "dO": 6}
 
 MODE_NONE, MODE_CAUSAL, MODE_DENSE, MODE_KEY = 0, 1, 2, 4
 MODE_NAMES = {MODE_NONE: "none", MODE_CAUSAL: "causal", MODE_DENSE: "dense_bias",
@@ -117,6 +117,7 @@ class Workload:
     p_mask: float = 0.0
     Nk: int = 0             # keys per head; 0: as many as queries (N)
     split_kv: bool = False  # launched as a split forward pass (key ranges + merge)
+    backward: bool = False  # the step is the backward pass (dQ, dK, dV for a seeded dO)
 
     @property
     def BH(self) -> int:
@@ -148,6 +149,9 @@ WORKLOADS = {
     # last key), 8 heads: one query tile per head, so the keys are split into ranges.
     7: Workload("b1h8_nq128_nk65536_d128_causal_splitkv", 1, 8, 128, 128, 128, MODE_CAUSAL,
                 "bf16", Nk=65536, split_kv=True),
+    # The backward pass of workload 2 (O bf16 from the forward pass, dO ~ N(0,1) in bf16).
+    8: Workload("b4h16_n2048_d128_causal_bwd", 4, 16, 2048, 128, 128, MODE_CAUSAL, "bf16",
+                backward=True),
 }
 
 
@@ -212,7 +216,10 @@ def make_inputs(w: Workload, workload_id: int, base: int = BASE_SEED) -> dict:
     if w.mode & MODE_KEY:
         ckey = key_bias(seed_for(workload_id, "ckey", base), seed_for(workload_id, "mask", base),
                         BH, Nk, w.p_mask)
-    return {"Q": Q, "K": K, "V": V, "C": C, "ckey": ckey, "scale": w.scale, "mode": w.mode}
+    out = {"Q": Q, "K": K, "V": V, "C": C, "ckey": ckey, "scale": w.scale, "mode": w.mode}
+    if w.backward:
+        out["dO"] = bf16_tensor(seed_for(workload_id, "dO", base), (BH, N, w.dv))
+    return out
 
 
 def random_case(seed: int, BH: int, N: int, d: int, dv: int, mode: int, qk_mult: float = 1.0,

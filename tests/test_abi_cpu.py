@@ -211,3 +211,39 @@ def test_splitkv_zero_queries_is_noop():
 @pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
 def test_valid_splitkv_call_without_gpu_reports_no_device():
     assert call_split(Nk=1000) == eta.ATTN_ERR_NO_DEVICE
+
+
+# ---------------------------------------------------------------- backward pass
+def call_bwd(**over):
+    a = dict(Q=QP, K=KP, V=VP, O=OP, o_dtype=1, dO=0xA00000, LSE=LP, mode=0, C=None, ckey=None,
+             BH=2, Nq=48, Nk=64, d=64, d_v=64, scale=0.125, dQ=0xB00000, dK=0xC00000,
+             dV=0xD00000, workspace=0xE00000, workspace_bytes=1 << 20, stream=None)
+    a.update(over)
+    return eta.attn_bwd_raw(*a.values())
+
+
+def test_bwd_workspace_bytes():
+    assert eta.attn_bwd_workspace_bytes(3, 200) == (eta.ATTN_OK, 2 * 3 * 256 * 4)
+    assert eta.attn_bwd_workspace_bytes(1, 0) == (eta.ATTN_OK, 0)
+    assert eta.attn_bwd_workspace_bytes(0, 5)[0] == eta.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("over", [
+    dict(mode=8), dict(mode=6, C=CP, ckey=KP), dict(Nk=0), dict(LSE=None), dict(dO=None),
+    dict(workspace=None), dict(workspace_bytes=16), dict(dQ=QP), dict(dK=0xC00000 + 8),
+    dict(dV=0xC00000), dict(workspace=0xA00000), dict(mode=2, C=None), dict(o_dtype=3),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_invalid_arguments_bwd(over):
+    assert call_bwd(**over) == eta.ATTN_ERR_INVALID_ARG
+
+
+def test_bwd_unsupported_width_and_empty():
+    assert call_bwd(d=96) == eta.ATTN_ERR_UNSUPPORTED
+    assert call_bwd(Nq=0, Nk=0, Q=None, K=None, V=None, O=None, dO=None, LSE=None, dQ=None,
+                    dK=None, dV=None, workspace=None) == eta.ATTN_OK
+
+
+@pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
+def test_valid_bwd_call_without_gpu_reports_no_device():
+    assert call_bwd() == eta.ATTN_ERR_NO_DEVICE
+    assert call_bwd(Nq=0, Q=None, O=None, dO=None, LSE=None, dQ=None, workspace=None) == eta.ATTN_ERR_NO_DEVICE

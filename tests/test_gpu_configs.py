@@ -21,6 +21,8 @@ def test_workload_sampled_parity(wid):
 
     wl = DeviceWorkload(wid)
     w, c = wl.w, wl.host
+    if w.backward:
+        return _check_backward(wl)
     wl.O.fill_(float("nan"))
     wl.LSE.fill_(float("nan"))
     wl.launch()
@@ -40,3 +42,31 @@ def test_workload_sampled_parity(wid):
     stats = compare(O.reshape(-1, w.dv)[rows], L.reshape(-1)[rows], O_ref, L_ref,
                     out_bf16=w.out_dtype != "f32", label=w.name)
     print(w.name, len(rows), "rows", stats)
+
+
+def _check_backward(wl):
+    """Backward workloads: dQ on sampled rows and dK, dV on sampled keys of three heads
+    against the oracle's gradients, at the tolerance of tests/test_gpu_bwd.py."""
+    import torch
+
+    import exact_tiled_attention_13_gb300 as eta
+    from test_gpu_bwd import compare_grad
+
+    w, c = wl.w, wl.host
+    for t in (wl.dQ, wl.dK, wl.dV):
+        t.fill_(float("nan"))
+    wl.launch()
+    torch.cuda.synchronize()
+    code, word = eta.attn_device_status(None)
+    assert code == eta.ATTN_OK, f"device watchdog tripped: {word:#x}"
+    dQ, dK, dV = (t.cpu().numpy().astype(np.float64) for t in (wl.dQ, wl.dK, wl.dV))
+    assert np.isfinite(dQ).all() and np.isfinite(dK).all() and np.isfinite(dV).all()
+    heads = sorted({0, w.BH // 2, w.BH - 1})
+    qr = np.unique(np.r_[np.arange(48), np.arange(w.N - 48, w.N), np.arange(7, w.N, 97)])
+    kr = np.unique(np.r_[np.arange(48), np.arange(w.Nkv - 48, w.Nkv), np.arange(5, w.Nkv, 89)])
+    rQ, rK, rV, _ = oracle.attention_bwd(c["Q"], c["K"], c["V"], c["dO"], w.mode, c["C"],
+                                         c["ckey"], w.scale, heads=heads, qrows=qr, krows=kr)
+    stats = {}
+    for name, G, R, idx in (("dQ", dQ, rQ, qr), ("dK", dK, rK, kr), ("dV", dV, rV, kr)):
+        stats[name] = compare_grad(G[heads][:, idx], R, f"{w.name} {name}")
+    print(w.name, stats)
