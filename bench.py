@@ -47,7 +47,7 @@ METRIC = "attention fwd TFLOP/s and % of GB300 BF16 tensor roofline (N=8192,d=12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1000 * 1000
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "ptx.cuh"]
+KERNEL_SOURCES = ["attn_fwd_kernel.cuh", "attn_merge_kernel.cuh", "attn_bwd_kernel.cuh", "ptx.cuh"]
 
 
 def parse_args(argv=None):
@@ -194,7 +194,8 @@ def kernel_source_sha() -> str:
 
 def recorded_traffic(workload_id: int):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
-    path = os.path.join(PROFILE_DIR, f"attn_fwd_{synth.WORKLOADS[workload_id].name}_traffic.txt")
+    w = synth.WORKLOADS[workload_id]
+    path = os.path.join(PROFILE_DIR, f"{'attn_bwd' if w.backward else 'attn_fwd'}_{w.name}_traffic.txt")
     try:
         with open(path) as f:
             kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
