@@ -16,14 +16,18 @@
 //          D_i = dO_i . O_i, into a caller workspace [BH][nq_tiles * 128] each.
 //   dkdv : one CTA per (head, 128-key tile j). Keeps K_j and V_j in shared memory and
 //          streams the query tiles i that see tile j (Q_i, dO_i and their Lp, D) through a
-//          ring of slots. Per query tile, on the tensor cores with accumulators in tensor
-//          memory: S^T = K_j Q_i^T and dP^T = V_j dO_i^T; the elementwise warps (thread =
-//          key row = tensor-memory lane) form P^T = exp2(S^T scale log2e - Lp) and
-//          dS^T = P^T o (dP^T - D) in bf16 over S^T and dP^T; then dV_j += P^T dO_i and
-//          dK_j += dS^T Q_i. At the end dV_j and scale dK_j are written in fp32.
+//          ring of slots. Per 64-query half of a query tile, on the tensor cores with
+//          accumulators in tensor memory: S^T = K_j Q_h^T and dP^T = V_j dO_h^T; the
+//          elementwise warps (thread = key row = tensor-memory lane) form
+//          P^T = exp2(S^T scale log2e - Lp) and dS^T = P^T o (dP^T - D) in bf16 over S^T
+//          and dP^T; then dV_j += P^T dO_h and dK_j += dS^T Q_h. At the end dV_j and
+//          scale dK_j are written in fp32.
 //   dq   : one CTA per (head, 128-query tile i). Keeps Q_i and dO_i, streams the K/V tiles
-//          the tile sees: S = Q_i K_j^T, dP = dO_i V_j^T, dS = P o (dP - D) in bf16 over
-//          dP, dQ_i += dS K_j; at the end scale dQ_i in fp32.
+//          the tile sees: S = Q_i K_t^T, dP = dO_i V_t^T, dS = P o (dP - D) in bf16 over
+//          S, dQ_i += dS K_t; at the end scale dQ_i in fp32. S is double-buffered, so
+//          the next tile's S and dP run on the tensor cores while dS is formed.
+// In dkdv the two 64-query halves of a tile have their own tensor-memory buffers: while
+// the elementwise warps work on one half, the tensor cores compute the other's S and dP.
 // Warp roles of dkdv and dq (12 warps): two elementwise warpgroups (each thread owns one
 // tensor-memory lane and half of the 128 columns), the MMA warp (whole warp, one elected
 // lane issues) and one TMA producer warp. Every wait is bounded (the forward kernel's
@@ -102,6 +106,12 @@ __global__ void __launch_bounds__(256)
 // Bias sources of the backward kernels.
 enum { BWD_BIAS_NONE = 0, BWD_BIAS_DENSE = 1, BWD_BIAS_KEY = 2 };
 
+// Both main kernels work through 128-wide tiles in two halves of 64 columns (queries in
+// dkdv, keys in dq). Each half has its own score and dP buffers in tensor memory, so the
+// elementwise warps work on one half while the tensor cores compute the next half's
+// products: MMA order S/dP(u+1), then the accumulating products of u.
+constexpr int HALF = 64;
+
 template <int D, int DV, bool CAUSAL, int BIAS>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "d must be 64 or 128");
@@ -117,26 +127,34 @@ struct BwdCfg {
   static constexpr int A_V_OFF = Q_TILE;
   static constexpr int A_SLOT_OFF = Q_TILE + DO_TILE;
   static constexpr int A_BAR_OFF = A_SLOT_OFF + A_QS * A_SLOT;
-  // dq: Q_i, dO_i resident; ring of (K_j, V_j) slots.
-  static constexpr int B_SLOT = Q_TILE + DO_TILE;
-  static constexpr int B_KS = cmin(3, (BUDGET - Q_TILE - DO_TILE) / B_SLOT);
+  // dq: Q_i, dO_i resident; a ring of K_j tiles and a ring of V_j tiles. V_j is released
+  // as soon as dP(j) is done, K_j only after dQ += dS K_j, so K gets the deeper ring.
+  static constexpr int B_REST = BUDGET - Q_TILE - DO_TILE;
+  static constexpr int B_KS = cmin(4, (B_REST - 2 * DO_TILE) / Q_TILE);
+  static constexpr int B_VS = cmin(4, (B_REST - B_KS * Q_TILE) / DO_TILE);
   static constexpr int B_Q_OFF = 0;
   static constexpr int B_DO_OFF = Q_TILE;
-  static constexpr int B_SLOT_OFF = Q_TILE + DO_TILE;
-  static constexpr int B_BAR_OFF = B_SLOT_OFF + B_KS * B_SLOT;
-  static_assert(A_QS >= 2 && B_KS >= 2, "need two ring slots");
-  static_assert(A_SLOT % 1024 == 0 && B_SLOT % 1024 == 0, "slots keep 1024-byte alignment");
+  static constexpr int B_K_OFF = Q_TILE + DO_TILE;
+  static constexpr int B_V_OFF = B_K_OFF + B_KS * Q_TILE;
+  static constexpr int B_BAR_OFF = B_V_OFF + B_VS * DO_TILE;
+  static_assert(A_QS >= 2 && B_KS >= 2 && B_VS >= 2, "need two ring slots");
+  static_assert(A_SLOT % 1024 == 0, "slots keep 1024-byte alignment");
 
-  // barriers (the same layout serves both kernels; RING = ring slots)
-  static constexpr int RING = A_QS > B_KS ? A_QS : B_KS;
+  // barriers (the same layout serves both kernels; RING = ring slots; dq's K ring uses
+  // FULL/EMPTY, its V ring VFULL/VEMPTY)
+  static constexpr int RING = cmin(4, A_QS > B_KS ? A_QS : B_KS);
   static constexpr int BAR_FIXED = 0;               // K_j/V_j (dkdv) or Q_i/dO_i (dq)
   static constexpr int BAR_FULL = 1;                // ring slot filled
   static constexpr int BAR_EMPTY = BAR_FULL + RING; // ring slot released
-  static constexpr int BAR_SFULL = BAR_EMPTY + RING;
-  static constexpr int BAR_PFULL = BAR_SFULL + 1;   // 8 elementwise warps arrive
-  static constexpr int BAR_ACC = BAR_PFULL + 1;
+  static constexpr int BAR_SFULL = BAR_EMPTY + RING;  // [2]: S and dP of a half ready
+  static constexpr int BAR_PFULL = BAR_SFULL + 2;     // [2]: its bf16 P and dS written (8 warps)
+  static constexpr int BAR_ACC = BAR_PFULL + 2;
   static constexpr int BAR_DRAIN = BAR_ACC + 1;
-  static constexpr int NUM_BARS = BAR_DRAIN + 1;
+  static constexpr int BAR_DPFULL = BAR_DRAIN + 1;  // dq: dP of a key tile ready
+  static constexpr int BAR_DPFREE = BAR_DPFULL + 1;  // dq: dP read into registers (8 warps)
+  static constexpr int BAR_VFULL = BAR_DPFREE + 1;   // dq: [B_VS]
+  static constexpr int BAR_VEMPTY = BAR_VFULL + 4;   // dq: [B_VS]
+  static constexpr int NUM_BARS = BAR_VEMPTY + 4;
   static constexpr int BAR_BYTES = NUM_BARS * 8;
   static constexpr int TAIL_BYTES = BAR_BYTES + 8;  // + tensor-memory address + abort flag
   static constexpr int A_SMEM = A_BAR_OFF + TAIL_BYTES + 1024;
@@ -146,7 +164,7 @@ struct BwdCfg {
   static constexpr int A_SMEM_TOTAL = A_SMEM > 120 * 1024 ? A_SMEM : 120 * 1024;
   static constexpr int B_SMEM_TOTAL = B_SMEM > 120 * 1024 ? B_SMEM : 120 * 1024;
 
-  // tensor memory
+  // tensor memory: half b of the scores at S_COL + 64 b, of dP at DP_COL + 64 b
   static constexpr int S_COL = 0;     // S^T (dkdv) or S (dq); P^T packed over it
   static constexpr int DP_COL = 128;  // dP^T or dP; dS^T / dS packed over it
   static constexpr int ACC0_COL = 256;        // dV (dkdv) or dQ (dq)
@@ -158,9 +176,10 @@ struct BwdCfg {
   static constexpr int MMA_WARP = 8;
   static constexpr int LOAD_WARP = 9;
 
-  static constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, false);
-  static constexpr uint32_t IDESC_NV = idesc_bf16_f32(128, DV, true);  // dV += P^T dO
-  static constexpr uint32_t IDESC_ND = idesc_bf16_f32(128, D, true);   // dK, dQ
+  static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(128, HALF, false);  // S, dP halves
+  static constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, false);     // full-width S, dP
+  static constexpr uint32_t IDESC_NV = idesc_bf16_f32(128, DV, true);       // dV += P^T dO
+  static constexpr uint32_t IDESC_ND = idesc_bf16_f32(128, D, true);        // dK, dQ
 };
 
 // K-major operand step ks (16 elements of the contraction) inside 128-row boxes of 64
@@ -168,11 +187,17 @@ struct BwdCfg {
 __device__ __forceinline__ uint32_t kmajor_step(int ks) {
   return static_cast<uint32_t>(((ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32) >> 4);
 }
-// Packed bf16 A operand in tensor memory for step ks (16 columns of the contraction):
-// elementwise warpgroup g owns contraction columns [64g, 64g + 64) and stores them,
-// two per 32-bit column, at [64g, 64g + 32).
-__device__ __forceinline__ uint32_t packed_col(int ks) {
-  return static_cast<uint32_t>(64 * (ks / 4) + 8 * (ks % 4));
+// Rows 64 h .. 64 h + 63 of a 128-row K-major box (eight 1024-byte groups of 8 rows).
+__device__ __forceinline__ uint32_t half_rows(int h) { return static_cast<uint32_t>((h * HALF * 128) >> 4); }
+// MN-major operand (contraction along rows): step ks of 16 rows, starting at row 64 h.
+__device__ __forceinline__ uint32_t mn_step(int h, int ks) {
+  return static_cast<uint32_t>(((h * HALF + ks * 16) * 128) >> 4);
+}
+// Packed bf16 A operand of half-buffer b for step ks (16 of its 64 columns): elementwise
+// warpgroup g owns columns [32 g, 32 g + 32) of the half and stores them, two per 32-bit
+// column, at [32 g, 32 g + 16) of the half's 64 columns.
+__device__ __forceinline__ uint32_t packed_col(int b, int ks) {
+  return static_cast<uint32_t>(HALF * b + 32 * (ks / 2) + 8 * (ks % 2));
 }
 
 // Loads a 32-column chunk of two tensor-memory matrices.
@@ -226,7 +251,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // This CTA: head bh, key tile j; the query tiles that see it are i_lo .. nq_tiles - 1.
+  // This CTA: head bh, key tile j; the query tiles that see it are i_lo .. nq_tiles - 1,
+  // each in two halves of 64 queries (units u = 0 .. 2 n_it - 1).
   const int bh = blockIdx.x / p.nkv_tiles;
   const int j = static_cast<int>(blockIdx.x % p.nkv_tiles);
   int i_lo = 0;
@@ -236,7 +262,11 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     i_lo = q0 >= p.Nq ? p.nq_tiles : (q0 <= 0 ? 0 : q0 / BM);
   }
   const int n_it = p.nq_tiles - i_lo;
+  const int n_u = 2 * n_it;
   BwdWatchdog wd{sbase + CF::A_BAR_OFF + CF::BAR_BYTES + 4, p};
+#ifdef ETA_PHASE_TRACE
+  int trace_n = 0;
+#endif
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(CF::BAR_FIXED), 1);
@@ -244,8 +274,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       mbar_init(BAR(CF::BAR_FULL + s), 1);
       mbar_init(BAR(CF::BAR_EMPTY + s), 1);
     }
-    mbar_init(BAR(CF::BAR_SFULL), 1);
-    mbar_init(BAR(CF::BAR_PFULL), 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(CF::BAR_SFULL + b), 1);
+      mbar_init(BAR(CF::BAR_PFULL + b), 8);
+    }
     mbar_init(BAR(CF::BAR_ACC), 1);
     mbar_init(BAR(CF::BAR_DRAIN), 1);
     *abort_flag = 0;
@@ -262,66 +294,77 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 
   if (warp < 8) {
     // ============================================================ elementwise
-    const int g = warp / 4;  // columns (queries) [64 g, 64 g + 64)
+    const int g = warp / 4;  // columns [32 g, 32 g + 32) of each 64-query half
     const int r = threadIdx.x % 128;
     const int key = j * BN + r;
     const bool key_ok = key < p.Nk;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
-    const uint32_t t_s = tmem + lane_off + CF::S_COL;
-    const uint32_t t_dp = tmem + lane_off + CF::DP_COL;
-    float kb = 0.0f;  // per-key bias of this row, log2-scaled
+    // Per-key bias of this row, log2-scaled (-inf for a padded key: its p is 0). Rows past
+    // the last key need no mask: their K and V rows are zero-filled, so they only produce
+    // dK and dV rows that are never stored.
+    float kb = 0.0f;
     if (BIAS == BWD_BIAS_KEY) kb = key_ok ? p.ckey[static_cast<size_t>(bh) * p.Nk + key] * LOG2E : 0.0f;
-    const bool row_dead = !key_ok || (BIAS == BWD_BIAS_KEY && kb == -INFINITY);
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int i = i_lo + it;
-      const int slot = it % CF::A_QS;
-      ok = wd.wait(BAR(CF::BAR_SFULL), it & 1, ROLE_SOFTMAX, CF::BAR_SFULL);
+    for (int u = 0; u < n_u; ++u) {
+      const int b = u & 1;  // half within the query tile = tensor-memory buffer
+      const int i = i_lo + u / 2;
+      const int slot = (u / 2) % CF::A_QS;
+      ok = wd.wait(BAR(CF::BAR_SFULL + b), (u / 2) & 1, ROLE_SOFTMAX, CF::BAR_SFULL + b);
       if (!ok) break;
       tc_fence_after();
+      ETA_TRACE(40);
+      const int c0 = HALF * b + 32 * g;  // query offset within the tile
       const float *Ls = reinterpret_cast<const float *>(smem + CF::A_SLOT_OFF + slot * CF::A_SLOT +
-                                                        CF::Q_TILE + CF::DO_TILE);
+                                                        CF::Q_TILE + CF::DO_TILE) + c0;
       const float *Ds = Ls + BM;
-      // Keys past the causal limit of the tile's first query need the elementwise test.
-      const bool diag = CAUSAL && (j * BN + BN - 1 > i * BM + p.causal_off);
+      // Keys past the causal limit of this chunk's first query need the elementwise test.
+      const bool diag = CAUSAL && (j * BN + BN - 1 > i * BM + c0 + p.causal_off);
+      const uint32_t t_s = tmem + lane_off + CF::S_COL + HALF * b + 32 * g;
+      const uint32_t t_dp = tmem + lane_off + CF::DP_COL + HALF * b + 32 * g;
+      uint32_t sr[32], dr[32];
+      ld_pair(t_s, t_dp, sr, dr);
+      ETA_TRACE(41);
+      if (diag) {  // keys past query q's causal limit: S = -inf, so p = 0
+        const int lim = i * BM + c0 + p.causal_off - key;  // column c is forbidden when c < -lim
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c0 = 64 * g + 32 * h;
-        uint32_t sr[32], dr[32];
-        ld_pair(t_s + c0, t_dp + c0, sr, dr);
-        uint32_t pp[16], dd[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          const float4 L4 = *reinterpret_cast<const float4 *>(Ls + c0 + c);
-          const float4 D4 = *reinterpret_cast<const float4 *>(Ds + c0 + c);
-          const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
-          const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
-          float pv[4], dv[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = i * BM + c0 + c + u;
-            float x = fmaf(__uint_as_float(sr[c + u]), p.scale_log2, kb) - Lv[u];
-            if (BIAS == BWD_BIAS_DENSE)
-              x += (key_ok && q < p.Nq) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
-                                        : 0.0f;
-            if (diag && key > q + p.causal_off) x = -INFINITY;
-            if (row_dead) x = -INFINITY;
-            const float pr = ex2_approx(x);
-            pv[u] = pr;
-            dv[u] = pr * (__uint_as_float(dr[c + u]) - Dv[u]);
-          }
-          pp[c / 2] = pack_bf16(pv[0], pv[1]);
-          pp[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
-          dd[c / 2] = pack_bf16(dv[0], dv[1]);
-          dd[c / 2 + 1] = pack_bf16(dv[2], dv[3]);
-        }
-        tmem_st16(t_s + 64 * g + 16 * h, pp);
-        tmem_st16(t_dp + 64 * g + 16 * h, dd);
+        for (int c = 0; c < 32; ++c)
+          if (c + lim < 0) sr[c] = __float_as_uint(-INFINITY);
       }
+      uint32_t pp[16], dd[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const float4 L4 = *reinterpret_cast<const float4 *>(Ls + c);
+        const float4 D4 = *reinterpret_cast<const float4 *>(Ds + c);
+        const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
+        const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+        float pv[4], dv[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          // x = (scale S + bias) log2(e) - LSE log2(e), so that p = 2^x = exp(S_ij - LSE_i).
+          float x = BIAS == BWD_BIAS_KEY ? fmaf(__uint_as_float(sr[c + v]), p.scale_log2, kb) - Lv[v]
+                                         : fmaf(__uint_as_float(sr[c + v]), p.scale_log2, -Lv[v]);
+          if (BIAS == BWD_BIAS_DENSE) {
+            const int q = i * BM + c0 + c + v;
+            x += (key_ok && q < p.Nq) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
+                                      : 0.0f;
+          }
+          const float pr = ex2_approx(x);
+          pv[v] = pr;
+          dv[v] = pr * (__uint_as_float(dr[c + v]) - Dv[v]);
+        }
+        pp[c / 2] = pack_bf16(pv[0], pv[1]);
+        pp[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
+        dd[c / 2] = pack_bf16(dv[0], dv[1]);
+        dd[c / 2 + 1] = pack_bf16(dv[2], dv[3]);
+      }
+      ETA_TRACE(42);
+      tmem_st16(t_s, pp);
+      tmem_st16(t_dp, dd);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      mbar_arrive_elect(BAR(CF::BAR_PFULL));
+      mbar_arrive_elect(BAR(CF::BAR_PFULL + b));
+      ETA_TRACE(43);
     }
     // ---------------------------------------------------------- epilogue: dV, scale dK
     float *dv_row = p.dV + (static_cast<size_t>(bh) * p.Nk + (key_ok ? key : 0)) * DV;
@@ -342,40 +385,56 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     bool ok = n_it == 0 || wd.wait(BAR(CF::BAR_FIXED), 0, ROLE_MMA, CF::BAR_FIXED);
     const uint64_t k_desc = smem_desc(sbase + CF::A_K_OFF, 16, 1024);
     const uint64_t v_desc = smem_desc(sbase + CF::A_V_OFF, 16, 1024);
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int slot = it % CF::A_QS;
+    // S^T and dP^T of unit u (both operands K-major; B = rows 64 h of the slot's tiles).
+    auto issue_sdp = [&](int u) -> bool {
+      const int b = u & 1;
+      const int slot = (u / 2) % CF::A_QS;
+      if (b == 0) {  // a new query tile: wait for its copies
+        if (!wd.wait(BAR(CF::BAR_FULL + slot), ((u / 2) / CF::A_QS) & 1, ROLE_MMA, CF::BAR_FULL + slot))
+          return false;
+        tc_fence_after();
+      }
       const uint32_t sl = sbase + CF::A_SLOT_OFF + slot * CF::A_SLOT;
-      ok = wd.wait(BAR(CF::BAR_FULL + slot), (it / CF::A_QS) & 1, ROLE_MMA, CF::BAR_FULL + slot);
-      if (!ok) break;
-      tc_fence_after();
-      // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (both operands K-major).
-      const uint64_t q_desc = smem_desc(sl, 16, 1024);
-      const uint64_t do_desc = smem_desc(sl + CF::Q_TILE, 16, 1024);
+      const uint64_t q_desc = smem_desc(sl, 16, 1024) + half_rows(b);
+      const uint64_t do_desc = smem_desc(sl + CF::Q_TILE, 16, 1024) + half_rows(b);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_ss_elect(tmem + CF::S_COL, k_desc + kmajor_step(ks), q_desc + kmajor_step(ks),
-                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
+        mma_ss_elect(tmem + CF::S_COL + HALF * b, k_desc + kmajor_step(ks), q_desc + kmajor_step(ks),
+                     CF::IDESC_HALF, ks > 0 ? 1u : 0u);
 #pragma unroll
       for (int ks = 0; ks < DV / 16; ++ks)
-        mma_ss_elect(tmem + CF::DP_COL, v_desc + kmajor_step(ks), do_desc + kmajor_step(ks),
-                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
-      mma_commit_elect(BAR(CF::BAR_SFULL));
-      ok = wd.wait(BAR(CF::BAR_PFULL), it & 1, ROLE_MMA, CF::BAR_PFULL);
+        mma_ss_elect(tmem + CF::DP_COL + HALF * b, v_desc + kmajor_step(ks), do_desc + kmajor_step(ks),
+                     CF::IDESC_HALF, ks > 0 ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_SFULL + b));
+      return true;
+    };
+    if (ok && n_u > 0) ok = issue_sdp(0);
+    for (int u = 0; ok && u < n_u; ++u) {
+      const int b = u & 1;
+      const int slot = (u / 2) % CF::A_QS;
+      // The next half's products go first, so the tensor cores work while this half's
+      // P and dS are formed (its buffer was last read by the products of u - 1).
+      ETA_TRACE(50);
+      if (u + 1 < n_u && !(ok = issue_sdp(u + 1))) break;
+      ETA_TRACE(51);
+      ok = wd.wait(BAR(CF::BAR_PFULL + b), (u / 2) & 1, ROLE_MMA, CF::BAR_PFULL + b);
       if (!ok) break;
       tc_fence_after();
-      // dV_j += P^T dO_i, dK_j += dS^T Q_i (A from tensor memory, B MN-major: the
-      // contraction runs over the 128 query rows of the slot's tiles).
+      ETA_TRACE(52);
+      // dV_j += P^T dO_h, dK_j += dS^T Q_h (A from tensor memory, B MN-major over the
+      // half's 64 query rows).
+      const uint32_t sl = sbase + CF::A_SLOT_OFF + slot * CF::A_SLOT;
       const uint64_t do_mn = smem_desc(sl + CF::Q_TILE, SW_CHUNK_BYTES, 1024);
       const uint64_t q_mn = smem_desc(sl, SW_CHUNK_BYTES, 1024);
 #pragma unroll
-      for (int ks = 0; ks < BM / 16; ++ks)
-        mma_ts_elect(tmem + CF::ACC0_COL, tmem + CF::S_COL + packed_col(ks),
-                     do_mn + ((ks * 16 * 128) >> 4), CF::IDESC_NV, (it > 0 || ks > 0) ? 1u : 0u);
+      for (int ks = 0; ks < HALF / 16; ++ks)
+        mma_ts_elect(tmem + CF::ACC0_COL, tmem + CF::S_COL + packed_col(b, ks), do_mn + mn_step(b, ks),
+                     CF::IDESC_NV, (u > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-      for (int ks = 0; ks < BM / 16; ++ks)
-        mma_ts_elect(tmem + CF::ACC1_COL, tmem + CF::DP_COL + packed_col(ks),
-                     q_mn + ((ks * 16 * 128) >> 4), CF::IDESC_ND, (it > 0 || ks > 0) ? 1u : 0u);
-      mma_commit_elect(BAR(CF::BAR_EMPTY + slot));
+      for (int ks = 0; ks < HALF / 16; ++ks)
+        mma_ts_elect(tmem + CF::ACC1_COL, tmem + CF::DP_COL + packed_col(b, ks), q_mn + mn_step(b, ks),
+                     CF::IDESC_ND, (u > 0 || ks > 0) ? 1u : 0u);
+      if (b == 1) mma_commit_elect(BAR(CF::BAR_EMPTY + slot));  // both halves of the tile done
     }
     if (ok && n_it > 0) mma_commit_elect(BAR(CF::BAR_ACC));
     mma_commit_elect(BAR(CF::BAR_DRAIN));
@@ -401,6 +460,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
                     CF::BAR_EMPTY + slot, false))
         break;
       const uint32_t sl = sbase + CF::A_SLOT_OFF + slot * CF::A_SLOT;
+      ETA_TRACE(60);
       mbar_arrive_expect_tx(BAR(CF::BAR_FULL + slot), CF::Q_TILE + CF::DO_TILE + CF::LD_BYTES);
       for (int kc = 0; kc < D / SW_CHUNK; ++kc)
         tma_load_3d(sl + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK, i * BM, bh, BAR(CF::BAR_FULL + slot));
@@ -428,12 +488,21 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 }
 
 // ------------------------------------------------------------------------ dQ
+// Tensor memory of the dQ kernel: two full-width score buffers S_0, S_1 (128 columns
+// each; dS is packed over the one it came from), one dP buffer and the dQ accumulator.
+// While the elementwise warps turn S(t), dP(t) into dS(t), the tensor cores compute
+// S(t+1) into the other buffer and, once dP(t) has been read into registers, dP(t+1).
+constexpr int DQ_S0_COL = 0;
+constexpr int DQ_DP_COL = 256;
+constexpr int DQ_ACC_COL = 384;
+
 template <int D, int DV, bool CAUSAL, int BIAS>
 __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const __grid_constant__ BwdParams p) {
   using CF = BwdCfg<D, DV, CAUSAL, BIAS>;
+  static_assert(DQ_ACC_COL + D <= CF::TMEM_COLS, "dQ accumulator past the tensor memory");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -444,6 +513,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::B_BAR_OFF + CF::BAR_BYTES + 4);
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  // Barriers of this kernel: SFULL[2] per score buffer, DSFULL[2] per score buffer (dS(t)
+  // written by the 8 elementwise warps), DPFULL, DPFREE (dP(t) read into registers by the
+  // 8 elementwise warps). DSFULL is per buffer because warps can finish a tile at
+  // different times: a fast warp's arrival for tile t+1 must not complete tile t's phase.
+  // A warp cannot get two tiles ahead: S(t+2) is issued only after DSFULL(t).
+  const int B_DPFREE = CF::BAR_DPFREE;
+  const int B_DSFULL = CF::BAR_PFULL;  // [2]
 
   // This CTA: head bh, query tile i; it visits key tiles 0 .. hi (none when hi < 0).
   const int bh = blockIdx.x / p.nq_tiles;
@@ -452,6 +528,9 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   if (CAUSAL) hi = cmin(floor_div(cmin(i * BM + BM - 1, p.Nq - 1) + p.causal_off, BN), hi);
   const int n_it = hi + 1 > 0 ? hi + 1 : 0;
   BwdWatchdog wd{sbase + CF::B_BAR_OFF + CF::BAR_BYTES + 4, p};
+#ifdef ETA_PHASE_TRACE
+  int trace_n = 0;
+#endif
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(CF::BAR_FIXED), 1);
@@ -459,8 +538,16 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       mbar_init(BAR(CF::BAR_FULL + s), 1);
       mbar_init(BAR(CF::BAR_EMPTY + s), 1);
     }
-    mbar_init(BAR(CF::BAR_SFULL), 1);
-    mbar_init(BAR(CF::BAR_PFULL), 8);
+    for (int s = 0; s < CF::B_VS; ++s) {
+      mbar_init(BAR(CF::BAR_VFULL + s), 1);
+      mbar_init(BAR(CF::BAR_VEMPTY + s), 1);
+    }
+    mbar_init(BAR(CF::BAR_SFULL + 0), 1);
+    mbar_init(BAR(CF::BAR_SFULL + 1), 1);
+    mbar_init(BAR(B_DSFULL + 0), 8);
+    mbar_init(BAR(B_DSFULL + 1), 8);
+    mbar_init(BAR(B_DPFREE), 8);
+    mbar_init(BAR(CF::BAR_DPFULL), 1);
     mbar_init(BAR(CF::BAR_ACC), 1);
     mbar_init(BAR(CF::BAR_DRAIN), 1);
     *abort_flag = 0;
@@ -477,55 +564,71 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 
   if (warp < 8) {
     // ============================================================ elementwise
-    const int g = warp / 4;  // columns (keys) [64 g, 64 g + 64)
+    const int g = warp / 4;  // columns (keys) [64 g, 64 g + 64) of each key tile
     const int r = threadIdx.x % 128;
     const int q = i * BM + r;
     const bool q_ok = q < p.Nq;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
-    const uint32_t t_s = tmem + lane_off + CF::S_COL;
-    const uint32_t t_dp = tmem + lane_off + CF::DP_COL;
     const size_t lrow = static_cast<size_t>(bh) * p.nqp + static_cast<size_t>(q);
     const float Lr = p.Lp[lrow];  // +inf for padding rows and rows with no allowed key
     const float Dr = p.Dd[lrow];
     const int lim = CAUSAL ? q + p.causal_off : INT_MAX;  // last key this row may see
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int j = it;
-      ok = wd.wait(BAR(CF::BAR_SFULL), it & 1, ROLE_SOFTMAX, CF::BAR_SFULL);
+    for (int t = 0; t < n_it; ++t) {
+      const int b = t & 1;
+      ok = wd.wait(BAR(CF::BAR_SFULL + b), (t >> 1) & 1, ROLE_SOFTMAX, CF::BAR_SFULL + b) &&
+           wd.wait(BAR(CF::BAR_DPFULL), t & 1, ROLE_SOFTMAX, CF::BAR_DPFULL);
       if (!ok) break;
       tc_fence_after();
-      const bool mask = (CAUSAL && (j * BN + BN - 1 > i * BM + p.causal_off)) ||
-                        (j == p.nkv_tiles - 1 && (p.Nk % BN) != 0);
+      ETA_TRACE(70);
+      // dP(t) into registers first: its buffer is then free for dP(t+1).
+      uint32_t da[32], db[32];
+      ld_pair(tmem + lane_off + DQ_DP_COL + 64 * g, tmem + lane_off + DQ_DP_COL + 64 * g + 32, da, db);
+      tc_fence_before();
+      __syncwarp();
+      mbar_arrive_elect(BAR(B_DPFREE));
+      ETA_TRACE(71);
+      const uint32_t t_s = tmem + lane_off + DQ_S0_COL + 128 * b + 64 * g;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int c0 = 64 * g + 32 * h;
-        uint32_t sr[32], dr[32];
-        ld_pair(t_s + c0, t_dp + c0, sr, dr);
+        uint32_t sr[32];
+        tmem_ld32(t_s + 32 * h, sr);
+        tmem_wait_ld(sr);
+        const int k0 = t * BN + 64 * g + 32 * h;  // first key of these 32 columns
+        if ((CAUSAL && (k0 + 31 > i * BM + p.causal_off)) || (k0 + 31 >= p.Nk)) {
+          const int last = cmin(lim, p.Nk - 1) - k0;  // column c is allowed when c <= last
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c > last) sr[c] = __float_as_uint(-INFINITY);
+        }
         uint32_t dd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float dv2[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int key = j * BN + c0 + c + u;
-            float x = fmaf(__uint_as_float(sr[c + u]), p.scale_log2, -Lr);
+          for (int v = 0; v < 2; ++v) {
+            const int key = k0 + c + v;
+            float x = fmaf(__uint_as_float(sr[c + v]), p.scale_log2, -Lr);
             if (BIAS == BWD_BIAS_KEY)
               x += key < p.Nk ? __ldg(p.ckey + static_cast<size_t>(bh) * p.Nk + key) * LOG2E : 0.0f;
             if (BIAS == BWD_BIAS_DENSE)
               x += (q_ok && key < p.Nk) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
                                         : 0.0f;
-            if (mask && (key > lim || key >= p.Nk)) x = -INFINITY;
             const float pr = ex2_approx(x);
-            dv2[u] = pr * (__uint_as_float(dr[c + u]) - Dr);
+            const float dpv = __uint_as_float(h == 0 ? da[c + v] : db[c + v]);
+            dv2[v] = pr * (dpv - Dr);
           }
           dd[c / 2] = pack_bf16(dv2[0], dv2[1]);
         }
-        tmem_st16(t_dp + 64 * g + 16 * h, dd);
+        // Packed dS over the S columns this warp has read: keys [64 g + 32 h, +32) at
+        // 32-bit columns [64 g + 16 h, +16).
+        tmem_st16(t_s + 16 * h, dd);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      mbar_arrive_elect(BAR(CF::BAR_PFULL));
+      mbar_arrive_elect(BAR(B_DSFULL + b));
+      ETA_TRACE(73);
     }
     // ---------------------------------------------------------- epilogue: scale dQ
     float *dq_row = p.dQ + (static_cast<size_t>(bh) * p.Nq + (q_ok ? q : 0)) * D;
@@ -533,7 +636,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       ok = wd.wait(BAR(CF::BAR_ACC), 0, ROLE_SOFTMAX, CF::BAR_ACC);
       if (ok) {
         tc_fence_after();
-        store_acc_row(tmem + lane_off + CF::ACC0_COL, g * D / 2, D / 2, p.scale, dq_row, q_ok);
+        store_acc_row(tmem + lane_off + DQ_ACC_COL, g * D / 2, D / 2, p.scale, dq_row, q_ok);
       }
     } else if (ok) {
       store_zero_row(D / 2, dq_row + g * D / 2, q_ok);
@@ -543,43 +646,67 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     bool ok = n_it == 0 || wd.wait(BAR(CF::BAR_FIXED), 0, ROLE_MMA, CF::BAR_FIXED);
     const uint64_t q_desc = smem_desc(sbase + CF::B_Q_OFF, 16, 1024);
     const uint64_t do_desc = smem_desc(sbase + CF::B_DO_OFF, 16, 1024);
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int slot = it % CF::B_KS;
-      const uint32_t sl = sbase + CF::B_SLOT_OFF + slot * CF::B_SLOT;
-      ok = wd.wait(BAR(CF::BAR_FULL + slot), (it / CF::B_KS) & 1, ROLE_MMA, CF::BAR_FULL + slot);
-      if (!ok) break;
+    auto k_addr = [&](int t) -> uint32_t { return sbase + CF::B_K_OFF + (t % CF::B_KS) * CF::Q_TILE; };
+    // S(t) = Q_i K_t^T into buffer t & 1, after waiting for the copy of K_t.
+    auto issue_s = [&](int t) -> bool {
+      const int slot = t % CF::B_KS;
+      if (!wd.wait(BAR(CF::BAR_FULL + slot), (t / CF::B_KS) & 1, ROLE_MMA, CF::BAR_FULL + slot)) return false;
       tc_fence_after();
-      // S = Q_i K_j^T and dP = dO_i V_j^T (both operands K-major).
-      const uint64_t k_desc = smem_desc(sl, 16, 1024);
-      const uint64_t v_desc = smem_desc(sl + CF::Q_TILE, 16, 1024);
+      const uint64_t k_desc = smem_desc(k_addr(t), 16, 1024);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_ss_elect(tmem + CF::S_COL, q_desc + kmajor_step(ks), k_desc + kmajor_step(ks),
+        mma_ss_elect(tmem + DQ_S0_COL + 128 * (t & 1), q_desc + kmajor_step(ks), k_desc + kmajor_step(ks),
                      CF::IDESC_SS, ks > 0 ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_SFULL + (t & 1)));
+      return true;
+    };
+    // dP(t) = dO_i V_t^T after waiting for the copy of V_t; V_t's slot is released when
+    // the product is done.
+    auto issue_dp = [&](int t) -> bool {
+      const int slot = t % CF::B_VS;
+      if (!wd.wait(BAR(CF::BAR_VFULL + slot), (t / CF::B_VS) & 1, ROLE_MMA, CF::BAR_VFULL + slot)) return false;
+      tc_fence_after();
+      const uint64_t v_desc = smem_desc(sbase + CF::B_V_OFF + slot * CF::DO_TILE, 16, 1024);
 #pragma unroll
       for (int ks = 0; ks < DV / 16; ++ks)
-        mma_ss_elect(tmem + CF::DP_COL, do_desc + kmajor_step(ks), v_desc + kmajor_step(ks),
-                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
-      mma_commit_elect(BAR(CF::BAR_SFULL));
-      ok = wd.wait(BAR(CF::BAR_PFULL), it & 1, ROLE_MMA, CF::BAR_PFULL);
+        mma_ss_elect(tmem + DQ_DP_COL, do_desc + kmajor_step(ks), v_desc + kmajor_step(ks), CF::IDESC_SS,
+                     ks > 0 ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_DPFULL));
+      mma_commit_elect(BAR(CF::BAR_VEMPTY + slot));
+      return true;
+    };
+    if (ok && n_it > 0) ok = issue_s(0) && issue_dp(0);
+    for (int t = 0; ok && t < n_it; ++t) {
+      ETA_TRACE(80);
+      if (t + 1 < n_it) {
+        // S(t+1) into the other buffer (last read by dQ(t-1), issued before it).
+        if (!(ok = issue_s(t + 1))) break;
+        ETA_TRACE(81);
+        // dP(t+1) once the elementwise warps hold dP(t) in registers.
+        if (!(ok = wd.wait(BAR(B_DPFREE), t & 1, ROLE_MMA, B_DPFREE))) break;
+        tc_fence_after();
+        if (!(ok = issue_dp(t + 1))) break;
+        ETA_TRACE(82);
+      }
+      ok = wd.wait(BAR(B_DSFULL + (t & 1)), (t >> 1) & 1, ROLE_MMA, B_DSFULL + (t & 1));
       if (!ok) break;
       tc_fence_after();
-      // dQ_i += dS K_j (A = dS from tensor memory, B = K_j MN-major over the 128 keys).
-      const uint64_t k_mn = smem_desc(sl, SW_CHUNK_BYTES, 1024);
+      ETA_TRACE(83);
+      // dQ_i += dS(t) K_t: A = dS packed in buffer t & 1, B = K_t MN-major over 128 keys.
+      const uint64_t k_mn = smem_desc(k_addr(t), SW_CHUNK_BYTES, 1024);
 #pragma unroll
       for (int ks = 0; ks < BN / 16; ++ks)
-        mma_ts_elect(tmem + CF::ACC0_COL, tmem + CF::DP_COL + packed_col(ks),
-                     k_mn + ((ks * 16 * 128) >> 4), CF::IDESC_ND, (it > 0 || ks > 0) ? 1u : 0u);
-      mma_commit_elect(BAR(CF::BAR_EMPTY + slot));
+        mma_ts_elect(tmem + DQ_ACC_COL, tmem + DQ_S0_COL + 128 * (t & 1) + 64 * (ks / 4) + 8 * (ks % 4),
+                     k_mn + ((ks * 16 * 128) >> 4), CF::IDESC_ND, (t > 0 || ks > 0) ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_EMPTY + (t % CF::B_KS)));
     }
     if (ok && n_it > 0) mma_commit_elect(BAR(CF::BAR_ACC));
     mma_commit_elect(BAR(CF::BAR_DRAIN));
     wd.drain(BAR(CF::BAR_DRAIN), 0, CF::BAR_DRAIN);
   } else if (warp == CF::LOAD_WARP && lane == 0) {
-    // ============================================================ TMA producer
+    // ============================================================ TMA producer: Q, dO, K
     if (n_it > 0) {
       tma_prefetch_desc(&tmK);
-      tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(BAR(CF::BAR_FIXED), CF::Q_TILE + CF::DO_TILE);
       for (int kc = 0; kc < D / SW_CHUNK; ++kc)
         tma_load_3d(sbase + CF::B_Q_OFF + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK, i * BM, bh,
@@ -590,24 +717,39 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     }
     int issued = 0;
     for (int it = 0; it < n_it; ++it) {
-      const int j = it;
       const int slot = it % CF::B_KS;
       if (!wd.wait1(BAR(CF::BAR_EMPTY + slot), ((it / CF::B_KS) & 1) ^ 1, ROLE_LOAD,
                     CF::BAR_EMPTY + slot, false))
         break;
-      const uint32_t sl = sbase + CF::B_SLOT_OFF + slot * CF::B_SLOT;
-      mbar_arrive_expect_tx(BAR(CF::BAR_FULL + slot), CF::Q_TILE + CF::DO_TILE);
+      const uint32_t sl = sbase + CF::B_K_OFF + slot * CF::Q_TILE;
+      mbar_arrive_expect_tx(BAR(CF::BAR_FULL + slot), CF::Q_TILE);
       for (int kc = 0; kc < D / SW_CHUNK; ++kc)
-        tma_load_3d(sl + kc * SW_CHUNK_BYTES, &tmK, kc * SW_CHUNK, j * BN, bh, BAR(CF::BAR_FULL + slot));
-      for (int kc = 0; kc < DV / SW_CHUNK; ++kc)
-        tma_load_3d(sl + CF::Q_TILE + kc * SW_CHUNK_BYTES, &tmV, kc * SW_CHUNK, j * BN, bh,
-                    BAR(CF::BAR_FULL + slot));
+        tma_load_3d(sl + kc * SW_CHUNK_BYTES, &tmK, kc * SW_CHUNK, it * BN, bh, BAR(CF::BAR_FULL + slot));
       ++issued;
     }
     if (n_it > 0) wd.wait1(BAR(CF::BAR_FIXED), 0, ROLE_DRAIN, CF::BAR_FIXED, true);
     for (int s = 0; s < CF::B_KS && s < issued; ++s) {
       const int lastpos = s + ((issued - 1 - s) / CF::B_KS) * CF::B_KS;
       wd.wait1(BAR(CF::BAR_FULL + s), (lastpos / CF::B_KS) & 1, ROLE_DRAIN, CF::BAR_FULL + s, true);
+    }
+  } else if (warp == CF::LOAD_WARP + 1 && lane == 0) {
+    // ============================================================ TMA producer: V
+    if (n_it > 0) tma_prefetch_desc(&tmV);
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int slot = it % CF::B_VS;
+      if (!wd.wait1(BAR(CF::BAR_VEMPTY + slot), ((it / CF::B_VS) & 1) ^ 1, ROLE_LOAD,
+                    CF::BAR_VEMPTY + slot, false))
+        break;
+      const uint32_t sl = sbase + CF::B_V_OFF + slot * CF::DO_TILE;
+      mbar_arrive_expect_tx(BAR(CF::BAR_VFULL + slot), CF::DO_TILE);
+      for (int kc = 0; kc < DV / SW_CHUNK; ++kc)
+        tma_load_3d(sl + kc * SW_CHUNK_BYTES, &tmV, kc * SW_CHUNK, it * BN, bh, BAR(CF::BAR_VFULL + slot));
+      ++issued;
+    }
+    for (int s = 0; s < CF::B_VS && s < issued; ++s) {
+      const int lastpos = s + ((issued - 1 - s) / CF::B_VS) * CF::B_VS;
+      wd.wait1(BAR(CF::BAR_VFULL + s), (lastpos / CF::B_VS) & 1, ROLE_DRAIN, CF::BAR_VFULL + s, true);
     }
   }
   __syncwarp();
