@@ -277,6 +277,14 @@ int check_pointers(const Problem &a) {
   return ATTN_OK;
 }
 
+// Heads per scheduling group: as many as keep their K and V (bf16) within about 48 MB, a
+// good part of the 126 MB L2 (see unit_of_block in the kernels).
+int head_group(int BH, int Nk, int d, int d_v) {
+  const double per_head = static_cast<double>(Nk) * (d + d_v) * 2.0;
+  const double g = 48.0 * 1024 * 1024 / (per_head > 1.0 ? per_head : 1.0);
+  return g >= BH ? BH : (g < 1.0 ? 1 : static_cast<int>(g));
+}
+
 // Launches the attention kernel. With n_splits > 1 each CTA covers `split_tiles` K/V
 // tiles of its head and writes fp32 partials to O_dst / LSE_dst instead of O / LSE.
 int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int split_tiles,
@@ -307,6 +315,7 @@ int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int s
   la.p.ctas_per_head = a.ctas_per_head();
   la.p.n_splits = n_splits;
   la.p.split_tiles = split_tiles;
+  la.p.head_group = head_group(a.BH, a.Nk, a.d, a.d_v);
   la.p.scale_log2 = a.scale * LOG2E;
   la.p.out_f32 = out_f32;
   la.p.O = O_dst;
@@ -334,6 +343,7 @@ int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int s
 }
 
 constexpr int kMaxSplits = 1024;
+
 
 // Number of key ranges for a split launch and the K/V tiles of each. A request of
 // n_splits ranges is rounded to whole tiles: split_tiles = ceil(nkv / n_splits), and
@@ -605,6 +615,7 @@ extern "C" int attn_bwd(const void *Q, const void *K, const void *V, const void 
   pp.nkv_tiles = (Nk + BN - 1) / BN;
   pp.causal_off = Nk - Nq;
   pp.nqp = nq_tiles * BM;
+  pp.head_group = head_group(BH, Nq + Nk, d, d_v);
   pp.scale_log2 = scale * LOG2E;
   pp.scale = scale;
   float *Lp = static_cast<float *>(workspace);

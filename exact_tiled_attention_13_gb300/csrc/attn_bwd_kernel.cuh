@@ -44,6 +44,7 @@ struct BwdParams {
   int nq_tiles, nkv_tiles;
   int causal_off;     // Nk - Nq: query i may see keys j <= i + causal_off
   int nqp;            // nq_tiles * 128: row stride of Lp and D
+  int head_group;     // heads per scheduling group (unit_of_block)
   float scale_log2;   // scale * log2(e)
   float scale;
   const float *Lp;    // [BH][nqp] LSE * log2(e), +inf where p must be 0
@@ -253,8 +254,9 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 
   // This CTA: head bh, key tile j; the query tiles that see it are i_lo .. nq_tiles - 1,
   // each in two halves of 64 queries (units u = 0 .. 2 n_it - 1).
-  const int bh = blockIdx.x / p.nkv_tiles;
-  const int j = static_cast<int>(blockIdx.x % p.nkv_tiles);
+  // Units of a head: key tiles from the first (seen by the most queries) on.
+  int bh, j;
+  unit_of_block(blockIdx.x, p.BH, p.nkv_tiles, p.head_group, &bh, &j);
   int i_lo = 0;
   if (CAUSAL) {
     // The first query that sees key 128 j is q0 = 128 j - (Nk - Nq); none when q0 >= Nq.
@@ -522,8 +524,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   const int B_DSFULL = CF::BAR_PFULL;  // [2]
 
   // This CTA: head bh, query tile i; it visits key tiles 0 .. hi (none when hi < 0).
-  const int bh = blockIdx.x / p.nq_tiles;
-  const int i = static_cast<int>(blockIdx.x % p.nq_tiles);
+  // Units of a head: query tiles from the last (sees the most keys) down.
+  int bh, ri;
+  unit_of_block(blockIdx.x, p.BH, p.nq_tiles, p.head_group, &bh, &ri);
+  const int i = p.nq_tiles - 1 - ri;
   int hi = p.nkv_tiles - 1;
   if (CAUSAL) hi = cmin(floor_div(cmin(i * BM + BM - 1, p.Nq - 1) + p.causal_off, BN), hi);
   const int n_it = hi + 1 > 0 ? hi + 1 : 0;

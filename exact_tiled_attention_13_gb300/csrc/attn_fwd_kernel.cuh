@@ -85,6 +85,7 @@ struct KernelParams {
   int ctas_per_head;  // ceil(nq_tiles / NQ)
   int n_splits;       // key ranges per head (1: the whole key sequence)
   int split_tiles;    // K/V tiles per key range
+  int head_group;     // heads per scheduling group (see unit_of_block)
   float scale_log2;   // scale * log2(e)
   int out_f32;        // O element type: 1 fp32, 0 bf16
   void *O;    // with n_splits > 1: fp32 partial outputs [n_splits][BH][Nq][d_v]
@@ -242,6 +243,22 @@ struct WatchdogT {
 
 using Watchdog = WatchdogT<KernelParams>;
 
+// Grid order. Each head has U work units, unit r = 0 holding the most work (for a causal
+// mask, the query tiles that see the most keys). Heads are taken in groups of G whose
+// K/V fit in L2 together; within a group the blocks go by unit rank first and head
+// second, so every head's largest unit starts before any head's smaller ones (longest
+// first) and the blocks that share a head's K/V still run close in time. Block b maps
+// to head *bh and rank *r.
+__device__ __forceinline__ void unit_of_block(unsigned b, int BH, int U, int G, int *bh, int *r) {
+  const unsigned per_group = static_cast<unsigned>(G) * static_cast<unsigned>(U);
+  const int gi = static_cast<int>(b / per_group);
+  const int g0 = gi * G;
+  const int gl = BH - g0 < G ? BH - g0 : G;
+  const int rem = static_cast<int>(b - static_cast<unsigned>(gi) * per_group);
+  *r = rem / gl;
+  *bh = g0 + rem % gl;
+}
+
 // Per-CTA schedule: which query tiles it owns and which K/V tiles each one visits.
 // Iteration `it` visits K/V tile j = hi_max - it; query tile q takes part in
 // iterations [first_it(q), n_it), i.e. K/V tiles hi(q) down to 0. With a causal mask
@@ -256,13 +273,10 @@ struct Schedule {
   int first0, first1;  // first_it of query tiles 0 and 1
 
   __device__ Schedule(const KernelParams &p) {
-    // Grid order: head, then key range, then query tiles, so the CTAs that share a
-    // head's K/V tiles run side by side.
-    const int per_head = p.ctas_per_head * p.n_splits;
-    bh = blockIdx.x / per_head;
-    const int r = static_cast<int>(blockIdx.x % per_head);
+    // A head's units: key range, then query tiles from the last (most causal work) down.
+    int r;
+    unit_of_block(blockIdx.x, p.BH, p.ctas_per_head * p.n_splits, p.head_group, &bh, &r);
     const int split = r / p.ctas_per_head;
-    // Within a head, the CTA with the most causal work starts first.
     cta_q = p.ctas_per_head - 1 - r % p.ctas_per_head;
     n_exist = cmin(NQ, p.nq_tiles - cta_q * NQ);
     const int lo = split * p.split_tiles;  // this CTA's K/V tiles: lo .. top
@@ -576,8 +590,9 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         const bool row_ok = q_row < p.Nq;
         const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;  // no allowed key: O = 0
         // Key range `split` of a split launch writes its own slice of the partials.
-        const int split = static_cast<int>(blockIdx.x % (p.ctas_per_head * p.n_splits)) /
-                          p.ctas_per_head;
+        int ubh, ur;
+        unit_of_block(blockIdx.x, p.BH, p.ctas_per_head * p.n_splits, p.head_group, &ubh, &ur);
+        const int split = ur / p.ctas_per_head;
         const size_t lrow = (static_cast<size_t>(split) * p.BH + sch.bh) * p.Nq + (row_ok ? q_row : 0);
         const size_t orow = lrow * DV;
 #pragma unroll
