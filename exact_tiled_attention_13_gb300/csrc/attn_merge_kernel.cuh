@@ -38,7 +38,10 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS_PER_BLOCK)
   if (row >= rows) return;
   const int lane = threadIdx.x % 32;
 
+  // The ranges' loads are independent: batches of 8 are issued before any is used, so
+  // the kernel is not a chain of memory round trips.
   float M = -INFINITY;
+#pragma unroll 8
   for (int s = 0; s < n_splits; ++s) M = fmaxf(M, __ldg(L_part + s * rows + row));
 
   float acc[W];
@@ -46,22 +49,30 @@ __global__ void __launch_bounds__(32 * MERGE_ROWS_PER_BLOCK)
   for (int c = 0; c < W; ++c) acc[c] = 0.0f;
   float wsum = 0.0f;
   if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const float L = __ldg(L_part + s * rows + row);
-      const float w = expf(L - M);  // 0 for an empty range (L = -inf)
-      const float *src = O_part + (s * rows + row) * DV + lane * W;
-      if constexpr (W == 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
-      } else {
-        const float2 v = __ldg(reinterpret_cast<const float2 *>(src));
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
+    constexpr int B = 8;
+    for (int s0 = 0; s0 < n_splits; s0 += B) {
+      float w[B], v[B][W];
+#pragma unroll
+      for (int k = 0; k < B; ++k) {
+        const int s = s0 + k < n_splits ? s0 + k : n_splits - 1;  // clamped: weight 0 below
+        w[k] = __ldg(L_part + s * rows + row);
+        const float *src = O_part + (s * rows + row) * DV + lane * W;
+        if constexpr (W == 4) {
+          const float4 t = __ldg(reinterpret_cast<const float4 *>(src));
+          v[k][0] = t.x, v[k][1] = t.y, v[k][2] = t.z, v[k][3] = t.w;
+        } else {
+          const float2 t = __ldg(reinterpret_cast<const float2 *>(src));
+          v[k][0] = t.x, v[k][1] = t.y;
+        }
       }
-      wsum += w;
+      // In increasing range order, as the sums are defined.
+#pragma unroll
+      for (int k = 0; k < B; ++k) {
+        const float wk = s0 + k < n_splits ? expf(w[k] - M) : 0.0f;  // 0 for an empty range
+#pragma unroll
+        for (int c = 0; c < W; ++c) acc[c] = fmaf(wk, v[k][c], acc[c]);
+        wsum += wk;
+      }
     }
   }
   const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
