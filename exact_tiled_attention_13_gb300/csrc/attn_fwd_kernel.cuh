@@ -13,10 +13,9 @@
 // dense bias, whose time is the bias bytes). Warp roles (12 or 8 warps):
 //   softmax warpgroup q (warps 4q..4q+3): thread = query row = tensor-memory lane.
 //     Reads its row of S from tensor memory, masks, takes the tile max b_t, the new
-//     running max m_t and alpha_t, writes P as bf16 back over S, rescales its row of o
-//     by alpha_t in tensor memory between the quarters of the exponential loop (skipped
-//     when every alpha of the warp is 1), accumulates l_t, and at the end writes
-//     O = o/l and LSE.
+//     exponent reference and alpha_t, writes P as bf16 back over S, rescales its row of o
+//     in tensor memory when the reference moves (rarely: see RESCALE_TAU), accumulates
+//     l_t, and at the end writes O = o/l and LSE.
 //   control warpgroup, one thread per copy role:
 //     MMA (whole warp, one elected lane issues): S_q = Q_q K_t^T (A and B from shared
 //       memory) and o_q += P_q V_t (A = P from tensor memory, B = V from shared memory)
@@ -75,6 +74,8 @@ constexpr int SW_CHUNK = 64;                 // bf16 columns per 128-byte swizzl
 constexpr int SW_CHUNK_BYTES = 128 * 128;    // one 128-row x 128-byte box
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
+// Softmax reference moves only for a tile max this far above it (log2 units): p <= 256.
+constexpr float RESCALE_TAU = 8.0f;
 
 struct KernelParams {
   int BH;
@@ -397,7 +398,8 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     const bool has_keys = sch.first_it(q) < sch.n_it;  // some K/V tile is visible to this tile
     const float sl2 = p.scale_log2;
     float m2 = -INFINITY;  // running max m_t, in log2(e)-scaled units
-    float l = 0.0f;        // running sum l_t
+    float l = 0.0f;        // running sum l_t of the fp32 p (for LSE)
+    float lr = 0.0f;       // l_t with each tile's largest p as rounded to bf16 (for O)
     uint32_t s_phase = 0;
     bool ok = true;
     int cpos = 0;  // dense-bias ring position
@@ -509,21 +511,37 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
             if (c > lim_j) x[c] = -INFINITY;
         }
 
-        // b_t and m_t = max(m_{t-1}, b_t); alpha_t = exp(m_{t-1} - m_t).
+        // b_t, then the exponent reference m_t. The recurrence's m_t = max(m_{t-1}, b_t)
+        // may be replaced by any reference that is used consistently for p, l and o: the
+        // final o_T / l_T is the same function. The reference moves to b_t only when b_t
+        // exceeds it by more than RESCALE_TAU (log2 units), so p <= 2^RESCALE_TAU stays
+        // far inside bf16 and fp32 range, and o needs rescaling (alpha_t != 1) only then.
         const float b = row_max128(x);
-        const float m_new = CF::BIASED ? fmaxf(m2, b) : fmaxf(m2, b * sl2);
-        // No allowed key seen yet: every p is 0 and alpha is irrelevant; use 0 as reference.
+        const float bs = CF::BIASED ? b : b * sl2;  // b_t in log2 units
+        const bool move = bs > m2 + RESCALE_TAU;    // also the first allowed key (m2 = -inf)
+        const float m_new = move ? bs : m2;
+        // No allowed key seen yet: every p is 0; use 0 as reference.
         const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-        const float alpha = (m_new == m2) ? 1.0f : ex2_approx(m2 - m_use);
-        // o_t = alpha_t o_{t-1}. The previous P V has completed (the S tile just read was
-        // committed after it). The 32-column chunks of o are loaded, scaled and stored
-        // between the quarters of the exponential loop, in the shadow of the exponential
-        // unit. It runs on every tile: multiplying by alpha = 1 is exact, and costs less
-        // than a branch in the unrolled loop; on a query tile's first K/V tile o holds no
-        // result yet and is overwritten by the first P V, which does not accumulate.
-        constexpr int OCH = DV / 32;  // chunks of o
-        uint32_t o[32];
-        tmem_ld32(t_o, o);
+        const float alpha = move ? ex2_approx(m2 - m_use) : 1.0f;
+        if (__any_sync(0xFFFFFFFFu, move) && it > sch.first_it(q)) {
+          // o_t = alpha_t o_{t-1}: the previous P V has completed (the S tile just read was
+          // committed after it). Rare once a row has seen its largest scores. On a query
+          // tile's first K/V tile o holds no result yet (the first P V overwrites it).
+#pragma unroll
+          for (int cc = 0; cc < DV / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(t_o + 32 * cc, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float f0, f1;
+              mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), alpha, alpha);
+              o[c] = __float_as_uint(f0);
+              o[c + 1] = __float_as_uint(f1);
+            }
+            tmem_st32(t_o + 32 * cc, o);
+          }
+        }
 
         // p_ij = exp(S_ij - m_t) as bf16 into tensor memory over S, 32 keys at a time;
         // the row sum runs alongside in four independent packed chains.
@@ -550,18 +568,6 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
             pk[16 * (qq & 1) + c2] = pack_bf16(p0, p1);
           }
           if (qq & 1) tmem_st32(t_s + 32 * (qq / 2), pk);
-          if (qq < OCH) {
-            tmem_wait_ld(o);
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              float f0, f1;
-              mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), alpha, alpha);
-              o[c] = __float_as_uint(f0);
-              o[c + 1] = __float_as_uint(f1);
-            }
-            tmem_st32(t_o + 32 * qq, o);
-            if (qq + 1 < OCH) tmem_ld32(t_o + 32 * (qq + 1), o);
-          }
         }
         tmem_wait_st();
         tc_fence_before();
@@ -569,11 +575,25 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         mbar_arrive_elect(BAR(CF::B_PFULL + q));
         ETA_TRACE(4);
 
-        // l_t = alpha_t l_{t-1} + sum_j p_ij (l sums the fp32 p, before bf16 rounding).
+        // l_t = alpha_t l_{t-1} + sum_j p_ij.
         add2(s[0], s[1], s[0], s[1], s[2], s[3]);
         add2(s[4], s[5], s[4], s[5], s[6], s[7]);
         add2(s[0], s[1], s[0], s[1], s[4], s[5]);
-        l = fmaf(alpha, l, s[0] + s[1]);
+        // The tile's largest p, computed as in the loop, and its bf16 rounding: under a
+        // stale reference it need not be exactly 1, so the denominator of O takes it as
+        // rounded, like the P that multiplies V (a row dominated by one key then gets
+        // that key's v to fp32 accuracy). The other p round as they would with the
+        // eager reference; LSE keeps the fp32 sum.
+        float pmax;
+        if constexpr (CF::BIASED) {
+          pmax = ex2_approx(b + neg_m);
+        } else {
+          pmax = ex2_approx(fmaf(b, sl2, neg_m));
+        }
+        const float pmax_r = __uint_as_float(pack_bf16(pmax, pmax) << 16);
+        const float tile_sum = s[0] + s[1];
+        l = fmaf(alpha, l, tile_sum);
+        lr = fmaf(alpha, lr, tile_sum + (pmax_r - pmax));
         ETA_TRACE(5);
         m2 = m_new;
       }
@@ -588,7 +608,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       if (ok) {
         if (has_keys) tc_fence_after();
         const bool row_ok = q_row < p.Nq;
-        const float inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;  // no allowed key: O = 0
+        const float inv_l = (lr > 0.0f) ? 1.0f / lr : 0.0f;  // no allowed key: O = 0
         // Key range `split` of a split launch writes its own slice of the partials.
         int ubh, ur;
         unit_of_block(blockIdx.x, p.BH, p.ctas_per_head * p.n_splits, p.head_group, &ubh, &ur);

@@ -18,8 +18,12 @@
  *
  * Numeric contract of this implementation: Q K^T and P V run on the tensor cores with
  * bf16 operands and fp32 accumulation; scores, the running max and sum, and O are fp32;
- * P is rounded to bf16 before it multiplies V, while l_i sums the unrounded fp32 p.
- * LSE_i = m_i + ln l_i (natural log, in the units of S, bias included).
+ * P is rounded to bf16 before it multiplies V; LSE_i = m_i + ln l_i (natural log, in the
+ * units of S, bias included) uses the sum of the unrounded fp32 p, and O_i = o_i / l_i
+ * uses that sum with each tile's largest p taken as rounded. The exponent reference
+ * m_t of the recurrence is moved only when a tile's maximum exceeds it by more than a
+ * factor 2^8 (any reference used consistently gives the same o_T / l_T), so o is
+ * rescaled only then.
  *
  * All entry points are plain C, take device pointers and sizes, and never allocate
  * device memory. They are thread-safe: calls from several host threads or on several
