@@ -61,43 +61,51 @@ struct BwdParams {
 using BwdWatchdog = WatchdogT<BwdParams>;
 
 // ------------------------------------------------------------------------ prep
-// O: [rows][DV] bf16 (out_f32 = 0) or fp32; dO: [rows][DV] bf16; LSE: [rows].
+// O: [rows][DV] bf16 (out_f32 = 0) or fp32; dO: [rows][DV] bf16; LSE: [rows]. DV / 8 lanes
+// (16 for d_v = 128, 8 for 64) share a row, each with one 16-byte load of dO (8 bf16)
+// and of O (16 or 32 bytes).
 template <int DV>
 __global__ void __launch_bounds__(256)
     attn_bwd_prep_kernel(const void *__restrict__ O, int out_f32, const uint16_t *__restrict__ dO,
                          const float *__restrict__ LSE, int BH, int Nq, int nqp, float *Lp,
                          float *Dd) {
-  constexpr int W = DV / 32;
-  const long long prow = static_cast<long long>(blockIdx.x) * 8 + threadIdx.x / 32;
-  if (prow >= static_cast<long long>(BH) * nqp) return;
-  const int lane = threadIdx.x % 32;
-  const int bh = static_cast<int>(prow / nqp);
-  const int i = static_cast<int>(prow % nqp);
+  constexpr int LPR = DV / 8;  // lanes per row
+  const long long prow = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / LPR;
+  const int sub = threadIdx.x % LPR;
+  const bool in = prow < static_cast<long long>(BH) * nqp;
+  const int bh = in ? static_cast<int>(prow / nqp) : 0;
+  const int i = in ? static_cast<int>(prow % nqp) : Nq;
   float acc = 0.0f;
   float lp = INFINITY;
   if (i < Nq) {
     const long long row = static_cast<long long>(bh) * Nq + i;
-    const uint16_t *g = dO + row * DV + lane * W;
-    float o[W], gv[W];
-#pragma unroll
-    for (int c = 0; c < W; ++c) gv[c] = __uint_as_float(static_cast<uint32_t>(g[c]) << 16);
+    const uint4 g = __ldg(reinterpret_cast<const uint4 *>(dO + row * DV) + sub);
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    float o[8];
     if (out_f32) {
-      const float *src = static_cast<const float *>(O) + row * DV + lane * W;
-#pragma unroll
-      for (int c = 0; c < W; ++c) o[c] = src[c];
+      const float4 *src = reinterpret_cast<const float4 *>(static_cast<const float *>(O) + row * DV) + 2 * sub;
+      const float4 a = __ldg(src), b = __ldg(src + 1);
+      o[0] = a.x, o[1] = a.y, o[2] = a.z, o[3] = a.w, o[4] = b.x, o[5] = b.y, o[6] = b.z, o[7] = b.w;
     } else {
-      const uint16_t *src = static_cast<const uint16_t *>(O) + row * DV + lane * W;
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(O) + row * DV) + sub);
+      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int c = 0; c < W; ++c) o[c] = __uint_as_float(static_cast<uint32_t>(src[c]) << 16);
+      for (int k = 0; k < 4; ++k) {
+        o[2 * k] = __uint_as_float(vw[k] << 16);
+        o[2 * k + 1] = __uint_as_float(vw[k] & 0xFFFF0000u);
+      }
     }
 #pragma unroll
-    for (int c = 0; c < W; ++c) acc = fmaf(gv[c], o[c], acc);
+    for (int k = 0; k < 4; ++k) {
+      acc = fmaf(__uint_as_float(gw[k] << 16), o[2 * k], acc);
+      acc = fmaf(__uint_as_float(gw[k] & 0xFFFF0000u), o[2 * k + 1], acc);
+    }
     const float lse = LSE[row];
     lp = lse == -INFINITY ? INFINITY : lse * LOG2E;
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
-  if (lane == 0) {
+  for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+  if (in && sub == 0) {
     Lp[prow] = lp;
     Dd[prow] = i < Nq ? acc : 0.0f;
   }
@@ -792,7 +800,7 @@ template <int DV>
 cudaError_t launch_bwd_prep(const void *O, int out_f32, const uint16_t *dO, const float *LSE,
                             int BH, int Nq, int nqp, float *Lp, float *Dd, cudaStream_t stream) {
   const long long rows = static_cast<long long>(BH) * nqp;
-  const long long blocks = (rows + 7) / 8;
+  const long long blocks = (rows * (DV / 8) + 255) / 256;
   attn_bwd_prep_kernel<DV><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(O, out_f32, dO, LSE, BH,
                                                                              Nq, nqp, Lp, Dd);
   return cudaGetLastError();
