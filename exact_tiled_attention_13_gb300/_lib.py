@@ -24,6 +24,7 @@ ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_CUDA = -7
 ATTN_ERR_SCRATCH_LIMIT = -8
 ATTN_STATIC_SCRATCH_BYTES = 33554432
+ATTN_ABI_VERSION = 104
 
 ATTN_FAULT_NONE = 0
 ATTN_FAULT_SKIP_FIRST_K = 1

@@ -180,7 +180,7 @@ cudaError_t dispatch_bwd(bool causal, int bias, const BwdLaunchArgs &a) {
 
 using namespace eta;
 
-extern "C" int attn_version(void) { return 100; }
+extern "C" int attn_version(void) { return ATTN_ABI_VERSION; }
 
 extern "C" const char *attn_strerror(int code) {
   switch (code) {

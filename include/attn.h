@@ -261,7 +261,10 @@ ATTN_API unsigned long long attn_set_wait_timeout_ns(unsigned long long ns);
 #define ATTN_FAULT_SKIP_FIRST_K 1
 ATTN_API int attn_set_fault_injection(int fault);
 
-/* ABI version of this header (major * 100 + minor). */
+/* ABI version of this header (major * 100 + minor): 1.00 attn_fwd; 1.01 attn_fwd_ex;
+ * 1.02 attn_fwd_splitkv, attn_fwd_splitkv_plan; 1.03 attn_fwd_splitkv_static;
+ * 1.04 attn_bwd, attn_bwd_workspace_bytes. attn_version() returns the library's. */
+#define ATTN_ABI_VERSION 104
 ATTN_API int attn_version(void);
 
 #ifdef __cplusplus

@@ -63,7 +63,7 @@ def test_strerror_and_version():
     for code in range(-7, 1):
         assert eta.attn_strerror(code)
     assert "unknown" in eta.attn_strerror(-99)
-    assert eta.attn_version() == 100
+    assert eta.attn_version() == _lib.ATTN_ABI_VERSION == 104
 
 
 def test_timeout_setting_roundtrip():
