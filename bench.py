@@ -392,7 +392,8 @@ def run_ours(args):
         raise SystemExit(f"watchdog tripped in the timed region: {word:#x}")
 
     region_ms = region_start.elapsed_time(region_end)
-    kernel_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
+    per_step = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
+    kernel_ms = float(np.mean(per_step))
     step_ms = reduce_max(dist, kernel_ms if flush is not None else region_ms / K, device)
     value = world * F / (step_ms * 1e-3) / 1e12
 
@@ -445,6 +446,9 @@ def run_ours(args):
                         "h2d_bytes_per_step": wl.h2d_bytes(), "d2h_bytes_per_step": wl.d2h_bytes(),
                         "ms_per_step": e2e_ms, "steps": E},
                 "gpu_launches": K * wl.launches_per_step, "clocks": clock_info,
+                "step_ms_percentiles": {"p10": float(np.percentile(per_step, 10)),
+                                        "p50": float(np.percentile(per_step, 50)),
+                                        "p90": float(np.percentile(per_step, 90))},
                 "library": os.path.relpath(eta.library_path(), ROOT)}
     barrier(dist, device)
     if line is not None:
