@@ -25,82 +25,67 @@
 
 namespace eta {
 
-constexpr int MERGE_ROWS_PER_BLOCK = 8;  // one warp per query row
-
+// One thread per output element: a block of d_v threads per query row, so that every
+// (range, element) load of the whole grid can be in flight at once (the work is a few
+// loads per thread; it is bound by memory latency, not by bandwidth or arithmetic).
 // O_part: [S][rows][DV] fp32; L_part: [S][rows] fp32; O: [rows][DV] (fp32 or bf16);
 // LSE: [rows] or null.
 template <int DV>
-__global__ void __launch_bounds__(32 * MERGE_ROWS_PER_BLOCK)
+__global__ void __launch_bounds__(DV)
     attn_merge_kernel(const float *__restrict__ O_part, const float *__restrict__ L_part,
                       int n_splits, long long rows, void *O, int out_f32, float *LSE) {
-  constexpr int W = DV / 32;  // columns per lane: 4 (d_v = 128) or 2 (d_v = 64)
-  const long long row = static_cast<long long>(blockIdx.x) * MERGE_ROWS_PER_BLOCK + threadIdx.x / 32;
-  if (row >= rows) return;
-  const int lane = threadIdx.x % 32;
+  const long long row = blockIdx.x;
+  const int col = threadIdx.x;
 
-  // The ranges' loads are independent: batches of 8 are issued before any is used, so
-  // the kernel is not a chain of memory round trips.
+  // The ranges' loads are independent and issued in batches of 32, so for up to 32
+  // ranges each pass is one memory round trip (the partials usually come from DRAM).
+  constexpr int B = 32;
   float M = -INFINITY;
-#pragma unroll 8
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, __ldg(L_part + s * rows + row));
-
-  float acc[W];
+  for (int s0 = 0; s0 < n_splits; s0 += B) {
+    float w[B];
 #pragma unroll
-  for (int c = 0; c < W; ++c) acc[c] = 0.0f;
-  float wsum = 0.0f;
+    for (int k = 0; k < B; ++k) w[k] = __ldg(L_part + (s0 + k < n_splits ? s0 + k : s0) * rows + row);
+#pragma unroll
+    for (int k = 0; k < B; ++k) M = fmaxf(M, w[k]);  // the clamped repeats change nothing
+  }
+
+  float acc = 0.0f, wsum = 0.0f;
   if (M != -INFINITY) {
-    constexpr int B = 8;
     for (int s0 = 0; s0 < n_splits; s0 += B) {
-      float w[B], v[B][W];
+      float w[B], v[B];
 #pragma unroll
       for (int k = 0; k < B; ++k) {
         const int s = s0 + k < n_splits ? s0 + k : n_splits - 1;  // clamped: weight 0 below
         w[k] = __ldg(L_part + s * rows + row);
-        const float *src = O_part + (s * rows + row) * DV + lane * W;
-        if constexpr (W == 4) {
-          const float4 t = __ldg(reinterpret_cast<const float4 *>(src));
-          v[k][0] = t.x, v[k][1] = t.y, v[k][2] = t.z, v[k][3] = t.w;
-        } else {
-          const float2 t = __ldg(reinterpret_cast<const float2 *>(src));
-          v[k][0] = t.x, v[k][1] = t.y;
-        }
+        v[k] = __ldg(O_part + (s * rows + row) * DV + col);
       }
       // In increasing range order, as the sums are defined.
 #pragma unroll
       for (int k = 0; k < B; ++k) {
         const float wk = s0 + k < n_splits ? expf(w[k] - M) : 0.0f;  // 0 for an empty range
-#pragma unroll
-        for (int c = 0; c < W; ++c) acc[c] = fmaf(wk, v[k][c], acc[c]);
+        acc = fmaf(wk, v[k], acc);
         wsum += wk;
       }
     }
   }
-  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-#pragma unroll
-  for (int c = 0; c < W; ++c) acc[c] *= inv;
-
+  const float r = wsum > 0.0f ? acc * (1.0f / wsum) : 0.0f;
   if (out_f32) {
-    float *dst = static_cast<float *>(O) + row * DV + lane * W;
-    if constexpr (W == 4)
-      *reinterpret_cast<float4 *>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    else
-      *reinterpret_cast<float2 *>(dst) = make_float2(acc[0], acc[1]);
+    static_cast<float *>(O)[row * DV + col] = r;
   } else {
-    uint16_t *dst = static_cast<uint16_t *>(O) + row * DV + lane * W;
-    if constexpr (W == 4)
-      *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]));
-    else
-      *reinterpret_cast<uint32_t *>(dst) = pack_bf16(acc[0], acc[1]);
+    // Pairs of neighbouring columns are packed by the even thread of each pair.
+    const float hi = __shfl_down_sync(0xFFFFFFFFu, r, 1);
+    if ((col & 1) == 0)
+      *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(O) + row * DV + col) = pack_bf16(r, hi);
   }
-  if (LSE != nullptr && lane == 0) LSE[row] = wsum > 0.0f ? M + logf(wsum) : -INFINITY;
+  if (LSE != nullptr && col == 0) LSE[row] = wsum > 0.0f ? M + logf(wsum) : -INFINITY;
 }
 
 template <int DV>
 cudaError_t launch_merge(const float *O_part, const float *L_part, int n_splits, long long rows,
                          void *O, int out_f32, float *LSE, cudaStream_t stream) {
-  const long long blocks = (rows + MERGE_ROWS_PER_BLOCK - 1) / MERGE_ROWS_PER_BLOCK;
-  attn_merge_kernel<DV><<<static_cast<unsigned>(blocks), 32 * MERGE_ROWS_PER_BLOCK, 0, stream>>>(
-      O_part, L_part, n_splits, rows, O, out_f32, LSE);
+  if (rows > 0x7FFFFFFFll) return cudaErrorInvalidValue;  // one block per row
+  attn_merge_kernel<DV><<<static_cast<unsigned>(rows), DV, 0, stream>>>(O_part, L_part, n_splits,
+                                                                         rows, O, out_f32, LSE);
   return cudaGetLastError();
 }
 
