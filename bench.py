@@ -49,8 +49,15 @@ L2_BYTES = 129 * 1000 * 1000
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 # Kernel sources behind each kind of step (a recorded ncu traffic figure is used only
 # while these files still hash to the value it was taken on).
-KERNEL_SOURCES_FWD = ["attn_fwd_kernel.cuh", "attn_merge_kernel.cuh", "ptx.cuh"]
-KERNEL_SOURCES_BWD = ["attn_bwd_kernel.cuh", "attn_fwd_kernel.cuh", "ptx.cuh"]
+KERNEL_SOURCES = {
+    "forward": ["attn_fwd_kernel.cuh", "ptx.cuh"],
+    "split": ["attn_fwd_kernel.cuh", "attn_merge_kernel.cuh", "ptx.cuh"],
+    "backward": ["attn_bwd_kernel.cuh", "attn_fwd_kernel.cuh", "ptx.cuh"],
+}
+
+
+def step_kind(w) -> str:
+    return "backward" if w.backward else ("split" if w.split_kv else "forward")
 
 
 def parse_args(argv=None):
@@ -187,9 +194,9 @@ def measured_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_sha(backward: bool = False) -> str:
+def kernel_source_sha(kind: str = "forward") -> str:
     h = hashlib.sha256()
-    for name in (KERNEL_SOURCES_BWD if backward else KERNEL_SOURCES_FWD):
+    for name in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, "exact_tiled_attention_13_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -202,7 +209,7 @@ def recorded_traffic(workload_id: int):
     try:
         with open(path) as f:
             kv = dict(line.split(":", 1) for line in f if ":" in line and not line.startswith("#"))
-        if kv.get("kernel_source_sha", "").strip() != kernel_source_sha(w.backward):
+        if kv.get("kernel_source_sha", "").strip() != kernel_source_sha(step_kind(w)):
             return None
         return float(kv["dram_bytes_per_launch"])
     except (OSError, ValueError, KeyError):
