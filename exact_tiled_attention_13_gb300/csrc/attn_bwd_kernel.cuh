@@ -120,6 +120,7 @@ enum { BWD_BIAS_NONE = 0, BWD_BIAS_DENSE = 1, BWD_BIAS_KEY = 2 };
 // elementwise warps work on one half while the tensor cores compute the next half's
 // products: MMA order S/dP(u+1), then the accumulating products of u.
 constexpr int HALF = 64;
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 template <int D, int DV, bool CAUSAL, int BIAS>
 struct BwdCfg {
@@ -147,6 +148,11 @@ struct BwdCfg {
   static constexpr int B_V_OFF = B_K_OFF + B_KS * Q_TILE;
   static constexpr int B_BAR_OFF = B_V_OFF + B_VS * DO_TILE;
   static_assert(A_QS >= 2 && B_KS >= 2 && B_VS >= 2, "need two ring slots");
+  // Epilogue stages (8 warps x 32 rows x (width / 2 + 4) floats) reuse the rings.
+  static_assert(8 * 32 * ((D > DV ? D : DV) / 2 + 4) * 4 <= A_QS * A_SLOT,
+                "dK/dV epilogue stage larger than the Q/dO ring it reuses");
+  static_assert(8 * 32 * (D / 2 + 4) * 4 <= B_KS * Q_TILE,
+                "dQ epilogue stage larger than the K ring it reuses");
   static_assert(A_SLOT % 1024 == 0, "slots keep 1024-byte alignment");
 
   // barriers (the same layout serves both kernels; RING = ring slots; dq's K ring uses
@@ -218,22 +224,40 @@ __device__ __forceinline__ void ld_pair(uint32_t ta, uint32_t tb, uint32_t (&a)[
   tmem_wait_ld(b);
 }
 
-// Writes a 128 x W fp32 accumulator row (this thread's lane) from tensor memory to
-// global memory, columns [c0, c0 + n) in 32-column chunks, times `mul`.
-__device__ __forceinline__ void store_acc_row(uint32_t tcol, int c0, int n, float mul, float *dst,
-                                              bool row_ok) {
-  for (int cc = c0; cc < c0 + n; cc += 32) {
-    uint32_t r[32];
-    tmem_ld32(tcol + cc, r);
-    tmem_wait_ld(r);
-    if (row_ok) {
-      float4 *d4 = reinterpret_cast<float4 *>(dst + cc);
+// Writes accumulator columns [c0, c0 + N) of this warp's 32 rows (its tensor-memory lanes),
+// times `mul`, to global memory through a per-warp shared-memory stage of 32 rows x (N + 4)
+// floats (the padding puts the rows of a column in different banks). A thread owns a row
+// in tensor memory; from the stage, N / 4 lanes write each row, so every store instruction
+// writes whole rows instead of one 16-byte piece per row. `grow0` is the global address of
+// the warp's first row (column 0), `rows_ok` how many of its rows exist.
+template <int N>
+__device__ __forceinline__ void store_acc_staged(uint32_t tcol, int c0, float mul, float *grow0,
+                                                 size_t row_stride, int rows_ok, float *stage) {
+  constexpr int P = N + 4;
+  const int lane = threadIdx.x % 32;
 #pragma unroll
-      for (int v = 0; v < 8; ++v)
-        d4[v] = make_float4(__uint_as_float(r[4 * v]) * mul, __uint_as_float(r[4 * v + 1]) * mul,
+  for (int cc = 0; cc < N; cc += 32) {
+    uint32_t r[32];
+    tmem_ld32(tcol + c0 + cc, r);
+    tmem_wait_ld(r);
+    float4 *srow = reinterpret_cast<float4 *>(stage + lane * P + cc);
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      srow[v] = make_float4(__uint_as_float(r[4 * v]) * mul, __uint_as_float(r[4 * v + 1]) * mul,
                             __uint_as_float(r[4 * v + 2]) * mul, __uint_as_float(r[4 * v + 3]) * mul);
-    }
   }
+  __syncwarp();
+  constexpr int LPR = N / 4;     // lanes per row
+  constexpr int RPS = 32 / LPR;  // rows per store instruction
+  const int sub = lane % LPR;
+#pragma unroll 4
+  for (int r0 = 0; r0 < 32; r0 += RPS) {
+    const int row = r0 + lane / LPR;
+    if (row < rows_ok)
+      *reinterpret_cast<float4 *>(grow0 + static_cast<size_t>(row) * row_stride + c0 + 4 * sub) =
+          *reinterpret_cast<const float4 *>(stage + row * P + 4 * sub);
+  }
+  __syncwarp();
 }
 
 __device__ __forceinline__ void store_zero_row(int n, float *dst, bool row_ok) {
@@ -383,8 +407,15 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       ok = wd.wait(BAR(CF::BAR_ACC), 0, ROLE_SOFTMAX, CF::BAR_ACC);
       if (ok) {
         tc_fence_after();
-        store_acc_row(tmem + lane_off + CF::ACC0_COL, g * DV / 2, DV / 2, 1.0f, dv_row, key_ok);
-        store_acc_row(tmem + lane_off + CF::ACC1_COL, g * D / 2, D / 2, p.scale, dk_row, key_ok);
+        // The Q/dO ring is idle now (every product has completed): per-warp stages there.
+        float *stage = reinterpret_cast<float *>(smem + CF::A_SLOT_OFF) + warp * 32 * (cmax(D, DV) / 2 + 4);
+        const int row0 = j * BN + 32 * (warp % 4);  // the warp's first key
+        const int rows_ok = p.Nk - row0 < 32 ? (p.Nk - row0 > 0 ? p.Nk - row0 : 0) : 32;
+        const size_t base = static_cast<size_t>(bh) * p.Nk + row0;
+        store_acc_staged<DV / 2>(tmem + lane_off + CF::ACC0_COL, g * DV / 2, 1.0f, p.dV + base * DV, DV,
+                                 rows_ok, stage);
+        store_acc_staged<D / 2>(tmem + lane_off + CF::ACC1_COL, g * D / 2, p.scale, p.dK + base * D, D,
+                                rows_ok, stage);
       }
     } else if (ok) {
       store_zero_row(DV / 2, dv_row + g * DV / 2, key_ok);
@@ -543,6 +574,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 #ifdef ETA_PHASE_TRACE
   int trace_n = 0;
 #endif
+  ETA_TRACE(90);
 
   if (threadIdx.x == 0) {
     mbar_init(BAR(CF::BAR_FIXED), 1);
@@ -648,8 +680,14 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       ok = wd.wait(BAR(CF::BAR_ACC), 0, ROLE_SOFTMAX, CF::BAR_ACC);
       if (ok) {
         tc_fence_after();
-        store_acc_row(tmem + lane_off + DQ_ACC_COL, g * D / 2, D / 2, p.scale, dq_row, q_ok);
+        // The K ring is idle now (every product has completed): per-warp stages there.
+        float *stage = reinterpret_cast<float *>(smem + CF::B_K_OFF) + warp * 32 * (D / 2 + 4);
+        const int row0 = i * BM + 32 * (warp % 4);  // the warp's first query
+        const int rows_ok = p.Nq - row0 < 32 ? (p.Nq - row0 > 0 ? p.Nq - row0 : 0) : 32;
+        store_acc_staged<D / 2>(tmem + lane_off + DQ_ACC_COL, g * D / 2, p.scale,
+                                p.dQ + (static_cast<size_t>(bh) * p.Nq + row0) * D, D, rows_ok, stage);
       }
+      ETA_TRACE(92);
     } else if (ok) {
       store_zero_row(D / 2, dq_row + g * D / 2, q_ok);
     }
