@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 #ifdef ETA_PHASE_TRACE
   int trace_n = 0;
 #endif
+  ETA_TRACE(90);
   const Schedule<NQ, CAUSAL> sch(p);
   Watchdog wd{sbase + CF::ABORT_OFF, p};
 
@@ -615,36 +616,104 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         const int split = ur / p.ctas_per_head;
         const size_t lrow = (static_cast<size_t>(split) * p.BH + sch.bh) * p.Nq + (row_ok ? q_row : 0);
         const size_t orow = lrow * DV;
+        if (has_keys && !CF::DENSE) {
+          // This warpgroup's Q tile is idle now (its last product has completed): each warp
+          // stages 32 rows x 128 bytes of O there at a time, in 16-byte units placed at
+          // (unit ^ row % 8) so that neither side of the stage has bank conflicts, and
+          // stores them as whole 128-byte row segments, four rows per instruction.
+          static_assert(CF::Q_TILE / 4 >= 32 * 128, "a warp's stage is 32 rows of 128 bytes");
+          uint8_t *stage = smem + CF::Q_OFF + q * CF::Q_TILE + (warp % 4) * (CF::Q_TILE / 4);
+          uint4 *srow = reinterpret_cast<uint4 *>(stage + lane * 128);
+          const int row0 = q_row - lane;  // the warp's first query row
+          const int rows_ok = p.Nq - row0 < 32 ? (p.Nq - row0 > 0 ? p.Nq - row0 : 0) : 32;
+          const size_t obase = ((static_cast<size_t>(split) * p.BH + sch.bh) * p.Nq + row0) * DV;
+          const int sub = lane % 8;
+          // All eight shared loads go before the global stores, which the compiler could not
+          // otherwise move them past.
+          auto store_stage = [&](uint8_t *g0, int row_bytes) {
+            __syncwarp();
+            uint4 val[8];
 #pragma unroll
-        for (int cc = 0; cc < DV / 32; ++cc) {
-          uint32_t o[32];
-          if (has_keys) {
-            tmem_ld32(t_o + 32 * cc, o);
-            tmem_wait_ld(o);
-          } else {
+            for (int i = 0; i < 8; ++i) {
+              const int rr = 4 * i + lane / 8;
+              val[i] = *reinterpret_cast<const uint4 *>(stage + rr * 128 + 16 * (sub ^ (rr & 7)));
+            }
+            __syncwarp();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) o[c] = 0u;
-          }
-          float f[32];
+            for (int i = 0; i < 8; ++i) {
+              const int rr = 4 * i + lane / 8;
+              if (rr < rows_ok)
+                *reinterpret_cast<uint4 *>(g0 + static_cast<size_t>(rr) * row_bytes + 16 * sub) = val[i];
+            }
+          };
+          if (p.out_f32) {
+#pragma unroll 1
+            for (int cc = 0; cc < DV / 32; ++cc) {
+              uint32_t o[32];
+              tmem_ld32(t_o + 32 * cc, o);
+              tmem_wait_ld(o);
+              float f[32];
 #pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            mul2(f[c], f[c + 1], __uint_as_float(o[c]), __uint_as_float(o[c + 1]), inv_l, inv_l);
-          if (row_ok) {
-            if (p.out_f32) {
-              float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.O) + orow + 32 * cc);
+              for (int c = 0; c < 32; c += 2)
+                mul2(f[c], f[c + 1], __uint_as_float(o[c]), __uint_as_float(o[c + 1]), inv_l, inv_l);
 #pragma unroll
               for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(f[4 * v + 0], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
-            } else {
-              uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.O) + orow + 32 * cc);
+                srow[v ^ (lane & 7)] = make_uint4(__float_as_uint(f[4 * v + 0]), __float_as_uint(f[4 * v + 1]),
+                                                  __float_as_uint(f[4 * v + 2]), __float_as_uint(f[4 * v + 3]));
+              store_stage(reinterpret_cast<uint8_t *>(static_cast<float *>(p.O) + obase + 32 * cc), DV * 4);
+            }
+          } else {
+#pragma unroll 1
+            for (int cc = 0; cc < DV / 64; ++cc) {
 #pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint4 w;
-                w.x = pack_bf16(f[8 * v + 0], f[8 * v + 1]);
-                w.y = pack_bf16(f[8 * v + 2], f[8 * v + 3]);
-                w.z = pack_bf16(f[8 * v + 4], f[8 * v + 5]);
-                w.w = pack_bf16(f[8 * v + 6], f[8 * v + 7]);
-                dst[v] = w;
+              for (int h = 0; h < 2; ++h) {
+                uint32_t o[32];
+                tmem_ld32(t_o + 64 * cc + 32 * h, o);
+                tmem_wait_ld(o);
+                float f[32];
+#pragma unroll
+                for (int c = 0; c < 32; c += 2)
+                  mul2(f[c], f[c + 1], __uint_as_float(o[c]), __uint_as_float(o[c + 1]), inv_l, inv_l);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                  srow[(4 * h + v) ^ (lane & 7)] =
+                      make_uint4(pack_bf16(f[8 * v + 0], f[8 * v + 1]), pack_bf16(f[8 * v + 2], f[8 * v + 3]),
+                                 pack_bf16(f[8 * v + 4], f[8 * v + 5]), pack_bf16(f[8 * v + 6], f[8 * v + 7]));
+              }
+              store_stage(reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.O) + obase + 64 * cc), DV * 2);
+            }
+          }
+        } else {
+          // Direct stores, one row per lane: for a tile that sees no key (O = 0; its Q copy
+          // may still be landing, so nothing is staged) and for the dense-bias kernel, whose
+          // single softmax warpgroup measured slower with the staged stores. Every lane runs
+          // the tensor-memory loads (warp-collective); only the stores depend on the row.
+#pragma unroll
+          for (int cc = 0; cc < DV / 32; ++cc) {
+            uint32_t o[32];
+            if (has_keys) {
+              tmem_ld32(t_o + 32 * cc, o);
+              tmem_wait_ld(o);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = 0u;
+            }
+            float f[32];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2)
+              mul2(f[c], f[c + 1], __uint_as_float(o[c]), __uint_as_float(o[c + 1]), inv_l, inv_l);
+            if (row_ok) {
+              if (p.out_f32) {
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.O) + orow + 32 * cc);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  dst[v] = make_float4(f[4 * v + 0], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
+              } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.O) + orow + 32 * cc);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                  dst[v] = make_uint4(pack_bf16(f[8 * v + 0], f[8 * v + 1]), pack_bf16(f[8 * v + 2], f[8 * v + 3]),
+                                      pack_bf16(f[8 * v + 4], f[8 * v + 5]), pack_bf16(f[8 * v + 6], f[8 * v + 7]));
               }
             }
           }
@@ -654,6 +723,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
           p.LSE[lrow] =
               (l > 0.0f) ? (m2 + lg2_approx(l)) * LN2 : -INFINITY;
         }
+        ETA_TRACE(92);
       }
     }
   } else {
