@@ -493,12 +493,9 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
           const float4 *kb = reinterpret_cast<const float4 *>(smem + CF::KB_OFF + slot * BN * 4);
 #pragma unroll
           for (int u = 0; u < BN / 4; ++u) {
-            const float4 cv = kb[u];
-            float b0, b1, b2, b3;
-            mul2(b0, b1, cv.x, cv.y, LOG2E, LOG2E);
-            mul2(b2, b3, cv.z, cv.w, LOG2E, LOG2E);
-            fma2(x[4 * u + 0], x[4 * u + 1], x[4 * u + 0], x[4 * u + 1], sl2, sl2, b0, b1);
-            fma2(x[4 * u + 2], x[4 * u + 3], x[4 * u + 2], x[4 * u + 3], sl2, sl2, b2, b3);
+            const float4 cv = kb[u];  // c_j log2(e), stored so by the bias copy
+            fma2(x[4 * u + 0], x[4 * u + 1], x[4 * u + 0], x[4 * u + 1], sl2, sl2, cv.x, cv.y);
+            fma2(x[4 * u + 2], x[4 * u + 3], x[4 * u + 2], x[4 * u + 3], sl2, sl2, cv.z, cv.w);
           }
           __syncwarp();
           mbar_arrive_elect(BAR(CF::B_KBEMPTY + slot));
@@ -914,6 +911,11 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
           v.y = (k0 + 1 < p.Nk) ? __ldg(src + k0 + 1) : 0.0f;
           v.z = (k0 + 2 < p.Nk) ? __ldg(src + k0 + 2) : 0.0f;
           v.w = (k0 + 3 < p.Nk) ? __ldg(src + k0 + 3) : 0.0f;
+          // Stored in log2(e) units, the scale of the softmax's exponents.
+          v.x *= LOG2E;
+          v.y *= LOG2E;
+          v.z *= LOG2E;
+          v.w *= LOG2E;
           reinterpret_cast<float4 *>(smem + CF::KB_OFF + slot * BN * 4)[lane] = v;
           __syncwarp();
           mbar_arrive_elect(BAR(CF::B_KBFULL + slot));
