@@ -513,6 +513,15 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       bulk_load(sl + CF::Q_TILE + CF::DO_TILE + BM * 4, p.Dd + lrow, BM * 4, BAR(CF::BAR_FULL + slot));
       ++issued;
     }
+    // The block the hardware will likely start next is about one wave ahead: warm L2 with
+    // its K and V tiles (each unit's own) so that its first products do not wait on HBM.
+    const unsigned next = blockIdx.x + nsmid();
+    if (next < gridDim.x) {
+      int nbh, nj;
+      unit_of_block(next, p.BH, p.nkv_tiles, p.head_group, &nbh, &nj);
+      for (int kc = 0; kc < D / SW_CHUNK; ++kc) tma_prefetch_l2_3d(&tmK, kc * SW_CHUNK, nj * BN, nbh);
+      for (int kc = 0; kc < DV / SW_CHUNK; ++kc) tma_prefetch_l2_3d(&tmV, kc * SW_CHUNK, nj * BN, nbh);
+    }
     // Copies still in flight land before the CTA exits.
     if (n_it > 0) wd.wait1(BAR(CF::BAR_FIXED), 0, ROLE_DRAIN, CF::BAR_FIXED, true);
     for (int s = 0; s < CF::A_QS && s < issued; ++s) {
@@ -776,6 +785,16 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       for (int kc = 0; kc < D / SW_CHUNK; ++kc)
         tma_load_3d(sl + kc * SW_CHUNK_BYTES, &tmK, kc * SW_CHUNK, it * BN, bh, BAR(CF::BAR_FULL + slot));
       ++issued;
+    }
+    // The block the hardware will likely start next is about one wave ahead: warm L2 with
+    // its Q and dO tiles (each unit's own) so that its first products do not wait on HBM.
+    const unsigned next = blockIdx.x + nsmid();
+    if (next < gridDim.x) {
+      int nbh, nri;
+      unit_of_block(next, p.BH, p.nq_tiles, p.head_group, &nbh, &nri);
+      const int ni = p.nq_tiles - 1 - nri;
+      for (int kc = 0; kc < D / SW_CHUNK; ++kc) tma_prefetch_l2_3d(&tmQ, kc * SW_CHUNK, ni * BM, nbh);
+      for (int kc = 0; kc < DV / SW_CHUNK; ++kc) tma_prefetch_l2_3d(&tmdO, kc * SW_CHUNK, ni * BM, nbh);
     }
     if (n_it > 0) wd.wait1(BAR(CF::BAR_FIXED), 0, ROLE_DRAIN, CF::BAR_FIXED, true);
     for (int s = 0; s < CF::B_KS && s < issued; ++s) {

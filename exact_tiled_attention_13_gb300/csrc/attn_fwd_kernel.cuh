@@ -273,10 +273,10 @@ struct Schedule {
   int bh, cta_q, n_exist, hi_max, n_it;
   int first0, first1;  // first_it of query tiles 0 and 1
 
-  __device__ Schedule(const KernelParams &p) {
+  __device__ explicit Schedule(const KernelParams &p, unsigned unit) {
     // A head's units: key range, then query tiles from the last (most causal work) down.
     int r;
-    unit_of_block(blockIdx.x, p.BH, p.ctas_per_head * p.n_splits, p.head_group, &bh, &r);
+    unit_of_block(unit, p.BH, p.ctas_per_head * p.n_splits, p.head_group, &bh, &r);
     const int split = r / p.ctas_per_head;
     cta_q = p.ctas_per_head - 1 - r % p.ctas_per_head;
     n_exist = cmin(NQ, p.nq_tiles - cta_q * NQ);
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   int trace_n = 0;
 #endif
   ETA_TRACE(90);
-  const Schedule<NQ, CAUSAL> sch(p);
+  const Schedule<NQ, CAUSAL> sch(p, blockIdx.x);
   Watchdog wd{sbase + CF::ABORT_OFF, p};
 
   // ------------------------------------------------------------------ set-up
@@ -840,6 +840,17 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
           tma_load_3d(sbase + CF::K_OFF + ks * CF::K_TILE + kc * SW_CHUNK_BYTES, &tmK,
                       kc * SW_CHUNK, j * BN, sch.bh, BAR(CF::B_KFULL + ks));
         last[ks] = it;
+      }
+      // The block the hardware will likely start next, on the first SM to free up, is about
+      // one wave ahead: warm L2 with its Q tiles (each unit's own, read from HBM once) so
+      // that its first S product does not wait on HBM. (Not in the dense-bias kernel, which
+      // is bound by the bias stream and measured slower with it.)
+      const unsigned next = blockIdx.x + nsmid();
+      if (!CF::DENSE && next < gridDim.x) {
+        const Schedule<NQ, CAUSAL> nxt(p, next);
+        for (int q = 0; q < nxt.n_exist; ++q)
+          for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+            tma_prefetch_l2_3d(&tmQ, kc * SW_CHUNK, nxt.q_tile(q) * BM, nxt.bh);
       }
       // Wait for the last copy into each slot to land before the CTA may exit.
       wd.wait1(BAR(CF::B_QFULL), 0, ROLE_DRAIN, CF::B_QFULL, true);

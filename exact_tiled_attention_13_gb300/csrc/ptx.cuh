@@ -86,6 +86,22 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// Brings a 3-D tile of the tensor into L2 (nothing lands in shared memory and nothing is
+// signalled): a hint that a later copy of the same tile will find it there.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// Number of SM identifiers of the device (at least the number of SMs).
+__device__ __forceinline__ unsigned nsmid() {
+  unsigned n;
+  asm("mov.u32 %0, %%nsmid;" : "=r"(n));
+  return n;
+}
+
 // 1-D bulk copy of `bytes` (a multiple of 16) from global to shared memory; both
 // addresses 16-byte aligned. Completion is signalled on `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
