@@ -47,7 +47,7 @@ struct BwdParams {
   int head_group;     // heads per scheduling group (unit_of_block)
   float scale_log2;   // scale * log2(e)
   float scale;
-  const float *Lp;    // [BH][nqp] LSE * log2(e), +inf where p must be 0
+  const float *Lp;    // [BH][nqp] -LSE * log2(e), -inf where p must be 0
   const float *Dd;    // [BH][nqp] D_i = dO_i . O_i
   const float *C;     // dense bias [BH][Nq][Nk] or null
   const float *ckey;  // per-key bias [BH][Nk] or null
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256)
   const int bh = in ? static_cast<int>(prow / nqp) : 0;
   const int i = in ? static_cast<int>(prow % nqp) : Nq;
   float acc = 0.0f;
-  float lp = INFINITY;
+  float lp = -INFINITY;
   if (i < Nq) {
     const long long row = static_cast<long long>(bh) * Nq + i;
     const uint4 g = __ldg(reinterpret_cast<const uint4 *>(dO + row * DV) + sub);
@@ -101,7 +101,9 @@ __global__ void __launch_bounds__(256)
       acc = fmaf(__uint_as_float(gw[k] & 0xFFFF0000u), o[2 * k + 1], acc);
     }
     const float lse = LSE[row];
-    lp = lse == -INFINITY ? INFINITY : lse * LOG2E;
+    // -LSE log2(e), so that 2^(S scale log2(e) + lp) = exp(S scale - LSE); -inf (every p
+    // is 0) for a row with no allowed key, as for a padding row.
+    lp = lse == -INFINITY ? -INFINITY : -lse * LOG2E;
   }
 #pragma unroll
   for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
@@ -148,9 +150,7 @@ struct BwdCfg {
   static constexpr int B_V_OFF = B_K_OFF + B_KS * Q_TILE;
   static constexpr int B_BAR_OFF = B_V_OFF + B_VS * DO_TILE;
   static_assert(A_QS >= 2 && B_KS >= 2 && B_VS >= 2, "need two ring slots");
-  // Epilogue stages (8 warps x 32 rows x (width / 2 + 4) floats) reuse the rings.
-  static_assert(8 * 32 * ((D > DV ? D : DV) / 2 + 4) * 4 <= A_QS * A_SLOT,
-                "dK/dV epilogue stage larger than the Q/dO ring it reuses");
+  // dQ epilogue stages (8 warps x 32 rows x (d / 2 + 4) floats) reuse the K ring.
   static_assert(8 * 32 * (D / 2 + 4) * 4 <= B_KS * Q_TILE,
                 "dQ epilogue stage larger than the K ring it reuses");
   static_assert(A_SLOT % 1024 == 0, "slots keep 1024-byte alignment");
@@ -186,10 +186,20 @@ struct BwdCfg {
   static constexpr int ACC1_COL = 256 + DV;   // dK (dkdv)
   static constexpr int TMEM_COLS = 512;
 
-  static constexpr int NUM_WARPS = 12;
+  static constexpr int NUM_WARPS = 12;  // dq: 8 elementwise warps, MMA, two copy warps
   static constexpr int THREADS = 32 * NUM_WARPS;
   static constexpr int MMA_WARP = 8;
   static constexpr int LOAD_WARP = 9;
+  // dkdv: 16 elementwise warps (four per tensor-memory lane quarter, 32 query columns
+  // each), the MMA warp and the copy warp.
+  static constexpr int A_EW_WARPS = 16;
+  static constexpr int A_THREADS = 32 * (A_EW_WARPS + 2);
+  static constexpr int A_MMA_WARP = A_EW_WARPS;
+  static constexpr int A_LOAD_WARP = A_EW_WARPS + 1;
+  // The dK/dV epilogue stages (16 warps x 32 rows x (width / 2 + 4) floats) reuse the K, V
+  // and ring memory from offset 0.
+  static_assert(16 * 32 * ((D > DV ? D : DV) / 2 + 4) * 4 <= A_SLOT_OFF + A_QS * A_SLOT,
+                "dK/dV epilogue stage larger than the memory it reuses");
 
   static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(128, HALF, false);  // S, dP halves
   static constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, false);     // full-width S, dP
@@ -268,7 +278,7 @@ __device__ __forceinline__ void store_zero_row(int n, float *dst, bool row_ok) {
 
 // ------------------------------------------------------------------------ dK, dV
 template <int D, int DV, bool CAUSAL, int BIAS>
-__global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::A_THREADS, 1)
     attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                          const __grid_constant__ BwdParams p) {
@@ -284,8 +294,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // This CTA: head bh, key tile j; the query tiles that see it are i_lo .. nq_tiles - 1,
-  // each in two halves of 64 queries (units u = 0 .. 2 n_it - 1).
+  // This CTA: head bh, key tile j; the query tiles that see it are i_lo .. nq_tiles - 1
+  // (tiles t = 0 .. n_it - 1).
   // Units of a head: key tiles from the first (seen by the most queries) on.
   int bh, j;
   unit_of_block(blockIdx.x, p.BH, p.nkv_tiles, p.head_group, &bh, &j);
@@ -296,7 +306,6 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     i_lo = q0 >= p.Nq ? p.nq_tiles : (q0 <= 0 ? 0 : q0 / BM);
   }
   const int n_it = p.nq_tiles - i_lo;
-  const int n_u = 2 * n_it;
   BwdWatchdog wd{sbase + CF::A_BAR_OFF + CF::BAR_BYTES + 4, p};
 #ifdef ETA_PHASE_TRACE
   int trace_n = 0;
@@ -308,16 +317,17 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       mbar_init(BAR(CF::BAR_FULL + s), 1);
       mbar_init(BAR(CF::BAR_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(BAR(CF::BAR_SFULL + b), 1);
-      mbar_init(BAR(CF::BAR_PFULL + b), 8);
-    }
+    mbar_init(BAR(CF::BAR_SFULL), 1);
+    mbar_init(BAR(CF::BAR_DPFULL), 1);
+    mbar_init(BAR(CF::BAR_DPFREE), CF::A_EW_WARPS);
+    mbar_init(BAR(CF::BAR_PFULL), CF::A_EW_WARPS);      // dS^T(t) written
+    mbar_init(BAR(CF::BAR_PFULL + 1), CF::A_EW_WARPS);  // P^T(t) written
     mbar_init(BAR(CF::BAR_ACC), 1);
     mbar_init(BAR(CF::BAR_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == CF::MMA_WARP) {
+  if (warp == CF::A_MMA_WARP) {
     tmem_alloc(smem_u32(tmem_ptr), CF::TMEM_COLS);
     tmem_relinquish();
   }
@@ -326,161 +336,209 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
 
-  if (warp < 8) {
+  if (warp < CF::A_EW_WARPS) {
     // ============================================================ elementwise
-    const int g = warp / 4;  // columns [32 g, 32 g + 32) of each 64-query half
+    // Tile t: S^T(t) in buffer t & 1, dP^T(t) in the other. Warp g = warp / 4 owns queries
+    // [32 g, 32 g + 32) of the tile (columns of both buffers) for its 32 keys (tensor-memory
+    // lanes). It forms P^T from S^T while dP^T is still being computed, then reads dP^T,
+    // frees its buffer for S^T(t+1), and writes dS^T. P^T and dS^T go packed (two bf16 per
+    // 32-bit column) over the columns of S^T this warp read: P^T at [32 g, 32 g + 16), dS^T
+    // at [32 g + 16, 32 g + 32).
+    const int g = warp / 4;
     const int r = threadIdx.x % 128;
     const int key = j * BN + r;
     const bool key_ok = key < p.Nk;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
+    const float sl2 = p.scale_log2;
     // Per-key bias of this row, log2-scaled (-inf for a padded key: its p is 0). Rows past
     // the last key need no mask: their K and V rows are zero-filled, so they only produce
     // dK and dV rows that are never stored.
     float kb = 0.0f;
     if (BIAS == BWD_BIAS_KEY) kb = key_ok ? p.ckey[static_cast<size_t>(bh) * p.Nk + key] * LOG2E : 0.0f;
     bool ok = true;
-    for (int u = 0; u < n_u; ++u) {
-      const int b = u & 1;  // half within the query tile = tensor-memory buffer
-      const int i = i_lo + u / 2;
-      const int slot = (u / 2) % CF::A_QS;
-      ok = wd.wait(BAR(CF::BAR_SFULL + b), (u / 2) & 1, ROLE_SOFTMAX, CF::BAR_SFULL + b);
-      if (!ok) break;
-      tc_fence_after();
-      ETA_TRACE(40);
-      const int c0 = HALF * b + 32 * g;  // query offset within the tile
+    for (int t = 0; t < n_it; ++t) {
+      const int i = i_lo + t;
+      const int slot = t % CF::A_QS;
+      const int c0 = 32 * g;  // query offset within the tile
+      const uint32_t t_s = tmem + lane_off + CF::S_COL + 128 * (t & 1) + c0;
+      const uint32_t t_dp = tmem + lane_off + CF::S_COL + 128 * ((t + 1) & 1) + c0;
       const float *Ls = reinterpret_cast<const float *>(smem + CF::A_SLOT_OFF + slot * CF::A_SLOT +
                                                         CF::Q_TILE + CF::DO_TILE) + c0;
       const float *Ds = Ls + BM;
-      // Keys past the causal limit of this chunk's first query need the elementwise test.
-      const bool diag = CAUSAL && (j * BN + BN - 1 > i * BM + c0 + p.causal_off);
-      const uint32_t t_s = tmem + lane_off + CF::S_COL + HALF * b + 32 * g;
-      const uint32_t t_dp = tmem + lane_off + CF::DP_COL + HALF * b + 32 * g;
-      uint32_t sr[32], dr[32];
-      ld_pair(t_s, t_dp, sr, dr);
-      ETA_TRACE(41);
-      if (diag) {  // keys past query q's causal limit: S = -inf, so p = 0
-        const int lim = i * BM + c0 + p.causal_off - key;  // column c is forbidden when c < -lim
+      ok = wd.wait(BAR(CF::BAR_SFULL), t & 1, ROLE_SOFTMAX, CF::BAR_SFULL);
+      if (!ok) break;
+      tc_fence_after();
+      ETA_TRACE(40);
+      // p = 2^x, x = scale S log2(e) + (bias log2(e) - LSE log2(e)) = log2 of exp(S_ij - LSE_i),
+      // in pairs of columns.
+      float pv[32];
+      {
+        uint32_t sr[32];
+        tmem_ld32(t_s, sr);
+        tmem_wait_ld(sr);
+        // Keys past the causal limit of this chunk's first query need the elementwise test.
+        if (CAUSAL && (j * BN + BN - 1 > i * BM + c0 + p.causal_off)) {
+          const int lim = i * BM + c0 + p.causal_off - key;  // column c is forbidden when c < -lim
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c + lim < 0) sr[c] = __float_as_uint(-INFINITY);
-      }
-      uint32_t pp[16], dd[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float4 L4 = *reinterpret_cast<const float4 *>(Ls + c);
-        const float4 D4 = *reinterpret_cast<const float4 *>(Ds + c);
-        const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
-        const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
-        float pv[4], dv[4];
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          // x = (scale S + bias) log2(e) - LSE log2(e), so that p = 2^x = exp(S_ij - LSE_i).
-          float x = BIAS == BWD_BIAS_KEY ? fmaf(__uint_as_float(sr[c + v]), p.scale_log2, kb) - Lv[v]
-                                         : fmaf(__uint_as_float(sr[c + v]), p.scale_log2, -Lv[v]);
-          if (BIAS == BWD_BIAS_DENSE) {
-            const int q = i * BM + c0 + c + v;
-            x += (key_ok && q < p.Nq) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
-                                      : 0.0f;
-          }
-          const float pr = ex2_approx(x);
-          pv[v] = pr;
-          dv[v] = pr * (__uint_as_float(dr[c + v]) - Dv[v]);
+          for (int c = 0; c < 32; ++c)
+            if (c + lim < 0) sr[c] = __float_as_uint(-INFINITY);
         }
-        pp[c / 2] = pack_bf16(pv[0], pv[1]);
-        pp[c / 2 + 1] = pack_bf16(pv[2], pv[3]);
-        dd[c / 2] = pack_bf16(dv[0], dv[1]);
-        dd[c / 2 + 1] = pack_bf16(dv[2], dv[3]);
+        uint32_t pp[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          const float4 L4 = *reinterpret_cast<const float4 *>(Ls + c);  // -LSE log2(e)
+          float b[4] = {L4.x, L4.y, L4.z, L4.w};
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            if (BIAS == BWD_BIAS_KEY) b[v] += kb;
+            if (BIAS == BWD_BIAS_DENSE) {
+              const int q = i * BM + c0 + c + v;
+              b[v] += (key_ok && q < p.Nq) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
+                                           : 0.0f;
+            }
+          }
+          float x[4];
+          fma2(x[0], x[1], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]), sl2, sl2, b[0], b[1]);
+          fma2(x[2], x[3], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]), sl2, sl2, b[2], b[3]);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) pv[c + v] = ex2_approx(x[v]);
+          pp[c / 2] = pack_bf16(pv[c], pv[c + 1]);
+          pp[c / 2 + 1] = pack_bf16(pv[c + 2], pv[c + 3]);
+        }
+        tmem_st16(t_s, pp);
       }
-      ETA_TRACE(42);
-      tmem_st16(t_s, pp);
-      tmem_st16(t_dp, dd);
+      // P^T(t) is written: dV += P^T dO may start while dS^T is formed.
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      mbar_arrive_elect(BAR(CF::BAR_PFULL + b));
+      mbar_arrive_elect(BAR(CF::BAR_PFULL + 1));
+      ETA_TRACE(41);
+      ok = wd.wait(BAR(CF::BAR_DPFULL), t & 1, ROLE_SOFTMAX, CF::BAR_DPFULL);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t dr[32];
+      tmem_ld32(t_dp, dr);
+      tmem_wait_ld(dr);
+      // dP^T(t) is in registers: its buffer may take S^T(t+1).
+      tc_fence_before();
+      __syncwarp();
+      mbar_arrive_elect(BAR(CF::BAR_DPFREE));
+      ETA_TRACE(42);
+      uint32_t dd[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const float4 D4 = *reinterpret_cast<const float4 *>(Ds + c);
+        // dS = p (dP - D), in pairs of columns.
+        float tq[4], dv[4];
+        sub2(tq[0], tq[1], __uint_as_float(dr[c]), __uint_as_float(dr[c + 1]), D4.x, D4.y);
+        sub2(tq[2], tq[3], __uint_as_float(dr[c + 2]), __uint_as_float(dr[c + 3]), D4.z, D4.w);
+        mul2(dv[0], dv[1], pv[c], pv[c + 1], tq[0], tq[1]);
+        mul2(dv[2], dv[3], pv[c + 2], pv[c + 3], tq[2], tq[3]);
+        dd[c / 2] = pack_bf16(dv[0], dv[1]);
+        dd[c / 2 + 1] = pack_bf16(dv[2], dv[3]);
+      }
+      tmem_st16(t_s + 16, dd);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      mbar_arrive_elect(BAR(CF::BAR_PFULL));
       ETA_TRACE(43);
     }
     // ---------------------------------------------------------- epilogue: dV, scale dK
-    float *dv_row = p.dV + (static_cast<size_t>(bh) * p.Nk + (key_ok ? key : 0)) * DV;
-    float *dk_row = p.dK + (static_cast<size_t>(bh) * p.Nk + (key_ok ? key : 0)) * D;
+    // Warps g = 0, 1 store halves of dV, warps g = 2, 3 halves of dK.
+    const bool is_dv = g < 2;
+    const int half = g & 1;
     if (ok && n_it > 0) {
       ok = wd.wait(BAR(CF::BAR_ACC), 0, ROLE_SOFTMAX, CF::BAR_ACC);
       if (ok) {
         tc_fence_after();
-        // The Q/dO ring is idle now (every product has completed): per-warp stages there.
-        float *stage = reinterpret_cast<float *>(smem + CF::A_SLOT_OFF) + warp * 32 * (cmax(D, DV) / 2 + 4);
+        // Every product has completed and every copy landed: per-warp stages over the K, V
+        // and ring memory.
+        float *stage = reinterpret_cast<float *>(smem) + warp * 32 * (cmax(D, DV) / 2 + 4);
         const int row0 = j * BN + 32 * (warp % 4);  // the warp's first key
         const int rows_ok = p.Nk - row0 < 32 ? (p.Nk - row0 > 0 ? p.Nk - row0 : 0) : 32;
         const size_t base = static_cast<size_t>(bh) * p.Nk + row0;
-        store_acc_staged<DV / 2>(tmem + lane_off + CF::ACC0_COL, g * DV / 2, 1.0f, p.dV + base * DV, DV,
-                                 rows_ok, stage);
-        store_acc_staged<D / 2>(tmem + lane_off + CF::ACC1_COL, g * D / 2, p.scale, p.dK + base * D, D,
-                                rows_ok, stage);
+        if (is_dv)
+          store_acc_staged<DV / 2>(tmem + lane_off + CF::ACC0_COL, half * DV / 2, 1.0f, p.dV + base * DV, DV,
+                                   rows_ok, stage);
+        else
+          store_acc_staged<D / 2>(tmem + lane_off + CF::ACC1_COL, half * D / 2, p.scale, p.dK + base * D, D,
+                                  rows_ok, stage);
       }
     } else if (ok) {
-      store_zero_row(DV / 2, dv_row + g * DV / 2, key_ok);
-      store_zero_row(D / 2, dk_row + g * D / 2, key_ok);
+      if (is_dv)
+        store_zero_row(DV / 2, p.dV + (static_cast<size_t>(bh) * p.Nk + (key_ok ? key : 0)) * DV + half * DV / 2, key_ok);
+      else
+        store_zero_row(D / 2, p.dK + (static_cast<size_t>(bh) * p.Nk + (key_ok ? key : 0)) * D + half * D / 2, key_ok);
     }
-  } else if (warp == CF::MMA_WARP) {
+  } else if (warp == CF::A_MMA_WARP) {
     // ============================================================ MMA issue
+    // Order on the tensor cores: S^T(0), dP^T(0); then per tile t: S^T(t+1) (once dP^T(t)
+    // is in registers), dV += P^T(t) dO_t (once P^T is written), dK += dS^T(t) Q_t (once
+    // dS^T is written), dP^T(t+1) into the buffer they came from.
     bool ok = n_it == 0 || wd.wait(BAR(CF::BAR_FIXED), 0, ROLE_MMA, CF::BAR_FIXED);
     const uint64_t k_desc = smem_desc(sbase + CF::A_K_OFF, 16, 1024);
     const uint64_t v_desc = smem_desc(sbase + CF::A_V_OFF, 16, 1024);
-    // S^T and dP^T of unit u (both operands K-major; B = rows 64 h of the slot's tiles).
-    auto issue_sdp = [&](int u) -> bool {
-      const int b = u & 1;
-      const int slot = (u / 2) % CF::A_QS;
-      if (b == 0) {  // a new query tile: wait for its copies
-        if (!wd.wait(BAR(CF::BAR_FULL + slot), ((u / 2) / CF::A_QS) & 1, ROLE_MMA, CF::BAR_FULL + slot))
-          return false;
-        tc_fence_after();
-      }
-      const uint32_t sl = sbase + CF::A_SLOT_OFF + slot * CF::A_SLOT;
-      const uint64_t q_desc = smem_desc(sl, 16, 1024) + half_rows(b);
-      const uint64_t do_desc = smem_desc(sl + CF::Q_TILE, 16, 1024) + half_rows(b);
+    auto slot_addr = [&](int t) -> uint32_t { return sbase + CF::A_SLOT_OFF + (t % CF::A_QS) * CF::A_SLOT; };
+    // S^T(t) = K Q_t^T into buffer t & 1, after waiting for tile t's copies.
+    auto issue_s = [&](int t) -> bool {
+      const int slot = t % CF::A_QS;
+      if (!wd.wait(BAR(CF::BAR_FULL + slot), (t / CF::A_QS) & 1, ROLE_MMA, CF::BAR_FULL + slot)) return false;
+      tc_fence_after();
+      const uint64_t q_desc = smem_desc(slot_addr(t), 16, 1024);
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks)
-        mma_ss_elect(tmem + CF::S_COL + HALF * b, k_desc + kmajor_step(ks), q_desc + kmajor_step(ks),
-                     CF::IDESC_HALF, ks > 0 ? 1u : 0u);
-#pragma unroll
-      for (int ks = 0; ks < DV / 16; ++ks)
-        mma_ss_elect(tmem + CF::DP_COL + HALF * b, v_desc + kmajor_step(ks), do_desc + kmajor_step(ks),
-                     CF::IDESC_HALF, ks > 0 ? 1u : 0u);
-      mma_commit_elect(BAR(CF::BAR_SFULL + b));
+        mma_ss_elect(tmem + CF::S_COL + 128 * (t & 1), k_desc + kmajor_step(ks), q_desc + kmajor_step(ks),
+                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_SFULL));
       return true;
     };
-    if (ok && n_u > 0) ok = issue_sdp(0);
-    for (int u = 0; ok && u < n_u; ++u) {
-      const int b = u & 1;
-      const int slot = (u / 2) % CF::A_QS;
-      // The next half's products go first, so the tensor cores work while this half's
-      // P and dS are formed (its buffer was last read by the products of u - 1).
+    // dP^T(t) = V dO_t^T into the other buffer (tile t's copies have landed).
+    auto issue_dp = [&](int t) {
+      const uint64_t do_desc = smem_desc(slot_addr(t) + CF::Q_TILE, 16, 1024);
+#pragma unroll
+      for (int ks = 0; ks < DV / 16; ++ks)
+        mma_ss_elect(tmem + CF::S_COL + 128 * ((t + 1) & 1), v_desc + kmajor_step(ks), do_desc + kmajor_step(ks),
+                     CF::IDESC_SS, ks > 0 ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_DPFULL));
+    };
+    if (ok && n_it > 0 && (ok = issue_s(0))) issue_dp(0);
+    for (int t = 0; ok && t < n_it; ++t) {
       ETA_TRACE(50);
-      if (u + 1 < n_u && !(ok = issue_sdp(u + 1))) break;
+      if (t + 1 < n_it) {
+        if (!(ok = wd.wait(BAR(CF::BAR_DPFREE), t & 1, ROLE_MMA, CF::BAR_DPFREE))) break;
+        tc_fence_after();
+        if (!(ok = issue_s(t + 1))) break;
+      }
       ETA_TRACE(51);
-      ok = wd.wait(BAR(CF::BAR_PFULL + b), (u / 2) & 1, ROLE_MMA, CF::BAR_PFULL + b);
+      // dV_j += P^T dO_t, then dK_j += dS^T Q_t (A from tensor memory: step ks covers
+      // queries [16 ks, 16 ks + 16), packed by warp group ks / 2; B MN-major over the
+      // tile's rows), each once its operand is written.
+      ok = wd.wait(BAR(CF::BAR_PFULL + 1), t & 1, ROLE_MMA, CF::BAR_PFULL + 1);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t sb = tmem + CF::S_COL + 128 * (t & 1);
+      const uint64_t do_mn = smem_desc(slot_addr(t) + CF::Q_TILE, SW_CHUNK_BYTES, 1024);
+      const uint64_t q_mn = smem_desc(slot_addr(t), SW_CHUNK_BYTES, 1024);
+#pragma unroll
+      for (int ks = 0; ks < BM / 16; ++ks)
+        mma_ts_elect(tmem + CF::ACC0_COL, sb + 32 * (ks / 2) + 8 * (ks % 2), do_mn + mn_step(0, ks),
+                     CF::IDESC_NV, (t > 0 || ks > 0) ? 1u : 0u);
+      ok = wd.wait(BAR(CF::BAR_PFULL), t & 1, ROLE_MMA, CF::BAR_PFULL);
       if (!ok) break;
       tc_fence_after();
       ETA_TRACE(52);
-      // dV_j += P^T dO_h, dK_j += dS^T Q_h (A from tensor memory, B MN-major over the
-      // half's 64 query rows).
-      const uint32_t sl = sbase + CF::A_SLOT_OFF + slot * CF::A_SLOT;
-      const uint64_t do_mn = smem_desc(sl + CF::Q_TILE, SW_CHUNK_BYTES, 1024);
-      const uint64_t q_mn = smem_desc(sl, SW_CHUNK_BYTES, 1024);
 #pragma unroll
-      for (int ks = 0; ks < HALF / 16; ++ks)
-        mma_ts_elect(tmem + CF::ACC0_COL, tmem + CF::S_COL + packed_col(b, ks), do_mn + mn_step(b, ks),
-                     CF::IDESC_NV, (u > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-      for (int ks = 0; ks < HALF / 16; ++ks)
-        mma_ts_elect(tmem + CF::ACC1_COL, tmem + CF::DP_COL + packed_col(b, ks), q_mn + mn_step(b, ks),
-                     CF::IDESC_ND, (u > 0 || ks > 0) ? 1u : 0u);
-      if (b == 1) mma_commit_elect(BAR(CF::BAR_EMPTY + slot));  // both halves of the tile done
+      for (int ks = 0; ks < BM / 16; ++ks)
+        mma_ts_elect(tmem + CF::ACC1_COL, sb + 16 + 32 * (ks / 2) + 8 * (ks % 2), q_mn + mn_step(0, ks),
+                     CF::IDESC_ND, (t > 0 || ks > 0) ? 1u : 0u);
+      mma_commit_elect(BAR(CF::BAR_EMPTY + (t % CF::A_QS)));
+      if (t + 1 < n_it) issue_dp(t + 1);
     }
     if (ok && n_it > 0) mma_commit_elect(BAR(CF::BAR_ACC));
     mma_commit_elect(BAR(CF::BAR_DRAIN));
     wd.drain(BAR(CF::BAR_DRAIN), 0, CF::BAR_DRAIN);
-  } else if (warp == CF::LOAD_WARP && lane == 0) {
+  } else if (warp == CF::A_LOAD_WARP && lane == 0) {
     // ============================================================ TMA producer
     if (n_it > 0) {
       tma_prefetch_desc(&tmQ);
@@ -534,7 +592,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == CF::MMA_WARP) tmem_dealloc(tmem, CF::TMEM_COLS);
+  if (warp == CF::A_MMA_WARP) tmem_dealloc(tmem, CF::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------------ dQ
@@ -623,7 +681,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     const bool q_ok = q < p.Nq;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
     const size_t lrow = static_cast<size_t>(bh) * p.nqp + static_cast<size_t>(q);
-    const float Lr = p.Lp[lrow];  // +inf for padding rows and rows with no allowed key
+    const float nL = p.Lp[lrow];  // -LSE log2(e); -inf for padding rows and rows with no allowed key
     const float Dr = p.Dd[lrow];
     const int lim = CAUSAL ? q + p.causal_off : INT_MAX;  // last key this row may see
     bool ok = true;
@@ -661,7 +719,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 #pragma unroll
           for (int v = 0; v < 2; ++v) {
             const int key = k0 + c + v;
-            float x = fmaf(__uint_as_float(sr[c + v]), p.scale_log2, -Lr);
+            float x = fmaf(__uint_as_float(sr[c + v]), p.scale_log2, nL);
             if (BIAS == BWD_BIAS_KEY)
               x += key < p.Nk ? __ldg(p.ckey + static_cast<size_t>(bh) * p.Nk + key) * LOG2E : 0.0f;
             if (BIAS == BWD_BIAS_DENSE)
@@ -847,7 +905,7 @@ cudaError_t launch_bwd(const BwdLaunchArgs &a) {
   if (e != cudaSuccess) return e;
   const unsigned grid_a = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.nkv_tiles);
   const unsigned grid_b = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.nq_tiles);
-  ka<<<grid_a, CF::THREADS, CF::A_SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
+  ka<<<grid_a, CF::A_THREADS, CF::A_SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   kb<<<grid_b, CF::THREADS, CF::B_SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
   return cudaGetLastError();

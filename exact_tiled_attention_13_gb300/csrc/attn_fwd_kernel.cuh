@@ -56,7 +56,8 @@ __device__ unsigned long long g_eta_trace[ETA_TRACE_CTAS][ETA_TRACE_WARPS][ETA_T
 #define ETA_TRACE(ev)                                                                        \
   do {                                                                                       \
     const unsigned long long eta_t = (static_cast<unsigned long long>(clock64()) << 8) | (ev); \
-    if (blockIdx.x < ETA_TRACE_CTAS && (threadIdx.x % 32) == 0 && trace_n < ETA_TRACE_EVENTS) \
+    if (blockIdx.x < ETA_TRACE_CTAS && threadIdx.x / 32 < ETA_TRACE_WARPS && (threadIdx.x % 32) == 0 && \
+        trace_n < ETA_TRACE_EVENTS)                                                          \
       g_eta_trace[blockIdx.x][threadIdx.x / 32][trace_n] = eta_t;                            \
     ++trace_n;                                                                               \
   } while (0)
