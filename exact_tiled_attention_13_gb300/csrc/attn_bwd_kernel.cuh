@@ -11,27 +11,26 @@
 // recurrence).
 //
 // Three kernels, no atomics (the result is deterministic):
-//   prep : one warp per query row: Lp_i = LSE_i log2(e) (+inf for a row with no allowed
-//          key and for the padding rows up to a whole tile, so that their p is 0) and
-//          D_i = dO_i . O_i, into a caller workspace [BH][nq_tiles * 128] each.
+//   prep : a few lanes per query row: Lp_i = -LSE_i log2(e) (-inf for a row with no
+//          allowed key and for the padding rows up to a whole tile, so that their p is 0)
+//          and D_i = dO_i . O_i, into a caller workspace [BH][nq_tiles * 128] each.
 //   dkdv : one CTA per (head, 128-key tile j). Keeps K_j and V_j in shared memory and
 //          streams the query tiles i that see tile j (Q_i, dO_i and their Lp, D) through a
-//          ring of slots. Per 64-query half of a query tile, on the tensor cores with
-//          accumulators in tensor memory: S^T = K_j Q_h^T and dP^T = V_j dO_h^T; the
-//          elementwise warps (thread = key row = tensor-memory lane) form
-//          P^T = exp2(S^T scale log2e - Lp) and dS^T = P^T o (dP^T - D) in bf16 over S^T
-//          and dP^T; then dV_j += P^T dO_h and dK_j += dS^T Q_h. At the end dV_j and
-//          scale dK_j are written in fp32.
+//          ring of slots. Per query tile, on the tensor cores with accumulators in tensor
+//          memory: S^T = K_j Q_i^T and dP^T = V_j dO_i^T in two 128-column buffers that
+//          swap roles every tile; the elementwise warps (thread = key row = tensor-memory
+//          lane) form P^T = exp2(S^T scale log2e + Lp) and dS^T = P^T o (dP^T - D) in bf16,
+//          packed over S^T; then dV_j += P^T dO_i and dK_j += dS^T Q_i, while S^T of the
+//          next tile goes to the buffer dP^T left. At the end dV_j and scale dK_j are
+//          written in fp32.
 //   dq   : one CTA per (head, 128-query tile i). Keeps Q_i and dO_i, streams the K/V tiles
 //          the tile sees: S = Q_i K_t^T, dP = dO_i V_t^T, dS = P o (dP - D) in bf16 over
 //          S, dQ_i += dS K_t; at the end scale dQ_i in fp32. S is double-buffered, so
 //          the next tile's S and dP run on the tensor cores while dS is formed.
-// In dkdv the two 64-query halves of a tile have their own tensor-memory buffers: while
-// the elementwise warps work on one half, the tensor cores compute the other's S and dP.
-// Warp roles of dkdv and dq (12 warps): two elementwise warpgroups (each thread owns one
-// tensor-memory lane and half of the 128 columns), the MMA warp (whole warp, one elected
-// lane issues) and one TMA producer warp. Every wait is bounded (the forward kernel's
-// watchdog): a wait that runs out is recorded and the CTA drains and returns.
+// Warp roles: elementwise warps (16 in dkdv, 32 query columns each; 8 in dq, 64 key
+// columns each; each thread owns one tensor-memory lane), the MMA warp (whole warp, one
+// elected lane issues) and TMA producer warps. Every wait is bounded (the forward
+// kernel's watchdog): a wait that runs out is recorded and the CTA drains and returns.
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -117,11 +116,6 @@ __global__ void __launch_bounds__(256)
 // Bias sources of the backward kernels.
 enum { BWD_BIAS_NONE = 0, BWD_BIAS_DENSE = 1, BWD_BIAS_KEY = 2 };
 
-// Both main kernels work through 128-wide tiles in two halves of 64 columns (queries in
-// dkdv, keys in dq). Each half has its own score and dP buffers in tensor memory, so the
-// elementwise warps work on one half while the tensor cores compute the next half's
-// products: MMA order S/dP(u+1), then the accumulating products of u.
-constexpr int HALF = 64;
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 
 template <int D, int DV, bool CAUSAL, int BIAS>
@@ -179,9 +173,8 @@ struct BwdCfg {
   static constexpr int A_SMEM_TOTAL = A_SMEM > 120 * 1024 ? A_SMEM : 120 * 1024;
   static constexpr int B_SMEM_TOTAL = B_SMEM > 120 * 1024 ? B_SMEM : 120 * 1024;
 
-  // tensor memory: half b of the scores at S_COL + 64 b, of dP at DP_COL + 64 b
-  static constexpr int S_COL = 0;     // S^T (dkdv) or S (dq); P^T packed over it
-  static constexpr int DP_COL = 128;  // dP^T or dP; dS^T / dS packed over it
+  // tensor memory (dkdv): the two score buffers at S_COL and S_COL + 128, then dV and dK
+  static constexpr int S_COL = 0;
   static constexpr int ACC0_COL = 256;        // dV (dkdv) or dQ (dq)
   static constexpr int ACC1_COL = 256 + DV;   // dK (dkdv)
   static constexpr int TMEM_COLS = 512;
@@ -201,7 +194,6 @@ struct BwdCfg {
   static_assert(16 * 32 * ((D > DV ? D : DV) / 2 + 4) * 4 <= A_SLOT_OFF + A_QS * A_SLOT,
                 "dK/dV epilogue stage larger than the memory it reuses");
 
-  static constexpr uint32_t IDESC_HALF = idesc_bf16_f32(128, HALF, false);  // S, dP halves
   static constexpr uint32_t IDESC_SS = idesc_bf16_f32(128, 128, false);     // full-width S, dP
   static constexpr uint32_t IDESC_NV = idesc_bf16_f32(128, DV, true);       // dV += P^T dO
   static constexpr uint32_t IDESC_ND = idesc_bf16_f32(128, D, true);        // dK, dQ
@@ -212,19 +204,8 @@ struct BwdCfg {
 __device__ __forceinline__ uint32_t kmajor_step(int ks) {
   return static_cast<uint32_t>(((ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32) >> 4);
 }
-// Rows 64 h .. 64 h + 63 of a 128-row K-major box (eight 1024-byte groups of 8 rows).
-__device__ __forceinline__ uint32_t half_rows(int h) { return static_cast<uint32_t>((h * HALF * 128) >> 4); }
-// MN-major operand (contraction along rows): step ks of 16 rows, starting at row 64 h.
-__device__ __forceinline__ uint32_t mn_step(int h, int ks) {
-  return static_cast<uint32_t>(((h * HALF + ks * 16) * 128) >> 4);
-}
-// Packed bf16 A operand of half-buffer b for step ks (16 of its 64 columns): elementwise
-// warpgroup g owns columns [32 g, 32 g + 32) of the half and stores them, two per 32-bit
-// column, at [32 g, 32 g + 16) of the half's 64 columns.
-__device__ __forceinline__ uint32_t packed_col(int b, int ks) {
-  return static_cast<uint32_t>(HALF * b + 32 * (ks / 2) + 8 * (ks % 2));
-}
-
+// MN-major operand (contraction along rows): step ks of 16 rows.
+__device__ __forceinline__ uint32_t mn_step(int ks) { return static_cast<uint32_t>((ks * 16 * 128) >> 4); }
 // Loads a 32-column chunk of two tensor-memory matrices.
 __device__ __forceinline__ void ld_pair(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
                                         uint32_t (&b)[32]) {
@@ -522,7 +503,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::A_THREADS, 1)
       const uint64_t q_mn = smem_desc(slot_addr(t), SW_CHUNK_BYTES, 1024);
 #pragma unroll
       for (int ks = 0; ks < BM / 16; ++ks)
-        mma_ts_elect(tmem + CF::ACC0_COL, sb + 32 * (ks / 2) + 8 * (ks % 2), do_mn + mn_step(0, ks),
+        mma_ts_elect(tmem + CF::ACC0_COL, sb + 32 * (ks / 2) + 8 * (ks % 2), do_mn + mn_step(ks),
                      CF::IDESC_NV, (t > 0 || ks > 0) ? 1u : 0u);
       ok = wd.wait(BAR(CF::BAR_PFULL), t & 1, ROLE_MMA, CF::BAR_PFULL);
       if (!ok) break;
@@ -530,7 +511,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::A_THREADS, 1)
       ETA_TRACE(52);
 #pragma unroll
       for (int ks = 0; ks < BM / 16; ++ks)
-        mma_ts_elect(tmem + CF::ACC1_COL, sb + 16 + 32 * (ks / 2) + 8 * (ks % 2), q_mn + mn_step(0, ks),
+        mma_ts_elect(tmem + CF::ACC1_COL, sb + 16 + 32 * (ks / 2) + 8 * (ks % 2), q_mn + mn_step(ks),
                      CF::IDESC_ND, (t > 0 || ks > 0) ? 1u : 0u);
       mma_commit_elect(BAR(CF::BAR_EMPTY + (t % CF::A_QS)));
       if (t + 1 < n_it) issue_dp(t + 1);
