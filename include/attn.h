@@ -210,7 +210,7 @@ ATTN_API int attn_fwd_splitkv_static(const void *Q, const void *K, const void *V
  *   LSE      fp32 [BH][Nq], the forward pass's LSE (required here)
  *   dQ       fp32 [BH][Nq][d];  dK fp32 [BH][Nk][d];  dV fp32 [BH][Nk][d_v]  (outputs)
  *   workspace device memory of attn_bwd_workspace_bytes(BH, Nq) bytes, 16-byte aligned,
- *            for the per-row statistics (LSE in log2 units and D); overwritten
+ *            for the per-row statistics (-LSE in log2 units and D); overwritten
  * Alignment: Q, K, V, O, dO, C, dQ, dK, dV 16 bytes; LSE, ckey 4 bytes.
  * Aliasing: dQ, dK, dV and the workspace overlap no input and no other output.
  * Nq == 0 writes zeros to dK and dV; Nk == 0 with Nq >= 1 is rejected.
