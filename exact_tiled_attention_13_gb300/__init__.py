@@ -13,13 +13,14 @@ from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_ERR_CUDA, ATTN_ERR_DEVIC
                    ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_FAULT_NONE, ATTN_FAULT_SKIP_FIRST_K,
                    ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK, ATTN_OUT_BF16, ATTN_OUT_F32,
                    AttnError, attn_bwd_raw, attn_bwd_workspace_bytes, attn_device_status,
-                   attn_fwd_ex_raw, attn_fwd_raw,
+                   attn_fwd_ex_raw, attn_fwd_host_raw, attn_fwd_host_staging_bytes, attn_fwd_raw,
                    attn_fwd_splitkv_plan, attn_fwd_splitkv_raw, attn_set_fault_injection,
                    attn_set_wait_timeout_ns, attn_version, library_path, load, strerror)
 
 __all__ = [
     "attn_fwd", "attn_fwd_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "attn_fwd_splitkv",
-    "attn_fwd_splitkv_raw", "attn_fwd_splitkv_plan", "splitkv_workspace", "attn_bwd",
+    "attn_fwd_splitkv_raw", "attn_fwd_splitkv_plan", "splitkv_workspace", "attn_fwd_host",
+    "attn_fwd_host_raw", "attn_fwd_host_staging_bytes", "host_staging", "attn_bwd",
     "attn_bwd_raw", "attn_bwd_workspace_bytes", "bwd_workspace", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
     "attn_set_fault_injection", "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
     "ATTN_BIAS_DENSE", "ATTN_BIAS_KEY", "ATTN_OUT_BF16", "ATTN_OUT_F32",
@@ -155,6 +156,35 @@ def attn_fwd_splitkv(Q, K, V, mode, C, ckey, scale, O, LSE=None, workspace=None,
                                 out_dtype, lse_ptr, _stream_handle(stream))
     if code != ATTN_OK:
         raise AttnError(code, "attn_fwd_splitkv")
+    return O, LSE
+
+
+def host_staging(mode, BH, Nq, Nk, d, d_v, out_dtype, heads_per_chunk=0, device="cuda"):
+    """A device staging tensor (uint8) of the size attn_fwd_host needs."""
+    import torch
+
+    code, nbytes = attn_fwd_host_staging_bytes(mode, BH, Nq, Nk, d, d_v, out_dtype, heads_per_chunk)
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd_host_staging_bytes")
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def attn_fwd_host(Q, K, V, mode, C, ckey, scale, O, LSE=None, staging=None, heads_per_chunk=0,
+                  stream=None):
+    """attn_fwd_ex on host (CPU) tensors, streamed through the GPU in chunks of heads
+    (include/attn.h, attn_fwd_host). Q, K, V, C, ckey, O, LSE: contiguous CPU tensors with
+    the shapes and dtypes of attn_fwd_ex (page-locked for the copies to overlap); staging:
+    a CUDA tensor of at least attn_fwd_host_staging_bytes (see host_staging). The call is
+    asynchronous on `stream`."""
+    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE)
+    if staging is None or not staging.is_cuda or not staging.is_contiguous():
+        raise ValueError("staging must be a contiguous CUDA tensor (see host_staging)")
+    code = attn_fwd_host_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), mode, c_ptr, k_ptr, BH, Nq, Nk,
+                             d, dv, scale, O.data_ptr(), out_dtype, lse_ptr, staging.data_ptr(),
+                             staging.numel() * staging.element_size(), heads_per_chunk,
+                             _stream_handle(stream))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_fwd_host")
     return O, LSE
 
 

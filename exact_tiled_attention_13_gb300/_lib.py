@@ -24,7 +24,7 @@ ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_CUDA = -7
 ATTN_ERR_SCRATCH_LIMIT = -8
 ATTN_STATIC_SCRATCH_BYTES = 33554432
-ATTN_ABI_VERSION = 104
+ATTN_ABI_VERSION = 105
 
 ATTN_FAULT_NONE = 0
 ATTN_FAULT_SKIP_FIRST_K = 1
@@ -50,6 +50,13 @@ SIGNATURES = {
                                                ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_float, ctypes.c_int, _P,
                                                ctypes.c_int, _P, _P]),
+    "attn_fwd_host": (ctypes.c_int, [_P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P,
+                                     ctypes.c_int, _P, _P, ctypes.c_ulonglong, ctypes.c_int, _P]),
+    "attn_fwd_host_staging_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_ulonglong)]),
     "attn_bwd": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, ctypes.c_ulonglong,
@@ -139,6 +146,23 @@ def attn_fwd_splitkv_plan(mode, BH, Nq, Nk, d, d_v, n_splits=0):
     code = load().attn_fwd_splitkv_plan(int(mode), int(BH), int(Nq), int(Nk), int(d), int(d_v),
                                         int(n_splits), ctypes.byref(splits), ctypes.byref(nbytes))
     return code, splits.value, nbytes.value
+
+
+def attn_fwd_host_raw(Q, K, V, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, O, out_dtype, LSE, staging,
+                      staging_bytes, heads_per_chunk, stream) -> int:
+    """attn_fwd_host (host tensors streamed through a device staging buffer) with plain
+    integers as pointers; returns its code unchanged."""
+    return load().attn_fwd_host(Q, K, V, int(mode), C, ckey, int(BH), int(Nq), int(Nk), int(d),
+                                int(d_v), float(scale), O, int(out_dtype), LSE, staging,
+                                int(staging_bytes), int(heads_per_chunk), stream)
+
+
+def attn_fwd_host_staging_bytes(mode, BH, Nq, Nk, d, d_v, out_dtype, heads_per_chunk=0):
+    """(code, bytes) of the staging buffer attn_fwd_host needs."""
+    nbytes = ctypes.c_ulonglong(0)
+    code = load().attn_fwd_host_staging_bytes(int(mode), int(BH), int(Nq), int(Nk), int(d), int(d_v),
+                                              int(out_dtype), int(heads_per_chunk), ctypes.byref(nbytes))
+    return code, nbytes.value
 
 
 def attn_bwd_raw(Q, K, V, O, o_dtype, dO, LSE, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, dQ, dK,

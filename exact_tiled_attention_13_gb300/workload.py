@@ -61,6 +61,13 @@ class DeviceWorkload:
         self.LSE = torch.empty(w.BH, w.N, dtype=torch.float32, device=device)
         self.O_h = torch.empty(self.O.shape, dtype=odt).pin_memory()
         self.LSE_h = torch.empty(self.LSE.shape, dtype=torch.float32).pin_memory()
+        # The plain forward pass streams host tensors through attn_fwd_host end to end.
+        self.staging = None
+        if not w.split_kv and not w.backward:
+            import exact_tiled_attention_13_gb300 as eta
+
+            self.staging = eta.host_staging(w.mode, w.BH, w.N, w.Nkv, w.d, w.dv,
+                                            1 if w.out_dtype == "f32" else 0, device=device)
         if w.backward:
             import exact_tiled_attention_13_gb300 as eta
 
@@ -113,9 +120,16 @@ class DeviceWorkload:
         return sum(d.numel() * d.element_size() for d, _ in self._outputs())
 
     def end_to_end(self, stream):
-        """One call the way a host-side user makes it: pinned host inputs in, host outputs out."""
+        """One call the way a host-side user makes it: pinned host inputs in, host outputs out.
+        The plain forward pass is one attn_fwd_host call (uploads, kernels and downloads of
+        chunks of heads overlapped); the split and backward passes copy, launch and copy back."""
         import exact_tiled_attention_13_gb300 as eta
 
+        if self.staging is not None:
+            w = self.w
+            eta.attn_fwd_host(self.Q_h, self.K_h, self.V_h, w.mode, self.C_h, self.ck_h, w.scale,
+                              self.O_h, self.LSE_h, self.staging, stream=stream)
+            return
         for d, h in self._inputs():
             d.copy_(h, non_blocking=True)
         self.launch(stream)

@@ -25,9 +25,10 @@
  * factor 2^8 (any reference used consistently gives the same o_T / l_T), so o is
  * rescaled only then.
  *
- * All entry points are plain C, take device pointers and sizes, and never allocate
- * device memory. They are thread-safe: calls from several host threads or on several
- * streams may overlap.
+ * All entry points are plain C, take device pointers and sizes (attn_fwd_host: host tensors
+ * and a device staging buffer), and never allocate device memory (attn_fwd_host creates
+ * three streams and seven events per device on its first call). They are thread-safe:
+ * calls from several host threads or on several streams may overlap.
  */
 #ifndef EXACT_TILED_ATTENTION_13_ATTN_H
 #define EXACT_TILED_ATTENTION_13_ATTN_H
@@ -193,6 +194,53 @@ ATTN_API int attn_fwd_splitkv_static(const void *Q, const void *K, const void *V
                                      int out_dtype, float *LSE, void *stream);
 
 /*
+ * attn_fwd_host -- attn_fwd_ex on tensors that live in host memory (the pages have no
+ * counterpart: this is a way of feeding the forward pass, not a step of the method).
+ * Heads are independent, so the call cuts the BH heads into chunks and streams them:
+ * the upload of one chunk, the attention of the previous one and the download of the
+ * one before run at the same time, on three streams the library creates once per device,
+ * through two slots of a caller-provided device staging buffer.
+ *   Q, K, V, C, ckey  HOST pointers, the layouts and dtypes of attn_fwd_ex (C, ckey as the
+ *                     mode requires, else NULL). Page-locked memory lets the copies overlap
+ *                     the kernels; pageable memory works but the copies then serialise.
+ *   O, LSE            HOST pointers for the outputs (LSE may be NULL).
+ *   staging           device memory of the current device, 256-byte aligned, at least
+ *                     attn_fwd_host_staging_bytes(...) bytes, owned by the caller; its
+ *                     contents do not matter and are overwritten. It must not be used by
+ *                     anything else until the work of this call on `stream` completes.
+ *   staging_bytes     its size.
+ *   heads_per_chunk   heads per chunk, >= 0; 0 lets the library choose: about eight chunks,
+ *                     but at least as many heads as 128 blocks need (one block per 128
+ *                     queries with a dense bias, per 256 otherwise), so each launch fills
+ *                     the GPU.
+ *   stream            the caller's stream: the call's work starts after work already queued
+ *                     on it, and work queued on it afterwards waits for the last download.
+ * The call queues the work and returns (asynchronous, like attn_fwd_ex); the host outputs
+ * are complete when `stream` has reached the point after the call. The results are
+ * bit-identical to attn_fwd_ex on the same data (the same kernel per head). Host buffers
+ * must not be written, nor outputs read, until then. Calls are serialised on a mutex
+ * while they queue their work.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG (a device pointer where a host pointer belongs,
+ * overlapping host buffers, staging too small or misaligned, bad sizes or mode), or what
+ * attn_fwd_ex or the CUDA runtime returns; after an error some chunks may already have
+ * been queued and the outputs are unspecified.
+ */
+ATTN_API int attn_fwd_host(const void *Q, const void *K, const void *V, int mode, const float *C,
+                           const float *ckey, int BH, int Nq, int Nk, int d, int d_v, float scale,
+                           void *O, int out_dtype, float *LSE, void *staging,
+                           unsigned long long staging_bytes, int heads_per_chunk, void *stream);
+
+/*
+ * attn_fwd_host_staging_bytes -- the staging size attn_fwd_host needs for these
+ * arguments (two chunk slots of Q, K, V, the bias, O and LSE, each 256-byte aligned; one
+ * slot when everything fits one chunk). Makes no CUDA call. Returns ATTN_OK, or
+ * ATTN_ERR_INVALID_ARG (NULL bytes, bad sizes, mode or dtype, negative heads_per_chunk).
+ */
+ATTN_API int attn_fwd_host_staging_bytes(int mode, int BH, int Nq, int Nk, int d, int d_v,
+                                         int out_dtype, int heads_per_chunk,
+                                         unsigned long long *bytes);
+
+/*
  * attn_bwd -- gradients dQ, dK, dV of O = softmax(Q K^T * scale + C) V for a loss
  * gradient dO, on `stream`. They are the derivatives of the attn_fwd_ex operation:
  *     dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij = dO_i . O_i,
@@ -264,7 +312,7 @@ ATTN_API int attn_set_fault_injection(int fault);
 /* ABI version of this header (major * 100 + minor): 1.00 attn_fwd; 1.01 attn_fwd_ex;
  * 1.02 attn_fwd_splitkv, attn_fwd_splitkv_plan; 1.03 attn_fwd_splitkv_static;
  * 1.04 attn_bwd, attn_bwd_workspace_bytes. attn_version() returns the library's. */
-#define ATTN_ABI_VERSION 104
+#define ATTN_ABI_VERSION 105
 ATTN_API int attn_version(void);
 
 #ifdef __cplusplus

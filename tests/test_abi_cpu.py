@@ -63,7 +63,7 @@ def test_strerror_and_version():
     for code in range(-7, 1):
         assert eta.attn_strerror(code)
     assert "unknown" in eta.attn_strerror(-99)
-    assert eta.attn_version() == _lib.ATTN_ABI_VERSION == 104
+    assert eta.attn_version() == _lib.ATTN_ABI_VERSION == 105
 
 
 def test_timeout_setting_roundtrip():
@@ -247,3 +247,57 @@ def test_bwd_unsupported_width_and_empty():
 def test_valid_bwd_call_without_gpu_reports_no_device():
     assert call_bwd() == eta.ATTN_ERR_NO_DEVICE
     assert call_bwd(Nq=0, Q=None, O=None, dO=None, LSE=None, dQ=None, workspace=None) == eta.ATTN_ERR_NO_DEVICE
+
+
+# ---------------------------------------------------------------- host-streamed forward
+def test_host_staging_bytes():
+    MiB = 1 << 20
+    # 64 heads of 8192 x 128 (bf16 O): chunks of 8 heads (32 blocks a head);
+    # a slot holds Q, K, V, O (16 MiB each at 8 heads) and LSE (256 KiB); two slots.
+    code, nbytes = eta.attn_fwd_host_staging_bytes(1, 64, 8192, 8192, 128, 128, 0)
+    assert code == eta.ATTN_OK and nbytes == 2 * (4 * 16 * MiB + 256 * 1024)
+    # 8 heads of 4096 (16 blocks a head): one chunk of all 8 heads, one slot.
+    code, nbytes = eta.attn_fwd_host_staging_bytes(4, 8, 4096, 4096, 64, 128, 1)
+    parts = [8 * 4096 * 64 * 2, 8 * 4096 * 64 * 2, 8 * 4096 * 128 * 2, 0, 8 * 4096 * 4, 8 * 4096 * 128 * 4, 8 * 4096 * 4]
+    assert code == eta.ATTN_OK and nbytes == sum(parts)
+    # 16 heads of 16384 (64 blocks a head): chunks of 2 heads (128 blocks).
+    code, nbytes = eta.attn_fwd_host_staging_bytes(0, 16, 16384, 16384, 128, 128, 1)
+    assert code == eta.ATTN_OK and nbytes == 2 * 2 * 16384 * (3 * 128 * 2 + 128 * 4 + 4)
+    # 64 heads of 2048 (8 blocks a head): chunks of 16 heads.
+    code, nbytes = eta.attn_fwd_host_staging_bytes(1, 64, 2048, 2048, 128, 128, 0)
+    assert code == eta.ATTN_OK and nbytes == 2 * 16 * 2048 * (4 * 128 * 2 + 4)
+    # One chunk (every head at once): one slot, each part rounded up to 256 bytes: Q 384,
+    # K 640, V 640, O 768 (fp32), LSE 12 bytes.
+    code, nbytes = eta.attn_fwd_host_staging_bytes(0, 1, 3, 5, 64, 64, 1)
+    assert code == eta.ATTN_OK and nbytes == 512 + 768 + 768 + 768 + 256
+    # Dense bias and fp32 O, chunks of 3 heads of BH = 7: C is 3 x 10 x 20 x 4 bytes.
+    code, nbytes = eta.attn_fwd_host_staging_bytes(2, 7, 10, 20, 64, 128, 1, 3)
+    parts = [3 * 10 * 64 * 2, 3 * 20 * 64 * 2, 3 * 20 * 128 * 2, 3 * 10 * 20 * 4, 0, 3 * 10 * 128 * 4, 3 * 10 * 4]
+    assert code == eta.ATTN_OK and nbytes == 2 * sum((x + 255) // 256 * 256 for x in parts)
+    for bad in (dict(mode=8), dict(mode=6), dict(BH=0), dict(out_dtype=2), dict(heads_per_chunk=-1)):
+        a = dict(mode=0, BH=2, Nq=4, Nk=4, d=64, d_v=64, out_dtype=0, heads_per_chunk=0)
+        a.update(bad)
+        assert eta.attn_fwd_host_staging_bytes(*a.values())[0] == eta.ATTN_ERR_INVALID_ARG
+    assert eta.attn_fwd_host_staging_bytes(0, 2, 4, 4, 96, 64, 0)[0] == eta.ATTN_ERR_UNSUPPORTED
+
+
+def call_host(**over):
+    a = dict(Q=QP, K=KP, V=VP, mode=0, C=None, ckey=None, BH=2, Nq=48, Nk=64, d=64, d_v=64,
+             scale=0.125, O=OP, out_dtype=1, LSE=LP, staging=0xF00000, staging_bytes=1 << 24,
+             heads_per_chunk=0, stream=None)
+    a.update(over)
+    return eta.attn_fwd_host_raw(*a.values())
+
+
+@pytest.mark.parametrize("over", [
+    dict(mode=8), dict(Nk=0), dict(Q=None), dict(O=None), dict(staging=None), dict(staging_bytes=16),
+    dict(staging=0xF00010), dict(mode=2), dict(mode=0, C=CP), dict(mode=4), dict(scale=0.0),
+    dict(heads_per_chunk=-2), dict(O=QP + 64),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_invalid_arguments_host(over):
+    assert call_host(**over) == eta.ATTN_ERR_INVALID_ARG
+
+
+def test_host_zero_queries_is_noop_and_widths():
+    assert call_host(Nq=0, Q=None, O=None, LSE=None, staging=None) == eta.ATTN_OK
+    assert call_host(d=96) == eta.ATTN_ERR_UNSUPPORTED
