@@ -12,7 +12,8 @@ from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_ERR_CUDA, ATTN_ERR_DEVIC
                    ATTN_ERR_LAUNCH, ATTN_ERR_NO_DEVICE, ATTN_ERR_UNSUPPORTED,
                    ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_FAULT_NONE, ATTN_FAULT_SKIP_FIRST_K,
                    ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK, ATTN_OUT_BF16, ATTN_OUT_F32,
-                   AttnError, attn_bwd_raw, attn_bwd_workspace_bytes, attn_device_status,
+                   AttnError, attn_bwd_host_raw, attn_bwd_host_staging_bytes, attn_bwd_raw,
+                   attn_bwd_workspace_bytes, attn_device_status,
                    attn_fwd_ex_raw, attn_fwd_host_raw, attn_fwd_host_staging_bytes, attn_fwd_raw,
                    attn_fwd_splitkv_plan, attn_fwd_splitkv_raw, attn_set_fault_injection,
                    attn_set_wait_timeout_ns, attn_version, library_path, load, strerror)
@@ -20,7 +21,8 @@ from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_ERR_CUDA, ATTN_ERR_DEVIC
 __all__ = [
     "attn_fwd", "attn_fwd_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "attn_fwd_splitkv",
     "attn_fwd_splitkv_raw", "attn_fwd_splitkv_plan", "splitkv_workspace", "attn_fwd_host",
-    "attn_fwd_host_raw", "attn_fwd_host_staging_bytes", "host_staging", "attn_bwd",
+    "attn_fwd_host_raw", "attn_fwd_host_staging_bytes", "host_staging", "attn_bwd_host",
+    "attn_bwd_host_raw", "attn_bwd_host_staging_bytes", "bwd_host_staging", "attn_bwd",
     "attn_bwd_raw", "attn_bwd_workspace_bytes", "bwd_workspace", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
     "attn_set_fault_injection", "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
     "ATTN_BIAS_DENSE", "ATTN_BIAS_KEY", "ATTN_OUT_BF16", "ATTN_OUT_F32",
@@ -220,4 +222,41 @@ def attn_bwd(Q, K, V, O, dO, LSE, mode, C, ckey, scale, dQ, dK, dV, workspace, s
                         workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if code != ATTN_OK:
         raise AttnError(code, "attn_bwd")
+    return dQ, dK, dV
+
+
+def bwd_host_staging(mode, BH, Nq, Nk, d, d_v, o_dtype, heads_per_chunk=0, device="cuda"):
+    """A device staging tensor (uint8) of the size attn_bwd_host needs."""
+    import torch
+
+    code, nbytes = attn_bwd_host_staging_bytes(mode, BH, Nq, Nk, d, d_v, o_dtype, heads_per_chunk)
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_bwd_host_staging_bytes")
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def attn_bwd_host(Q, K, V, O, dO, LSE, mode, C, ckey, scale, dQ, dK, dV, staging, heads_per_chunk=0,
+                  stream=None):
+    """attn_bwd on host (CPU) tensors, streamed through the GPU in chunks of heads
+    (include/attn.h, attn_bwd_host); the arguments of attn_bwd, all on the CPU, plus a CUDA
+    staging tensor (see bwd_host_staging). Asynchronous on `stream`."""
+    import torch
+
+    for name, t in (("Q", Q), ("K", K), ("V", V), ("O", O), ("dO", dO), ("LSE", LSE), ("dQ", dQ),
+                    ("dK", dK), ("dV", dV)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    if staging is None or not staging.is_cuda or not staging.is_contiguous():
+        raise ValueError("staging must be a contiguous CUDA tensor (see bwd_host_staging)")
+    BH, Nq, d = Q.shape
+    Nk, dv = K.shape[1], V.shape[2]
+    o_dtype = ATTN_OUT_F32 if O.dtype == torch.float32 else ATTN_OUT_BF16
+    code = attn_bwd_host_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), o_dtype,
+                             dO.data_ptr(), LSE.data_ptr(), mode,
+                             None if C is None else C.data_ptr(), None if ckey is None else ckey.data_ptr(),
+                             BH, Nq, Nk, d, dv, scale, dQ.data_ptr(), dK.data_ptr(), dV.data_ptr(),
+                             staging.data_ptr(), staging.numel() * staging.element_size(), heads_per_chunk,
+                             _stream_handle(stream))
+    if code != ATTN_OK:
+        raise AttnError(code, "attn_bwd_host")
     return dQ, dK, dV

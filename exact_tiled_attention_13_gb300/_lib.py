@@ -24,7 +24,7 @@ ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_CUDA = -7
 ATTN_ERR_SCRATCH_LIMIT = -8
 ATTN_STATIC_SCRATCH_BYTES = 33554432
-ATTN_ABI_VERSION = 105
+ATTN_ABI_VERSION = 106
 
 ATTN_FAULT_NONE = 0
 ATTN_FAULT_SKIP_FIRST_K = 1
@@ -54,6 +54,14 @@ SIGNATURES = {
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, _P,
                                      ctypes.c_int, _P, _P, ctypes.c_ulonglong, ctypes.c_int, _P]),
     "attn_fwd_host_staging_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_int,
+                                                   ctypes.POINTER(ctypes.c_ulonglong)]),
+    "attn_bwd_host": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, _P, _P, ctypes.c_int, _P, _P,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_float, _P, _P, _P, _P, ctypes.c_ulonglong,
+                                     ctypes.c_int, _P]),
+    "attn_bwd_host_staging_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_int,
                                                    ctypes.POINTER(ctypes.c_ulonglong)]),
@@ -171,6 +179,23 @@ def attn_bwd_raw(Q, K, V, O, o_dtype, dO, LSE, mode, C, ckey, BH, Nq, Nk, d, d_v
     return load().attn_bwd(Q, K, V, O, int(o_dtype), dO, LSE, int(mode), C, ckey, int(BH), int(Nq),
                            int(Nk), int(d), int(d_v), float(scale), dQ, dK, dV, workspace,
                            int(workspace_bytes), stream)
+
+
+def attn_bwd_host_raw(Q, K, V, O, o_dtype, dO, LSE, mode, C, ckey, BH, Nq, Nk, d, d_v, scale, dQ,
+                      dK, dV, staging, staging_bytes, heads_per_chunk, stream) -> int:
+    """attn_bwd_host (host tensors streamed through a device staging buffer) with plain
+    integers as pointers; returns its code unchanged."""
+    return load().attn_bwd_host(Q, K, V, O, int(o_dtype), dO, LSE, int(mode), C, ckey, int(BH),
+                                int(Nq), int(Nk), int(d), int(d_v), float(scale), dQ, dK, dV, staging,
+                                int(staging_bytes), int(heads_per_chunk), stream)
+
+
+def attn_bwd_host_staging_bytes(mode, BH, Nq, Nk, d, d_v, o_dtype, heads_per_chunk=0):
+    """(code, bytes) of the staging buffer attn_bwd_host needs."""
+    nbytes = ctypes.c_ulonglong(0)
+    code = load().attn_bwd_host_staging_bytes(int(mode), int(BH), int(Nq), int(Nk), int(d), int(d_v),
+                                              int(o_dtype), int(heads_per_chunk), ctypes.byref(nbytes))
+    return code, nbytes.value
 
 
 def attn_bwd_workspace_bytes(BH, Nq):

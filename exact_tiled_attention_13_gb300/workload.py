@@ -85,6 +85,9 @@ class DeviceWorkload:
                             for t in (self.dQ, self.dK, self.dV)]
             self.workspace = eta.bwd_workspace(w.BH, w.N, device=device)
             self.launches_per_step = 3
+            # End to end the backward pass streams host tensors through attn_bwd_host.
+            self.bwd_staging = eta.bwd_host_staging(w.mode, w.BH, w.N, w.Nkv, w.d, w.dv,
+                                                    1 if w.out_dtype == "f32" else 0, device=device)
 
     def launch(self, stream=None):
         import exact_tiled_attention_13_gb300 as eta
@@ -121,14 +124,20 @@ class DeviceWorkload:
 
     def end_to_end(self, stream):
         """One call the way a host-side user makes it: pinned host inputs in, host outputs out.
-        The plain forward pass is one attn_fwd_host call (uploads, kernels and downloads of
-        chunks of heads overlapped); the split and backward passes copy, launch and copy back."""
+        The plain forward and the backward pass are one attn_fwd_host / attn_bwd_host call
+        (uploads, kernels and downloads of chunks of heads overlapped); the split pass copies,
+        launches and copies back."""
         import exact_tiled_attention_13_gb300 as eta
 
+        w = self.w
         if self.staging is not None:
-            w = self.w
             eta.attn_fwd_host(self.Q_h, self.K_h, self.V_h, w.mode, self.C_h, self.ck_h, w.scale,
                               self.O_h, self.LSE_h, self.staging, stream=stream)
+            return
+        if w.backward:
+            eta.attn_bwd_host(self.Q_h, self.K_h, self.V_h, self.O_h, self.dO_h, self.LSE_h, w.mode,
+                              self.C_h, self.ck_h, w.scale, *self.grads_h, self.bwd_staging,
+                              stream=stream)
             return
         for d, h in self._inputs():
             d.copy_(h, non_blocking=True)

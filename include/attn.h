@@ -25,9 +25,10 @@
  * factor 2^8 (any reference used consistently gives the same o_T / l_T), so o is
  * rescaled only then.
  *
- * All entry points are plain C, take device pointers and sizes (attn_fwd_host: host tensors
- * and a device staging buffer), and never allocate device memory (attn_fwd_host creates
- * three streams and seven events per device on its first call). They are thread-safe:
+ * All entry points are plain C, take device pointers and sizes (attn_fwd_host and
+ * attn_bwd_host: host tensors and a device staging buffer), and never allocate device
+ * memory (the host-streaming calls create three streams and seven events per device on
+ * their first call). They are thread-safe:
  * calls from several host threads or on several streams may overlap.
  */
 #ifndef EXACT_TILED_ATTENTION_13_ATTN_H
@@ -275,6 +276,30 @@ ATTN_API int attn_bwd(const void *Q, const void *K, const void *V, const void *O
  * x 4 bytes. Returns ATTN_OK, or ATTN_ERR_INVALID_ARG (BH < 1, Nq < 0, NULL bytes). */
 ATTN_API int attn_bwd_workspace_bytes(int BH, int Nq, unsigned long long *bytes);
 
+/*
+ * attn_bwd_host -- attn_bwd on tensors that live in host memory, streamed through the GPU
+ * in chunks of heads like attn_fwd_host (no counterpart on the pages either).
+ *   Q, K, V, O, dO, LSE, C, ckey  HOST pointers, the layouts and dtypes of attn_bwd.
+ *   dQ, dK, dV        HOST pointers for the fp32 gradients.
+ *   staging, staging_bytes, heads_per_chunk, stream  as for attn_fwd_host, with the size
+ *                     from attn_bwd_host_staging_bytes (the chunks also hold each one's
+ *                     row-statistics workspace). By default a chunk holds about an eighth
+ *                     of the heads, but at least as many as 128 blocks need (one block per
+ *                     128-query or 128-key tile, whichever count is larger).
+ * Asynchronous on `stream` like attn_bwd; the gradients are bit-identical to attn_bwd's.
+ * Returns what attn_fwd_host returns for the same kinds of error, or what attn_bwd returns.
+ */
+ATTN_API int attn_bwd_host(const void *Q, const void *K, const void *V, const void *O, int o_dtype,
+                           const void *dO, const float *LSE, int mode, const float *C,
+                           const float *ckey, int BH, int Nq, int Nk, int d, int d_v, float scale,
+                           float *dQ, float *dK, float *dV, void *staging,
+                           unsigned long long staging_bytes, int heads_per_chunk, void *stream);
+
+/* attn_bwd_host_staging_bytes -- the staging size attn_bwd_host needs; no CUDA call. */
+ATTN_API int attn_bwd_host_staging_bytes(int mode, int BH, int Nq, int Nk, int d, int d_v,
+                                         int o_dtype, int heads_per_chunk,
+                                         unsigned long long *bytes);
+
 /* Static English text for a return code (never NULL). */
 ATTN_API const char *attn_strerror(int code);
 
@@ -312,7 +337,7 @@ ATTN_API int attn_set_fault_injection(int fault);
 /* ABI version of this header (major * 100 + minor): 1.00 attn_fwd; 1.01 attn_fwd_ex;
  * 1.02 attn_fwd_splitkv, attn_fwd_splitkv_plan; 1.03 attn_fwd_splitkv_static;
  * 1.04 attn_bwd, attn_bwd_workspace_bytes. attn_version() returns the library's. */
-#define ATTN_ABI_VERSION 105
+#define ATTN_ABI_VERSION 106
 ATTN_API int attn_version(void);
 
 #ifdef __cplusplus

@@ -63,7 +63,7 @@ def test_strerror_and_version():
     for code in range(-7, 1):
         assert eta.attn_strerror(code)
     assert "unknown" in eta.attn_strerror(-99)
-    assert eta.attn_version() == _lib.ATTN_ABI_VERSION == 105
+    assert eta.attn_version() == _lib.ATTN_ABI_VERSION == 106
 
 
 def test_timeout_setting_roundtrip():
@@ -301,3 +301,38 @@ def test_invalid_arguments_host(over):
 def test_host_zero_queries_is_noop_and_widths():
     assert call_host(Nq=0, Q=None, O=None, LSE=None, staging=None) == eta.ATTN_OK
     assert call_host(d=96) == eta.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_host_staging_bytes():
+    # 64 heads of 2048 (16 query and 16 key tiles): chunks of 8 heads, two slots; per head
+    # Q, K, V, O (bf16), dO 512 KiB each, LSE 8 KiB, dQ, dK, dV 1 MiB each, workspace 16 KiB.
+    code, nbytes = eta.attn_bwd_host_staging_bytes(1, 64, 2048, 2048, 128, 128, 0)
+    per_head = 5 * 512 * 1024 + 8 * 1024 + 3 * 1024 * 1024 + 16 * 1024
+    assert code == eta.ATTN_OK and nbytes == 2 * 8 * per_head
+    for bad in (dict(mode=8), dict(BH=0), dict(o_dtype=2), dict(heads_per_chunk=-1), dict(Nq=-1)):
+        a = dict(mode=0, BH=2, Nq=4, Nk=4, d=64, d_v=64, o_dtype=0, heads_per_chunk=0)
+        a.update(bad)
+        assert eta.attn_bwd_host_staging_bytes(*a.values())[0] == eta.ATTN_ERR_INVALID_ARG
+    assert eta.attn_bwd_host_staging_bytes(0, 2, 4, 4, 64, 96, 0)[0] == eta.ATTN_ERR_UNSUPPORTED
+
+
+def call_bwd_host(**over):
+    a = dict(Q=QP, K=KP, V=VP, O=OP, o_dtype=1, dO=0xA00000, LSE=LP, mode=0, C=None, ckey=None,
+             BH=2, Nq=48, Nk=64, d=64, d_v=64, scale=0.125, dQ=0xB00000, dK=0xC00000,
+             dV=0xD00000, staging=0xF00000, staging_bytes=1 << 24, heads_per_chunk=0, stream=None)
+    a.update(over)
+    return eta.attn_bwd_host_raw(*a.values())
+
+
+@pytest.mark.parametrize("over", [
+    dict(mode=8), dict(Nk=0), dict(K=None), dict(dV=None), dict(LSE=None), dict(dQ=None),
+    dict(staging=None), dict(staging_bytes=16), dict(staging=0xF00040), dict(mode=2), dict(mode=4),
+    dict(scale=-1.0), dict(dQ=QP + 16),
+], ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_invalid_arguments_bwd_host(over):
+    assert call_bwd_host(**over) == eta.ATTN_ERR_INVALID_ARG
+
+
+def test_bwd_host_empty_and_widths():
+    assert call_bwd_host(Nq=0, Nk=0) == eta.ATTN_OK
+    assert call_bwd_host(d=96) == eta.ATTN_ERR_UNSUPPORTED

@@ -1,6 +1,7 @@
-"""attn_fwd_host on the GPU: host tensors streamed through a device staging buffer in chunks
-of heads. Every head runs the same kernel as attn_fwd_ex, so the host outputs must equal
-attn_fwd_ex's bit for bit; attn_fwd_ex itself is checked against the oracle elsewhere."""
+"""attn_fwd_host and attn_bwd_host on the GPU: host tensors streamed through a device
+staging buffer in chunks of heads. Every head runs the same kernels as attn_fwd_ex and
+attn_bwd, so the host outputs must equal theirs bit for bit; those calls themselves are
+checked against the oracle elsewhere."""
 import numpy as np
 import pytest
 
@@ -124,3 +125,44 @@ def test_device_pointer_where_host_belongs_is_rejected():
                                  64, 64, 0.125, O.data_ptr(), 1, None, staging.data_ptr(),
                                  staging.numel(), 0, torch.cuda.current_stream().cuda_stream)
     assert code == eta.ATTN_ERR_INVALID_ARG
+
+
+# (BH, Nq, Nk, d, dv, mode, o_f32, p_mask, heads_per_chunk)
+BWD_CASES = [
+    (5, 256, 256, 128, 128, CAUSAL, False, 0.0, 2),
+    (3, 200, 333, 64, 128, CAUSAL | DENSE, True, 0.2, 1),
+    (4, 130, 257, 128, 64, KEY, True, 0.3, 0),
+    (2, 333, 200, 64, 64, CAUSAL, True, 0.0, 1),   # rows with no allowed key
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: f"bh{c[0]}-nq{c[1]}-nk{c[2]}-d{c[3]}-dv{c[4]}-"
+                         f"{synth.MODE_NAMES[c[5]]}-h{c[8]}")
+def test_bwd_host_stream_equals_device_call(case):
+    import torch
+
+    import exact_tiled_attention_13_gb300 as eta
+
+    BH, Nq, Nk, d, dv, mode, o_f32, pm, hpc = case
+    c = synth.random_case_ex(9400 + BH + Nq + Nk, BH, Nq, Nk, d, dv, mode, 1.0, pm)
+    Q, K, V, C, ck = host_tensors(c)
+    dO = torch.from_numpy(synth.bf16_tensor(9500 + Nq, (BH, Nq, dv)).view(np.int16)).view(torch.bfloat16).pin_memory()
+    cuda = lambda t: None if t is None else t.cuda()
+    # Forward on the device for O and LSE.
+    odt = torch.float32 if o_f32 else torch.bfloat16
+    O_d = torch.empty((BH, Nq, dv), dtype=odt, device="cuda")
+    L_d = torch.empty((BH, Nq), device="cuda")
+    eta.attn_fwd_ex(cuda(Q), cuda(K), cuda(V), mode, cuda(C), cuda(ck), c["scale"], O_d, L_d)
+    O_h, L_h = O_d.cpu().pin_memory(), L_d.cpu().pin_memory()
+    grads_h = [torch.full(s, float("nan")).pin_memory() for s in ((BH, Nq, d), (BH, Nk, d), (BH, Nk, dv))]
+    staging = eta.bwd_host_staging(mode, BH, Nq, Nk, d, dv, 1 if o_f32 else 0, hpc)
+    eta.attn_bwd_host(Q, K, V, O_h, dO, L_h, mode, C, ck, c["scale"], *grads_h, staging, hpc)
+    torch.cuda.current_stream().synchronize()
+    grads_d = [torch.empty(g.shape, device="cuda") for g in grads_h]
+    ws = eta.bwd_workspace(BH, Nq)
+    eta.attn_bwd(cuda(Q), cuda(K), cuda(V), O_d, cuda(dO), L_d, mode, cuda(C), cuda(ck), c["scale"], *grads_d, ws)
+    torch.cuda.synchronize()
+    code, word = eta.attn_device_status(None)
+    assert code == eta.ATTN_OK, f"watchdog {word:#x}"
+    for name, gh, gd in zip(("dQ", "dK", "dV"), grads_h, grads_d):
+        assert torch.equal(gh, gd.cpu()), f"{name} differs from attn_bwd"
