@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import tempfile
@@ -199,11 +200,19 @@ def measured_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """The source without comments, trailing spaces and blank lines: what the compiler sees,
+    so that a comment edit does not retire a profile of unchanged code."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", line).rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def kernel_source_sha(kind: str = "forward") -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "exact_tiled_attention_13_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "exact_tiled_attention_13_gb300", "csrc", name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

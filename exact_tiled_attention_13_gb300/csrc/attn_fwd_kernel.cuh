@@ -15,7 +15,8 @@
 //     Reads its row of S from tensor memory, masks, takes the tile max b_t, the new
 //     exponent reference and alpha_t, writes P as bf16 back over S, rescales its row of o
 //     in tensor memory when the reference moves (rarely: see RESCALE_TAU), accumulates
-//     l_t, and at the end writes O = o/l and LSE.
+//     l_t, and at the end writes O = o/l (staged through its idle Q tile so the stores
+//     write whole 128-byte row segments) and LSE.
 //   control warpgroup, one thread per copy role:
 //     MMA (whole warp, one elected lane issues): S_q = Q_q K_t^T (A and B from shared
 //       memory) and o_q += P_q V_t (A = P from tensor memory, B = V from shared memory)
@@ -23,7 +24,10 @@
 //     Q/K load, V load: TMA copies of Q once and of K_t, V_t into rings of shared-memory
 //       slots guarded by full/empty mbarrier pairs (AI Infra ch. 5, Fig. 5-5: producer
 //       copies, consumer computes, one full and one empty barrier per slot).
-//     bias load (dense bias only): TMA copies of 128 x 32 fp32 bias chunks.
+//     bias load: TMA copies of 128 x 32 fp32 dense-bias chunks, or the whole warp copying
+//       each K/V tile's 128 per-key biases (scaled by log2(e)) into a small ring.
+//   After its last K copy the Q/K warp prefetches into L2 the Q tiles of the block one
+//   SM count ahead, the one the hardware is likely to start next on a freed SM.
 // Causal tiles above the diagonal are never loaded or multiplied; tiles are visited
 // from the diagonal down so each row meets an allowed key in its first tile.
 //
