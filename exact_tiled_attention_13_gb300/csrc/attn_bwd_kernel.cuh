@@ -69,6 +69,8 @@ __global__ void __launch_bounds__(256)
                          const float *__restrict__ LSE, int BH, int Nq, int nqp, float *Lp,
                          float *Dd) {
   constexpr int LPR = DV / 8;  // lanes per row
+  grid_dep_wait();  // O and LSE may come from the forward kernel just before
+  if (threadIdx.x == 0) grid_dep_launch();
   const long long prow = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / LPR;
   const int sub = threadIdx.x % LPR;
   const bool in = prow < static_cast<long long>(BH) * nqp;
@@ -316,6 +318,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::A_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
+  // Set-up done: wait for the previous kernel on the stream (programmatic launch) before any
+  // global memory is touched, and let the next one start launching.
+  grid_dep_wait();
+  if (threadIdx.x == 0) grid_dep_launch();
 
   if (warp < CF::A_EW_WARPS) {
     // ============================================================ elementwise
@@ -653,6 +659,10 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
+  // Set-up done: wait for the previous kernel on the stream (programmatic launch) before any
+  // global memory is touched, and let the next one start launching.
+  grid_dep_wait();
+  if (threadIdx.x == 0) grid_dep_launch();
 
   if (warp < 8) {
     // ============================================================ elementwise
@@ -886,10 +896,10 @@ cudaError_t launch_bwd(const BwdLaunchArgs &a) {
   if (e != cudaSuccess) return e;
   const unsigned grid_a = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.nkv_tiles);
   const unsigned grid_b = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.nq_tiles);
-  ka<<<grid_a, CF::A_THREADS, CF::A_SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  kb<<<grid_b, CF::THREADS, CF::B_SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
-  return cudaGetLastError();
+  e = launch_pdl(ka, dim3(grid_a), dim3(CF::A_THREADS), CF::A_SMEM_TOTAL, a.stream, a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
+  if (e != cudaSuccess || (e = cudaGetLastError()) != cudaSuccess) return e;
+  e = launch_pdl(kb, dim3(grid_b), dim3(CF::THREADS), CF::B_SMEM_TOTAL, a.stream, a.tmQ, a.tmK, a.tmV, a.tmdO, a.p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int DV>
@@ -897,9 +907,9 @@ cudaError_t launch_bwd_prep(const void *O, int out_f32, const uint16_t *dO, cons
                             int BH, int Nq, int nqp, float *Lp, float *Dd, cudaStream_t stream) {
   const long long rows = static_cast<long long>(BH) * nqp;
   const long long blocks = (rows * (DV / 8) + 255) / 256;
-  attn_bwd_prep_kernel<DV><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(O, out_f32, dO, LSE, BH,
-                                                                             Nq, nqp, Lp, Dd);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(attn_bwd_prep_kernel<DV>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                                   stream, O, out_f32, dO, LSE, BH, Nq, nqp, Lp, Dd);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace eta

@@ -389,6 +389,10 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
+  // Set-up done: now wait for the previous kernel on the stream (programmatic launch) before
+  // any global memory is touched, and let the next one start launching.
+  grid_dep_wait();
+  if (threadIdx.x == 0) grid_dep_launch();
 
   if (warp < CF::CTRL_WARP0) {
     // ================================================================ softmax
@@ -976,8 +980,8 @@ cudaError_t launch_attn(const LaunchArgs &a) {
   }
   const unsigned grid = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ctas_per_head) *
                         static_cast<unsigned>(a.p.n_splits);
-  kern<<<grid, CF::THREADS, CF::SMEM_TOTAL, a.stream>>>(a.tmQ, a.tmK, a.tmV, a.tmC, a.p);
-  return cudaGetLastError();
+  e = launch_pdl(kern, dim3(grid), dim3(CF::THREADS), CF::SMEM_TOTAL, a.stream, a.tmQ, a.tmK, a.tmV, a.tmC, a.p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace eta

@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(DV)
                       int n_splits, long long rows, void *O, int out_f32, float *LSE) {
   const long long row = blockIdx.x;
   const int col = threadIdx.x;
+  grid_dep_wait();  // the attention kernel's partials
+  if (col == 0) grid_dep_launch();
 
   // The ranges' loads are independent and issued in batches of 32, so for up to 32
   // ranges each pass is one memory round trip (the partials usually come from DRAM).
@@ -84,9 +86,9 @@ template <int DV>
 cudaError_t launch_merge(const float *O_part, const float *L_part, int n_splits, long long rows,
                          void *O, int out_f32, float *LSE, cudaStream_t stream) {
   if (rows > 0x7FFFFFFFll) return cudaErrorInvalidValue;  // one block per row
-  attn_merge_kernel<DV><<<static_cast<unsigned>(rows), DV, 0, stream>>>(O_part, L_part, n_splits,
-                                                                         rows, O, out_f32, LSE);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(attn_merge_kernel<DV>, dim3(static_cast<unsigned>(rows)), dim3(DV), 0, stream,
+                                   O_part, L_part, n_splits, rows, O, out_f32, LSE);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace eta

@@ -95,6 +95,31 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int x, int 
                : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream serialization
+// may start while the previous kernel on the stream is still running; it must not touch
+// global memory before grid_dep_wait(), which returns once that kernel has completed and
+// its writes are visible (at once when there is no such kernel). grid_dep_launch() lets
+// the next such kernel start launching once every block of this one has issued it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launches `kernel` with programmatic stream serialization (see grid_dep_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Number of SM identifiers of the device (at least the number of SMs).
 __device__ __forceinline__ unsigned nsmid() {
   unsigned n;
