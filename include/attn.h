@@ -2,8 +2,8 @@
  * attn.h -- C ABI of the exact tiled attention forward pass for NVIDIA GB300 (sm_103a).
  *
  * The operation is exact scaled dot-product attention for B*H independent heads,
- * as defined in "Compilers and kernels" (aaai.latere.ai/zh/infrastructure/
- * compilers-kernels), section "FlashAttention rewrites the algorithm around IO",
+ * as defined in "Compilers and kernels", section "FlashAttention rewrites the algorithm
+ * around IO",
  * first display and its symbol list:
  *
  *     S = Q K^T * scale + C,  m_i = max_j S_ij,  l_i = sum_j exp(S_ij - m_i),

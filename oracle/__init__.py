@@ -6,8 +6,8 @@ import this package. The CUDA product path never does. The arithmetic lives in
 and P materialised), compiled here with gcc on first use; this module only
 marshals numpy arrays.
 
-Definition followed: "Compilers and kernels" (aaai.latere.ai/zh/infrastructure/
-compilers-kernels), section "FlashAttention rewrites the algorithm around IO":
+Definition followed: "Compilers and kernels", section "FlashAttention rewrites the
+algorithm around IO":
 S = Q K^T * scale + C, m_i = max_j S_ij, l_i = sum_j exp(S_ij - m_i),
 P = exp(S - m) / l, O = P V; LSE_i = m_i + ln l_i is reported beside O.
 Second, test-only path: the blockwise online recurrence of the same section and

@@ -5,9 +5,8 @@
  * may load this code. It shares nothing with the CUDA path: no headers, helpers,
  * constants or tables. It is plain and slow on purpose.
  *
- * What it computes, for one attention head, follows "Compilers and kernels"
- * (aaai.latere.ai/zh/infrastructure/compilers-kernels), section "FlashAttention
- * rewrites the algorithm around IO", first display and its symbol list:
+ * What it computes, for one attention head, follows "Compilers and kernels", section
+ * "FlashAttention rewrites the algorithm around IO", first display and its symbol list:
  *
  *     S = Q K^T / sqrt(d) + C,   P_ij = exp(S_ij - m_i) / l_i,   O = P V,
  *     m_i = max_j S_ij,          l_i = sum_j exp(S_ij - m_i),
@@ -28,8 +27,8 @@
  *
  * The second, test-only path is the pages' blockwise online recurrence (same
  * section, the display for b_t, m_t, alpha_t, l_t, o_t and O_i = o_T / l_T) and
- * the three-quantity form of "AI Infra, ch. 5 Operators and runtime"
- * (pre.everytik.com/books/ai-infra/05), section 5.3 "FlashAttention", Example 5-6:
+ * the three-quantity form of "AI Infra, ch. 5 Operators and runtime", section 5.3
+ * "FlashAttention", Example 5-6:
  * state (m, l, u), r = e^{m - m'}, l' = r l + p, u' = r u + p V, output u'/l'.
  *
  * All arithmetic is IEEE fp64 on the exact values of the bf16 / fp32 inputs.

@@ -6,11 +6,11 @@ oracle; tests/test_oracle_mutants.py runs them on copies of the oracle source wi
 a planted mistake and requires that some pin fails for every mistake.
 
 Sources of the facts:
-  * "Compilers and kernels" (aaai.latere.ai/zh/infrastructure/compilers-kernels),
-    section "FlashAttention rewrites the algorithm around IO": the definition of
+  * "Compilers and kernels", section "FlashAttention rewrites the algorithm around
+    IO": the definition of
     S, P, O, m, l; the assumption of at least one allowed key per row; the blockwise
     recurrence over blocks that partition the allowed keys and its exactness.
-  * "AI Infra ch. 5" (pre.everytik.com/books/ai-infra/05), section 5.3, Example 5-6
+  * "AI Infra ch. 5 Operators and runtime", section 5.3, Example 5-6
     and Exercise 5-3 (the (m, l, u) update), and section 5.4 (two blocks holding 1
     and 3 cannot be merged without their statistics).
   * Closed forms and invariants of softmax attention (rows of P sum to 1, constant V,
