@@ -58,7 +58,7 @@ extern "C" {
 /* Return codes. Zero is success; every error is negative. */
 #define ATTN_OK 0
 #define ATTN_ERR_INVALID_ARG (-1)        /* null/misaligned/overlapping pointer, bad size, mode or scale */
-#define ATTN_ERR_UNSUPPORTED (-2)        /* a head width d or d_v this build has no kernel for */
+#define ATTN_ERR_UNSUPPORTED (-2)        /* a head width d or d_v the library has no kernel for */
 #define ATTN_ERR_NO_DEVICE (-3)          /* no CUDA device, or no CUDA driver */
 #define ATTN_ERR_UNSUPPORTED_DEVICE (-4) /* the current device is not compute capability 10.3 */
 #define ATTN_ERR_LAUNCH (-5)             /* the kernel launch was rejected by the CUDA runtime */
