@@ -19,7 +19,7 @@ from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_ERR_CUDA, ATTN_ERR_DEVIC
                    attn_set_wait_timeout_ns, attn_version, library_path, load, strerror)
 
 __all__ = [
-    "attn_fwd", "attn_fwd_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "attn_fwd_splitkv",
+    "attention", "attn_fwd", "attn_fwd_raw", "attn_fwd_ex", "attn_fwd_ex_raw", "attn_fwd_splitkv",
     "attn_fwd_splitkv_raw", "attn_fwd_splitkv_plan", "splitkv_workspace", "attn_fwd_host",
     "attn_fwd_host_raw", "attn_fwd_host_staging_bytes", "host_staging", "attn_bwd_host",
     "attn_bwd_host_raw", "attn_bwd_host_staging_bytes", "bwd_host_staging", "attn_bwd",
@@ -260,3 +260,10 @@ def attn_bwd_host(Q, K, V, O, dO, LSE, mode, C, ckey, scale, dQ, dK, dV, staging
     if code != ATTN_OK:
         raise AttnError(code, "attn_bwd_host")
     return dQ, dK, dV
+
+
+def attention(q, k, v, causal=False, bias=None, key_bias=None, scale=None):
+    """Differentiable attention on the library's kernels (see autograd.attention)."""
+    from .autograd import attention as _attention
+
+    return _attention(q, k, v, causal, bias, key_bias, scale)
