@@ -97,10 +97,15 @@ int current_device(int *dev_out, unsigned int **watchdog) {
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   // Make the device's primary context current on this thread: a thread that has not yet
   // made a runtime call that binds it (a framework's worker thread, say) would otherwise
-  // have no context for the driver calls that encode the tensor maps.
-  if (cudaSetDevice(dev) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_CUDA;
+  // have no context for the driver calls that encode the tensor maps. Once per thread and
+  // device.
+  thread_local int bound_dev = -1;
+  if (bound_dev != dev) {
+    if (cudaSetDevice(dev) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    bound_dev = dev;
   }
   std::lock_guard<std::mutex> lock(g_device_mutex);
   DeviceInfo &info = g_devices[dev];
