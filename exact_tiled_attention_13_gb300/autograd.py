@@ -27,6 +27,7 @@ def _function():
             return O
 
         @staticmethod
+        @torch.autograd.function.once_differentiable
         def backward(ctx, dO):
             q, k, v, O, LSE = ctx.saved_tensors
             dO = dO.to(torch.bfloat16).contiguous()
@@ -47,12 +48,16 @@ def attention(q, k, v, causal: bool = False, bias=None, key_bias=None, scale: fl
     """softmax(q k^T * scale + C) v for bf16 CUDA tensors q [BH, Nq, d], k [BH, Nk, d],
     v [BH, Nk, d_v], differentiable in q, k and v. C is the causal mask (aligned at the
     last key) and/or `bias` (fp32 [BH, Nq, Nk]) or `key_bias` (fp32 [BH, Nk]); scale
-    defaults to 1 / sqrt(d). Returns O in bf16."""
+    defaults to 1 / sqrt(d). Returns O in bf16. The backward pass is first-order only (no
+    double backward), and a bias that requires grad is rejected with ValueError."""
     global _FN
     if _FN is None:
         _FN = _function()
     from . import ATTN_BIAS_DENSE, ATTN_BIAS_KEY
 
+    for name, t in (("bias", bias), ("key_bias", key_bias)):
+        if t is not None and t.requires_grad:
+            raise ValueError(f"attention(): {name} takes no gradient; pass it detached")
     mode = ATTN_MASK_CAUSAL if causal else ATTN_MASK_NONE
     if bias is not None:
         mode |= ATTN_BIAS_DENSE

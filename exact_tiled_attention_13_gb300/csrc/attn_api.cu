@@ -60,6 +60,25 @@ std::mutex g_device_mutex;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_once;
+
+// The context current on this thread, or null; *known is false when the driver entry point
+// could not be found (then nothing is known about the thread's binding).
+CUcontext thread_context(bool *known) {
+  std::call_once(g_ctx_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  *known = g_ctx_current != nullptr && g_ctx_current(&ctx) == CUDA_SUCCESS;
+  return *known ? ctx : nullptr;
+}
 
 bool ranges_overlap(const void *a, size_t na, const void *b, size_t nb) {
   if (!a || !b || na == 0 || nb == 0) return false;
@@ -97,10 +116,12 @@ int current_device(int *dev_out, unsigned int **watchdog) {
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
   // Make the device's primary context current on this thread: a thread that has not yet
   // made a runtime call that binds it (a framework's worker thread, say) would otherwise
-  // have no context for the driver calls that encode the tensor maps. Once per thread and
-  // device.
+  // have no context for the driver calls that encode the tensor maps. Done once per thread
+  // and device, and again whenever the thread has been left with no current context (a
+  // context popped or destroyed through the driver API since).
   thread_local int bound_dev = -1;
-  if (bound_dev != dev) {
+  bool known = false;
+  if (bound_dev != dev || (thread_context(&known) == nullptr && known)) {
     if (cudaSetDevice(dev) != cudaSuccess) {
       cudaGetLastError();
       return ATTN_ERR_CUDA;

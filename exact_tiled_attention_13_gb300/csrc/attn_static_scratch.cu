@@ -21,7 +21,9 @@ void *g_scratch_ptr[kMaxDevices];
 bool g_scratch_ready[kMaxDevices];
 std::mutex g_scratch_mutex;
 
-// Device address of g_scratch on the current device, looked up once per device.
+// Device address of g_scratch on the current device, looked up once per device and kept for
+// the life of the process (a cudaDeviceReset unloads the module and invalidates it; the
+// header tells callers not to reset a device the library is still used on).
 int scratch_on_current_device(void **out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -31,6 +33,15 @@ int scratch_on_current_device(void **out) {
                                                                          : ATTN_ERR_CUDA;
   }
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  // The library holds device code for compute capability 10.3 only: on any other device the
+  // symbol lookup would fail, so report the unsupported device the way every entry point does.
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED_DEVICE;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (!g_scratch_ready[dev]) {
     void *ptr = nullptr;

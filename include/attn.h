@@ -30,6 +30,12 @@
  * memory (the host-streaming calls create three streams and seven events per device on
  * their first call). They are thread-safe:
  * calls from several host threads or on several streams may overlap.
+ *
+ * Device reset: the library caches, per device, the device addresses of its own
+ * __device__ variables (the watchdog word, the fixed scratch array of
+ * attn_fwd_splitkv_static). cudaDeviceReset or cuDevicePrimaryCtxReset unloads the
+ * library's device code with the context and leaves those addresses stale: do not reset
+ * a device and then call this library on it again in the same process.
  */
 #ifndef EXACT_TILED_ATTENTION_13_ATTN_H
 #define EXACT_TILED_ATTENTION_13_ATTN_H
@@ -300,14 +306,20 @@ ATTN_API int attn_bwd_host_staging_bytes(int mode, int BH, int Nq, int Nk, int d
                                          int o_dtype, int heads_per_chunk,
                                          unsigned long long *bytes);
 
-/* Static English text for a return code (never NULL). */
+/* Static English text for a return code (never NULL). The pages have no counterpart: it
+ * spells out the error part of the kernel contract (shapes, layout, aliasing, errors) that
+ * "AI compiler engineer: how a compute graph becomes a GPU kernel" asks every kernel
+ * interface to state. */
 ATTN_API const char *attn_strerror(int code);
 
 /*
  * attn_device_status -- synchronizes `stream` (NULL: the legacy default stream),
  * then reads and clears the current device's watchdog word. Every pipeline wait in
  * the kernels is bounded; a wait that runs out records where it stopped in that
- * word and the kernel returns without hanging the device.
+ * word and the kernel returns without hanging the device. This is the pages' advice
+ * for a program that stops making progress ("AI Infra ch. 5", section 5.1, the passage
+ * on telling a slow program from a stuck one: every wait names the event it waits for,
+ * and a wait is given a timeout after which it reports what was still outstanding).
  * Returns ATTN_OK, ATTN_ERR_DEVICE_TIMEOUT, or ATTN_ERR_CUDA / ATTN_ERR_NO_DEVICE
  * when the synchronization or the read itself fails.
  * If `detail` is not NULL it receives the raw watchdog word (0 when clear).
@@ -336,7 +348,8 @@ ATTN_API int attn_set_fault_injection(int fault);
 
 /* ABI version of this header (major * 100 + minor): 1.00 attn_fwd; 1.01 attn_fwd_ex;
  * 1.02 attn_fwd_splitkv, attn_fwd_splitkv_plan; 1.03 attn_fwd_splitkv_static;
- * 1.04 attn_bwd, attn_bwd_workspace_bytes. attn_version() returns the library's. */
+ * 1.04 attn_bwd, attn_bwd_workspace_bytes; 1.05 attn_fwd_host, attn_fwd_host_staging_bytes;
+ * 1.06 attn_bwd_host, attn_bwd_host_staging_bytes. attn_version() returns the library's. */
 #define ATTN_ABI_VERSION 106
 ATTN_API int attn_version(void);
 

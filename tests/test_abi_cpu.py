@@ -213,6 +213,16 @@ def test_valid_splitkv_call_without_gpu_reports_no_device():
     assert call_split(Nk=1000) == eta.ATTN_ERR_NO_DEVICE
 
 
+@pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
+def test_static_splitkv_reports_the_device_like_the_workspace_call():
+    # A plan that fits the fixed array: the device is examined before the array's address is
+    # looked up, so the code is the one attn_fwd_splitkv returns, not a generic CUDA failure.
+    code = _lib.attn_fwd_splitkv_static_raw(QP, KP, VP, 0, None, None, 2, 48, 1000, 64, 64,
+                                            0.125, 4, OP, 1, LP, None)
+    assert code == eta.ATTN_ERR_NO_DEVICE
+    assert code == call_split(Nk=1000)
+
+
 # ---------------------------------------------------------------- backward pass
 def call_bwd(**over):
     a = dict(Q=QP, K=KP, V=VP, O=OP, o_dtype=1, dO=0xA00000, LSE=LP, mode=0, C=None, ckey=None,
