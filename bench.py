@@ -16,6 +16,8 @@ roofline  : the kernel's achieved TFLOP/s (or GB/s when bandwidth-bound) over th
 e2e       : the same metric through the public call with pinned host inputs copied in
             and O, LSE copied back every step
 cpu_baseline: the fp64 CPU oracle timed on a bounded row sample on this host's cores
+workloads : (one GPU) every other synthetic workload timed in the same run, each with its
+            step time, TFLOP/s, roofline fraction and the clocks of its own timed region
 --impl reference: the same line for the oracle alone (the reference arm)
 
 Under torchrun (WORLD_SIZE > 1) every rank runs an independent replica of the
@@ -76,6 +78,11 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="rows in the CPU-baseline sample (0: sized to ~15 s of oracle work)")
+    ap.add_argument("--workloads", default="all",
+                    help="other workloads timed in the same run and reported under 'workloads' "
+                         "(comma-separated ids, 'all' for every one but --workload, 'none')")
+    ap.add_argument("--workload-steps", type=int, default=0,
+                    help="timed steps of each workload under 'workloads' (0: max(--steps, 50))")
     return ap.parse_args(argv)
 
 
@@ -357,6 +364,119 @@ def run_reference(args):
     return 0
 
 
+def time_steps(wl, stream, steps, warmup, flush, device):
+    """Per-step CUDA-event times (ms) of `steps` launches of `wl` after `warmup` untimed
+    ones, and the time of the whole region. With `flush` (inputs that fit in L2) a buffer
+    twice the size of L2 is written before every timed launch, outside its events."""
+    import torch
+
+    for _ in range(max(3, warmup)):
+        wl.launch(stream)
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(float(i))
+        starts[i].record(stream)
+        wl.launch(stream)
+        ends[i].record(stream)
+    r1.record(stream)
+    torch.cuda.synchronize(device)
+    return np.array([a.elapsed_time(b) for a, b in zip(starts, ends)]), r0.elapsed_time(r1)
+
+
+def launch_floor_ms(stream, steps, flush, device):
+    """Event time of an (almost) empty kernel timed like a flushed workload's step: the
+    launch and event overhead below which no step can go."""
+    import torch
+
+    for _ in range(3):
+        torch.cuda._sleep(1)
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(float(i))
+        starts[i].record(stream)
+        torch.cuda._sleep(1)
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    return float(np.median([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+
+
+def roofline_of(F, B, kernel_ms, peaks):
+    """Bound, achieved rate and fraction of the measured peak for one step time."""
+    bound = "tensor" if F / (peaks["bf16_tflops"] * 1e12) >= B / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    if bound == "tensor":
+        achieved, peak, unit = F / (kernel_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = B / (kernel_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak}
+
+
+def other_workloads(args, stream, device, local):
+    """Every other workload timed in this run: step time, throughput, roofline fraction and
+    the clocks of its own timed region (one entry per workload id)."""
+    import torch
+
+    import exact_tiled_attention_13_gb300 as eta
+    from exact_tiled_attention_13_gb300.workload import DeviceWorkload
+
+    if args.workloads == "none":
+        return []
+    ids = (sorted(synth.WORKLOADS) if args.workloads == "all"
+           else [int(x) for x in args.workloads.split(",") if x.strip()])
+    peaks, _ = measured_peaks()
+    steps = args.workload_steps or max(args.steps, 50)
+    out = []
+    for wid in ids:
+        if wid == args.workload:
+            continue
+        w = synth.WORKLOADS[wid]
+        F, B = workload_figures(w)
+        wl = DeviceWorkload(wid, device=device)
+        flush = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+                 if needs_flush(w) else None)
+        clocks = ClockSampler(local)
+        clocks.start()
+        time.sleep(0.3)
+        t0 = time.time()
+        per_step, region_ms = time_steps(wl, stream, steps, args.warmup, flush, device)
+        t1 = time.time()
+        clock_info = clocks.stop(t0, t1)
+        code, word = eta.attn_device_status(None)
+        if code != eta.ATTN_OK:
+            raise SystemExit(f"watchdog tripped on workload {wid}: {word:#x}")
+        kernel_ms = float(np.mean(per_step)) if flush is not None else region_ms / steps
+        entry = {"id": wid, "workload": w.name, "ms_per_step": kernel_ms,
+                 "value": F / (kernel_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                 "steps": steps, "warmup": max(3, args.warmup),
+                 "launches_per_step": wl.launches_per_step,
+                 "roofline": roofline_of(F, B, kernel_ms, peaks),
+                 "algorithmic_flops": F, "algorithmic_bytes": B,
+                 "l2": ("L2 flushed between steps (a 258 MB write outside each step's events); "
+                        "step time = mean of the launches' own event times") if flush is not None
+                 else "inputs larger than L2, launches back to back; step time = region / steps",
+                 "step_ms_percentiles": {"p10": float(np.percentile(per_step, 10)),
+                                         "p50": float(np.percentile(per_step, 50)),
+                                         "p90": float(np.percentile(per_step, 90))},
+                 "clocks": clock_info, "config": config_dict(w, 1)}
+        if wid == 1:
+            entry["launch_floor_ms"] = launch_floor_ms(stream, steps, flush, device)
+            entry["launch_floor_note"] = ("median event time of torch.cuda._sleep(1), an almost "
+                                          "empty kernel, timed like this workload's steps")
+        out.append(entry)
+        del wl, flush
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -457,6 +577,7 @@ def run_ours(args):
                             f"together (the attention kernels dominate)")
 
     line = None
+    extra = other_workloads(args, stream, device, local) if world == 1 else []
     if rank == 0:
         nrows = args.cpu_rows or cpu_rows_for_seconds(w, wl.host, 15.0)
         cpu = cpu_baseline(w, wl.host, nrows)
@@ -473,6 +594,9 @@ def run_ours(args):
                                         "p50": float(np.percentile(per_step, 50)),
                                         "p90": float(np.percentile(per_step, 90))},
                 "library": os.path.relpath(eta.library_path(), ROOT)}
+        if extra:
+            line["workloads"] = extra
+            line["gpu_launches_workloads"] = sum(e["steps"] * e["launches_per_step"] for e in extra)
     barrier(dist, device)
     if line is not None:
         print(json.dumps(line), flush=True)
