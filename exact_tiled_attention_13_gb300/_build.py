@@ -24,6 +24,7 @@ SOURCES = [
     "attn_inst_d64_dv128.cu",
     "attn_inst_d128_dv64.cu",
     "attn_inst_d128_dv128.cu",
+    "attn_pair_inst.cu",
     "attn_static_scratch.cu",
     "attn_host_stream.cu",
     "attn_bwd_inst_d64_dv64.cu",
@@ -31,7 +32,7 @@ SOURCES = [
     "attn_bwd_inst_d128_dv64.cu",
     "attn_bwd_inst_d128_dv128.cu",
 ]
-HEADERS = ["attn_fwd_kernel.cuh", "attn_merge_kernel.cuh", "attn_bwd_kernel.cuh", "ptx.cuh"]
+HEADERS = ["attn_fwd_kernel.cuh", "attn_fwd_pair_kernel.cuh", "attn_merge_kernel.cuh", "attn_bwd_kernel.cuh", "ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "--expt-relaxed-constexpr", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden"]

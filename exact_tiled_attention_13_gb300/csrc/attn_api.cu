@@ -30,6 +30,13 @@ ETA_DECLARE(128, 64)
 ETA_DECLARE(128, 128)
 #undef ETA_DECLARE
 #undef ETA_DECLARE_C
+// CTA-pair forward kernels (attn_pair_inst.cu).
+template <int D, int DV, bool CAUSAL>
+cudaError_t launch_attn_pair(const LaunchArgs &);
+extern template cudaError_t launch_attn_pair<64, 128, false>(const LaunchArgs &);
+extern template cudaError_t launch_attn_pair<64, 128, true>(const LaunchArgs &);
+extern template cudaError_t launch_attn_pair<128, 128, false>(const LaunchArgs &);
+extern template cudaError_t launch_attn_pair<128, 128, true>(const LaunchArgs &);
 #define ETA_DECLARE_BWD_C(D, DV, C)                                                       \
   extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_NONE>(const BwdLaunchArgs &);  \
   extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_DENSE>(const BwdLaunchArgs &); \
@@ -318,6 +325,16 @@ int head_group(int BH, int Nk, int d, int d_v) {
   return g >= BH ? BH : (g < 1.0 ? 1 : static_cast<int>(g));
 }
 
+// The CTA-pair kernel (attn_fwd_pair_kernel.cuh) can serve the problems without a bias term
+// with 128 value columns, in one key range. It is not dispatched yet: one block per 128
+// query rows pays its start-up and drain per block, which keeps it at the speed of
+// attn_fwd_kernel (a persistent form that overlaps them is the next step).
+bool use_pair_kernel(const Problem &a, int n_splits) {
+  (void)a;
+  (void)n_splits;
+  return false;
+}
+
 // Launches the attention kernel. With n_splits > 1 each CTA covers `split_tiles` K/V
 // tiles of its head and writes fp32 partials to O_dst / LSE_dst instead of O / LSE.
 int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int split_tiles,
@@ -359,12 +376,18 @@ int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int s
   la.p.timeout_ns = g_timeout_ns.load();
   la.p.fault = g_fault.load();
   la.stream = static_cast<cudaStream_t>(a.stream);
-  if (static_cast<uint64_t>(a.BH) * la.p.ctas_per_head * n_splits > 0x7FFFFFFFull)
+  if (static_cast<uint64_t>(a.BH) * la.p.ctas_per_head * n_splits > 0x3FFFFFFFull)
     return ATTN_ERR_INVALID_ARG;
 
   cudaError_t e;
   const bool causal = a.causal();
-  if (a.d == 64 && a.d_v == 64) e = dispatch<64, 64>(causal, bias, la);
+  if (use_pair_kernel(a, n_splits)) {
+    // CTA pairs: each CTA copies 64 keys of every K tile (one 64 x 64 box per 128-byte span).
+    if (encode_3d(&la.tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.d, nk, bh, SW_CHUNK, BN / 2) != ATTN_OK)
+      return ATTN_ERR_CUDA;
+    if (a.d == 64) e = causal ? launch_attn_pair<64, 128, true>(la) : launch_attn_pair<64, 128, false>(la);
+    else e = causal ? launch_attn_pair<128, 128, true>(la) : launch_attn_pair<128, 128, false>(la);
+  } else if (a.d == 64 && a.d_v == 64) e = dispatch<64, 64>(causal, bias, la);
   else if (a.d == 64) e = dispatch<64, 128>(causal, bias, la);
   else if (a.d_v == 64) e = dispatch<128, 64>(causal, bias, la);
   else e = dispatch<128, 128>(causal, bias, la);

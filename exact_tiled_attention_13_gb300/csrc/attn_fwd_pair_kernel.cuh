@@ -1,0 +1,595 @@
+// Exact attention forward pass on CTA pairs, for sm_103a (no bias term: the plain and the
+// causal mask, d = 64 or 128, d_v = 128).
+//
+// The recurrence is the one in "Compilers and kernels", section "FlashAttention rewrites
+// the algorithm around IO" (b_t, m_t, alpha_t, l_t, o_t, O_i = o_T / l_T), evaluated over
+// 128-key tiles as in attn_fwd_kernel.cuh. What differs is how the work is laid on the
+// chip.
+//
+// A cluster of two CTAs on two SMs owns 256 query rows of one head, 128 in each CTA. The
+// tensor-core products are the pair's (.cta_group::2, M = 256): S = Q K^T with each CTA's
+// Q rows in its own shared memory and the K tile split between the two (64 keys each), and
+// o += P V with each CTA's P in its own tensor memory and the V tile split by columns (64
+// value columns each). So each SM stages and streams half of every K and V tile: half the
+// shared-memory operand traffic and half the L2 traffic per SM of one CTA doing all 128
+// keys, at the same tensor rate.
+//
+// One query tile per CTA leaves room in tensor memory (512 columns) for two S buffers, two
+// P buffers (bf16) and o. An S buffer is released as soon as the softmax has loaded it, so
+// the even CTA computes S(t+1) and S(t+2) while the softmax of S(t) runs, and the chain
+// softmax -> P -> P V -> next S no longer serialises the tensor cores (the products of one
+// query tile depend on its softmax only through P).
+//
+// Warp roles (12 warps in each CTA):
+//   softmax, warps 0-7: two warpgroups that take the key tiles in turn (even tiles in the
+//     first, odd tiles in the second); thread = query row = tensor-memory lane, a whole row
+//     of 128 keys per tile. The two warpgroups run out of phase, so one's exponentials
+//     overlap the other's loads and maxima. The recurrence couples consecutive tiles only
+//     through the exponent reference: each warp passes the reference it settled on to the
+//     other warpgroup's warp of the same rows (a word per row in shared memory and an
+//     mbarrier), and keeps its own share of l; the shares are brought to the final
+//     reference and added in the epilogue. The warpgroup whose tile moves the reference
+//     rescales o (all 128 columns of its rows) once the previous P V has completed.
+//   MMA, warps 8 (S products) and 11 (P V products) of the even CTA: issue the pair's
+//     products; each commit signals the mbarrier at the same offset in both CTAs
+//     (multicast). S(t) waits for the softmax to have loaded S(t-2) from its buffer.
+//   Q/K load (warp 9) and V load (warp 10) of both CTAs: TMA copies of this CTA's halves;
+//     completion is signalled on the even CTA's full barriers, whose expected byte count
+//     covers both halves, so the MMA warp waits once per tile.
+// Every mbarrier wait is bounded in time, as in attn_fwd_kernel.cuh.
+#pragma once
+
+#include "attn_fwd_kernel.cuh"
+
+namespace eta {
+
+template <int D, int DV, bool CAUSAL>
+struct PairCfg {
+  static_assert(D == 64 || D == 128, "d must be 64 or 128");
+  static_assert(DV == 128, "the pair kernel splits 128 value columns in two 128-byte halves");
+  static constexpr int Q_TILE = BM * D * 2;       // this CTA's 128 query rows
+  static constexpr int KH_ROWS = BN / 2;          // keys of a K tile held by one CTA
+  static constexpr int KH_BOX = KH_ROWS * 128;    // one 64-row x 128-byte box
+  static constexpr int KH_TILE = KH_ROWS * D * 2;
+  static constexpr int VH_COLS = DV / 2;          // value columns held by one CTA
+  static constexpr int VH_TILE = BN * VH_COLS * 2;
+  static constexpr int NS = 2;                    // S buffers (and P buffers) in tensor memory
+  static constexpr int KS = 4;
+  static constexpr int VS = 4;
+  static_assert(VS >= 3, "the softmax tells P(t) V apart by the phase of its V slot");
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + Q_TILE;
+  static constexpr int V_OFF = K_OFF + KS * KH_TILE;
+  static constexpr int RX_OFF = V_OFF + VS * VH_TILE;     // references passed on, 2 x 128 fp32
+  static constexpr int LX_OFF = RX_OFF + 2 * BM * 4;       // shares of l, 2 x 2 x 128 fp32
+  static constexpr int BAR_OFF = LX_OFF + 2 * 2 * BM * 4;
+  static constexpr int B_QFULL = 0;
+  static constexpr int B_KFULL = 1;
+  static constexpr int B_KEMPTY = B_KFULL + KS;
+  static constexpr int B_VFULL = B_KEMPTY + KS;
+  static constexpr int B_VEMPTY = B_VFULL + VS;   // P(t) V done (V slot free, P buffer free, o holds P(t) V)
+  static constexpr int B_SFULL = B_VEMPTY + VS;   // S(t) computed (both CTAs)
+  static constexpr int B_SEMPTY = B_SFULL + NS;   // S(t) loaded by the 4 softmax warps of each CTA (even CTA)
+  static constexpr int B_PFULL = B_SEMPTY + NS;   // P(t) written by the 4 softmax warps of each CTA (even CTA)
+  static constexpr int B_OFULL = B_PFULL + NS;    // last P V done
+  static constexpr int B_DRAIN = B_OFULL + 1;     // products of the S issuer drained
+  static constexpr int B_DRAIN2 = B_DRAIN + 1;    // products of the P V issuer drained
+  static constexpr int B_HREF = B_DRAIN2 + 1;      // reference passed on by warpgroup g, warp q: 4 g + q
+  static constexpr int NUM_BARS = B_HREF + 8;
+  static constexpr int TMEMPTR_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int ABORT_OFF = TMEMPTR_OFF + 4;
+  static constexpr int SMEM_USED = ABORT_OFF + 4;
+  // At least 120 KB so one CTA holds an SM (it allocates all of the SM's tensor memory).
+  static constexpr int SMEM_TOTAL = SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
+  static_assert(SMEM_TOTAL <= 232448, "shared memory over the sm_103a per-CTA limit");
+  static_assert(KS * KH_TILE + VS * VH_TILE >= 8 * 32 * 128,
+                "the idle K and V rings stage 32 rows x 128 bytes per softmax warp");
+
+  static constexpr int MMA_WARP = 8;
+  static constexpr int LOAD_WARP = 9;   // Q and K
+  static constexpr int VLOAD_WARP = 10; // V
+  static constexpr int PV_WARP = 11;    // issues the P V products (MMA_WARP issues S)
+  static constexpr int NUM_WARPS = 12;
+  static constexpr int THREADS = 32 * NUM_WARPS;
+  static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
+  static constexpr int REGS_SOFTMAX = 216;
+  static constexpr int REGS_CTRL = 72;
+  static constexpr int REGS_NEEDED = 128 * (2 * REGS_SOFTMAX + REGS_CTRL);
+  static_assert(REGS_NEEDED <= THREADS * LAUNCH_REGS,
+                "register split exceeds the registers the block is launched with");
+  // Tensor memory: S(t) in buffer t % 2, P(t) (bf16 pairs, 64 columns) in its own buffer
+  // t % 2, then o. An S buffer is free once the softmax has loaded it, a P buffer once the
+  // P V product that read it has completed.
+  static constexpr int P_COL = NS * BN;
+  static constexpr int O_COL = P_COL + NS * (BN / 2);
+  static constexpr int TMEM_COLS = 512;
+  static_assert(O_COL + DV <= TMEM_COLS, "tensor memory holds 512 columns");
+
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(2 * BM, BN, false);
+  static constexpr uint32_t IDESC_PV = idesc_bf16_f32(2 * BM, DV, true);
+};
+
+// The pair's schedule: query rows [256 pt, 256 pt + 256) of head bh, this CTA's 128 of them
+// in query tile qt; K/V tiles hi_max down to 0 (the pair's last row decides hi_max, so the
+// even CTA's rows may meet a last tile that is wholly above their causal limit: its scores
+// are all masked and its P is 0).
+template <bool CAUSAL>
+struct PairSchedule {
+  int bh, pt, qt, hi_max, n_it;
+  __device__ PairSchedule(const KernelParams &p, unsigned cluster, unsigned rank) {
+    int r;
+    unit_of_block(cluster, p.BH, p.ctas_per_head, p.head_group, &bh, &r);
+    pt = p.ctas_per_head - 1 - r;  // longest first
+    qt = 2 * pt + static_cast<int>(rank);
+    const int top = p.nkv_tiles - 1;
+    if (CAUSAL) {
+      const int last_row = cmin(2 * pt * BM + 2 * BM - 1, p.Nq - 1);
+      hi_max = cmin(floor_div(last_row + p.causal_off, BN), top);
+    } else {
+      hi_max = top;
+    }
+    n_it = hi_max >= 0 ? hi_max + 1 : 0;
+  }
+};
+
+// Waits (bounded) about 20 us: after an abort, copies already issued by this CTA that
+// signal the other CTA's barriers cannot be observed here; give them time to land.
+__device__ __forceinline__ void settle_after_abort() {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < 20000ull) {
+  }
+}
+
+template <int D, int DV, bool CAUSAL>
+__global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
+    attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ KernelParams p) {
+  using CF = PairCfg<D, DV, CAUSAL>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + CF::BAR_OFF;
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem + CF::TMEMPTR_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + CF::ABORT_OFF);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = pair::cluster_rank();
+  const bool leader = rank == 0;
+  // The even CTA's copy of a barrier (the one the MMA warp waits on).
+  auto LBAR = [&](int i) -> uint32_t { return pair::map_shared(BAR(i), 0); };
+  const PairSchedule<CAUSAL> sch(p, blockIdx.x >> 1, rank);
+  Watchdog wd{sbase + CF::ABORT_OFF, p};
+#ifdef ETA_PHASE_TRACE
+  int trace_n = 0;
+#endif
+
+  // ------------------------------------------------------------------ set-up
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(CF::B_QFULL), 1);
+    for (int s = 0; s < CF::KS; ++s) {
+      mbar_init(BAR(CF::B_KFULL + s), 1);
+      mbar_init(BAR(CF::B_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < CF::VS; ++s) {
+      mbar_init(BAR(CF::B_VFULL + s), 1);
+      mbar_init(BAR(CF::B_VEMPTY + s), 1);
+    }
+    for (int b = 0; b < CF::NS; ++b) {
+      mbar_init(BAR(CF::B_SFULL + b), 1);
+      mbar_init(BAR(CF::B_SEMPTY + b), 8);  // one arrival per softmax warp of the tile, both CTAs
+      mbar_init(BAR(CF::B_PFULL + b), 8);
+    }
+    mbar_init(BAR(CF::B_OFULL), 1);
+    mbar_init(BAR(CF::B_DRAIN), 1);
+    mbar_init(BAR(CF::B_DRAIN2), 1);
+    for (int h = 0; h < 8; ++h) mbar_init(BAR(CF::B_HREF + h), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  // The other CTA signals this CTA's barriers, so both CTAs initialise theirs first; and
+  // the pair's tensor-memory allocation is one collective instruction of a warp in each
+  // CTA, issued once both are known to be running.
+  pair::cluster_sync();
+  if (warp == CF::MMA_WARP) {
+    pair::tmem_alloc(smem_u32(tmem_ptr), CF::TMEM_COLS);
+    pair::tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_ptr;
+  grid_dep_wait();
+  if (threadIdx.x == 0) grid_dep_launch();
+
+  if (warp < CF::MMA_WARP) {
+    // ================================================================ softmax
+    regs_increase<CF::REGS_SOFTMAX>();
+    const int wg = warp / 4;  // this warpgroup takes the tiles it with it % 2 == wg
+    const int wq = warp % 4;  // tensor-memory lanes [32 wq, 32 wq + 32)
+    const int row = 32 * wq + lane;
+    const int q_row = sch.qt * BM + row;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
+    const uint32_t t_o = tmem + lane_off + CF::O_COL;
+    float *rx = reinterpret_cast<float *>(smem + CF::RX_OFF);  // [2 warpgroups][128 rows]
+    float *lx = reinterpret_cast<float *>(smem + CF::LX_OFF);  // [2 sums][2 warpgroups][128 rows]
+    const int h_mine = CF::B_HREF + 4 * wg + wq;
+    const int h_other = CF::B_HREF + 4 * (wg ^ 1) + wq;
+    const float sl2 = p.scale_log2;
+    float m_prev = -INFINITY;  // reference of this warpgroup's previous tile, log2(e)-scaled
+    float l = 0.0f;            // this warpgroup's share of l (fp32 p, for LSE), relative to m_prev
+    float lr = 0.0f;           // the same with each tile's largest p as rounded (for O)
+    bool ok = true;
+    int j_mask = CAUSAL ? floor_div(sch.qt * BM + p.causal_off + 1, BN) : INT_MAX;
+    if (p.Nk % BN != 0) j_mask = cmin(j_mask, p.nkv_tiles - 1);
+    const int lim = CAUSAL ? cmin(q_row + p.causal_off, p.Nk - 1) : p.Nk - 1;
+
+    for (int it = wg; it < sch.n_it; it += 2) {
+      const int b = it % CF::NS;  // = wg: each warpgroup has its S and P buffers
+      const int j = sch.hi_max - it;
+      const uint32_t t_s = tmem + lane_off + b * BN;
+      const uint32_t t_p = tmem + lane_off + CF::P_COL + b * (BN / 2);
+      ok = wd.wait(BAR(CF::B_SFULL + b), (it / CF::NS) & 1, ROLE_SOFTMAX, CF::B_SFULL + b);
+      if (!ok) break;
+      tc_fence_after();
+      ETA_TRACE(1);
+      uint32_t r0[32], r1[32], r2[32], r3[32];
+      tmem_ld32(t_s + 0, r0);
+      tmem_ld32(t_s + 32, r1);
+      tmem_ld32(t_s + 64, r2);
+      tmem_ld32(t_s + 96, r3);
+      tmem_wait_ld(r0);
+      tmem_wait_ld(r1);
+      tmem_wait_ld(r2);
+      tmem_wait_ld(r3);
+      // S(it) is in registers: its buffer may take S(it + 2).
+      tc_fence_before();
+      __syncwarp();
+      if (leader) mbar_arrive_elect(BAR(CF::B_SEMPTY + b));
+      else pair::mbar_arrive_cluster_elect(LBAR(CF::B_SEMPTY + b));
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        x[c] = __uint_as_float(r0[c]);
+        x[32 + c] = __uint_as_float(r1[c]);
+        x[64 + c] = __uint_as_float(r2[c]);
+        x[96 + c] = __uint_as_float(r3[c]);
+      }
+      if (j >= j_mask) {
+        const int lim_j = lim - j * BN;
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c > lim_j) x[c] = -INFINITY;
+      }
+      const float bt = row_max128(x);
+      ETA_TRACE(2);
+      // The reference after tile it - 1, from the other warpgroup; then this tile's: moved
+      // to b_t only when b_t exceeds it by more than RESCALE_TAU (log2 units), as in
+      // attn_fwd_kernel.cuh. It is passed on at once: the other warpgroup's next tile waits
+      // for it, and nothing else.
+      float m_in = -INFINITY;
+      if (it > 0) {
+        ok = wd.wait(BAR(h_other), ((it - 1) >> 1) & 1, ROLE_SOFTMAX, h_other);
+        if (!ok) break;
+        m_in = rx[(wg ^ 1) * BM + row];
+      }
+      const float bs = bt * sl2;
+      const bool move = bs > m_in + RESCALE_TAU;  // also the first allowed key (m_in = -inf)
+      const float m_new = move ? bs : m_in;
+      rx[wg * BM + row] = m_new;
+      __syncwarp();
+      mbar_arrive_elect(BAR(h_mine));
+      ETA_TRACE(3);
+      // No allowed key seen yet: every p is 0; use 0 as reference.
+      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+      // P buffer b was last read by P(it-2) V. (VS >= 3: P(it-2-VS) V completed before this
+      // warpgroup's previous tile, P(it-2+VS) V needs a later P of its own.)
+      if (it >= CF::NS) {
+        const int pv = it - CF::NS;
+        ok = wd.wait(BAR(CF::B_VEMPTY + pv % CF::VS), (pv / CF::VS) & 1, ROLE_SOFTMAX, CF::B_VEMPTY + pv % CF::VS);
+        if (!ok) break;
+        tc_fence_after();
+      }
+      // p_ij = 2^(x scale log2e - m) as bf16 into the P buffer, 32 keys at a time; the row
+      // sum runs alongside in four independent packed chains.
+      const float neg_m = -m_use;
+      float s[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s[k] = 0.0f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+          const int c = 32 * qq + 2 * c2;
+          float a0, a1;
+          fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg_m, neg_m);
+          const float p0 = ex2_approx(a0);
+          const float p1 = ex2_approx(a1);
+          const int k = 2 * (c2 & 3);
+          add2(s[k], s[k + 1], s[k], s[k + 1], p0, p1);
+          pk[16 * (qq & 1) + c2] = pack_bf16(p0, p1);
+        }
+        if (qq & 1) tmem_st32(t_p + 32 * (qq / 2), pk);
+      }
+      if (__any_sync(0xFFFFFFFFu, move && m_in != -INFINITY)) {
+        // o (after P(it-1) V) is relative to m_in: o_t = alpha_t o_{t-1} needs that product
+        // complete, which the wait here overlaps with the exponentials above; P(it) V, which
+        // adds to o, waits for this tile's arrival below. Rows that saw no allowed key yet
+        // have o = 0. (VS >= 3: P(it-1-VS) V completed before P(it-2) V, waited above;
+        // P(it-1+VS) V needs a later P of this warpgroup.)
+        const int pv = it - 1;
+        ok = wd.wait(BAR(CF::B_VEMPTY + pv % CF::VS), (pv / CF::VS) & 1, ROLE_SOFTMAX, CF::B_VEMPTY + pv % CF::VS);
+        if (!ok) break;
+        tc_fence_after();
+        const float alpha_o = move ? ex2_approx(m_in - m_use) : 1.0f;
+#pragma unroll
+        for (int cc = 0; cc < DV / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(t_o + 32 * cc, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float f0, f1;
+            mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), alpha_o, alpha_o);
+            o[c] = __float_as_uint(f0);
+            o[c + 1] = __float_as_uint(f1);
+          }
+          tmem_st32(t_o + 32 * cc, o);
+        }
+      }
+
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (leader) mbar_arrive_elect(BAR(CF::B_PFULL + b));
+      else pair::mbar_arrive_cluster_elect(LBAR(CF::B_PFULL + b));
+      ETA_TRACE(4);
+
+      add2(s[0], s[1], s[0], s[1], s[2], s[3]);
+      add2(s[4], s[5], s[4], s[5], s[6], s[7]);
+      add2(s[0], s[1], s[0], s[1], s[4], s[5]);
+      const float tile_sum = s[0] + s[1];
+      // The tile's largest p as rounded to bf16 joins O's denominator (see
+      // attn_fwd_kernel.cuh); this warpgroup's shares move from m_prev to the new reference.
+      const float pmax = ex2_approx(fmaf(bt, sl2, neg_m));
+      const float corr = __uint_as_float(pack_bf16(pmax, pmax) << 16) - pmax;
+      const float alpha = ex2_approx(m_prev - m_use);  // 1 when the reference stayed; 0 from -inf
+      l = fmaf(alpha, l, tile_sum);
+      lr = fmaf(alpha, lr, tile_sum + corr);
+      m_prev = m_new;
+      ETA_TRACE(5);
+    }
+
+    // ------------------------------------------------ epilogue: O = o_T / l_T, LSE
+    // The reference after the last tile (passed on by the other warpgroup when the last
+    // tile was its), both shares of l brought to it and added.
+    float m_last = m_prev;
+    if (ok && sch.n_it > 0 && ((sch.n_it - 1) & 1) != wg) {
+      ok = wd.wait(BAR(h_other), ((sch.n_it - 1) >> 1) & 1, ROLE_SOFTMAX, h_other);
+      if (ok) m_last = rx[(wg ^ 1) * BM + row];
+    }
+    {
+      const float f = ex2_approx(m_prev - (m_last == -INFINITY ? 0.0f : m_last));
+      l *= f;
+      lr *= f;
+    }
+    if (ok && sch.n_it > 0) ok = wd.wait(BAR(CF::B_OFULL), 0, ROLE_SOFTMAX, CF::B_OFULL);
+    lx[(0 * 2 + wg) * BM + row] = l;
+    lx[(1 * 2 + wg) * BM + row] = lr;
+    const int half = wg;  // this warpgroup stores O's columns [64 half, 64 half + 64)
+    if (pair::bar_and(1 + wq, 64, ok)) {
+      if (sch.n_it > 0) tc_fence_after();
+      const float l_row = l + lx[(0 * 2 + (wg ^ 1)) * BM + row];
+      const float lr_row = lr + lx[(1 * 2 + (wg ^ 1)) * BM + row];
+      const float inv_l = (lr_row > 0.0f) ? 1.0f / lr_row : 0.0f;  // no allowed key: O = 0
+      const uint32_t t_oh = t_o + 64 * half;
+      // The K and V rings are idle once the last product completed: each warp stages 32 rows x 128
+      // bytes there at a time, in 16-byte units at (unit ^ row % 8) so neither side has bank
+      // conflicts, and stores them as whole 128-byte row segments, four rows per instruction.
+      uint8_t *stage = smem + CF::K_OFF + warp * (32 * 128);
+      uint4 *srow = reinterpret_cast<uint4 *>(stage + lane * 128);
+      const int row0 = q_row - lane;
+      const int rows_ok = p.Nq - row0 < 32 ? (p.Nq - row0 > 0 ? p.Nq - row0 : 0) : 32;
+      const size_t obase = (static_cast<size_t>(sch.bh) * p.Nq + row0) * DV + 64 * half;
+      const int sub = lane % 8;
+      auto store_stage = [&](uint8_t *g0, int row_bytes) {
+        __syncwarp();
+        uint4 val[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + lane / 8;
+          val[i] = *reinterpret_cast<const uint4 *>(stage + rr * 128 + 16 * (sub ^ (rr & 7)));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rr = 4 * i + lane / 8;
+          if (rr < rows_ok)
+            *reinterpret_cast<uint4 *>(g0 + static_cast<size_t>(rr) * row_bytes + 16 * sub) = val[i];
+        }
+      };
+      // o of a pair that visited no tile was never written: its rows get O = 0.
+      auto load_o = [&](int col, float (&f)[32]) {
+        uint32_t o[32];
+        if (sch.n_it > 0) {
+          tmem_ld32(t_oh + col, o);
+          tmem_wait_ld(o);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) o[c] = 0u;
+        }
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          mul2(f[c], f[c + 1], __uint_as_float(o[c]), __uint_as_float(o[c + 1]), inv_l, inv_l);
+      };
+      if (p.out_f32) {
+#pragma unroll 1
+        for (int cc = 0; cc < 2; ++cc) {
+          float f[32];
+          load_o(32 * cc, f);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            srow[v ^ (lane & 7)] = make_uint4(__float_as_uint(f[4 * v + 0]), __float_as_uint(f[4 * v + 1]),
+                                              __float_as_uint(f[4 * v + 2]), __float_as_uint(f[4 * v + 3]));
+          store_stage(reinterpret_cast<uint8_t *>(static_cast<float *>(p.O) + obase + 32 * cc), DV * 4);
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float f[32];
+          load_o(32 * h, f);
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            srow[(4 * h + v) ^ (lane & 7)] =
+                make_uint4(pack_bf16(f[8 * v + 0], f[8 * v + 1]), pack_bf16(f[8 * v + 2], f[8 * v + 3]),
+                           pack_bf16(f[8 * v + 4], f[8 * v + 5]), pack_bf16(f[8 * v + 6], f[8 * v + 7]));
+        }
+        store_stage(reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.O) + obase), DV * 2);
+      }
+      // LSE_i = m_i + ln l_i, from the log2-scaled reference.
+      if (half == 0 && q_row < p.Nq && p.LSE != nullptr)
+        p.LSE[static_cast<size_t>(sch.bh) * p.Nq + q_row] =
+            (l_row > 0.0f) ? (m_last + lg2_approx(l_row)) * LN2 : -INFINITY;
+    }
+  } else {
+    regs_decrease<CF::REGS_CTRL>();
+    if ((warp == CF::MMA_WARP || warp == CF::PV_WARP) && leader) {
+      // ============================================================== MMA issue (even CTA)
+      // Two issuing warps, one for the S products and one for the P V products. The tensor
+      // cores take few instructions ahead, so an issuing thread blocks on every product;
+      // with one issuer, its waits and commits between products left the pipe idle. Each
+      // commit covers the products of its own thread, so S(it) waits for P(it - NS) V,
+      // which last read its buffer, instead of relying on one thread's issue order.
+      const uint16_t both = 3;
+      const bool s_role = warp == CF::MMA_WARP;
+      const int drain_bar = s_role ? CF::B_DRAIN : CF::B_DRAIN2;
+      bool ok = wd.wait(BAR(CF::B_QFULL), 0, ROLE_MMA, CF::B_QFULL);
+      if (ok) tc_fence_after();
+      if (s_role) {
+        for (int it = 0; ok && it < sch.n_it; ++it) {
+          const int kslot = it % CF::KS;
+          const int b = it % CF::NS;
+          ok = wd.wait(BAR(CF::B_KFULL + kslot), (it / CF::KS) & 1, ROLE_MMA, CF::B_KFULL + kslot);
+          // Buffer b is free once both CTAs' softmax warps have loaded S(it - NS).
+          if (ok && it >= CF::NS)
+            ok = wd.wait(BAR(CF::B_SEMPTY + b), ((it / CF::NS) & 1) ^ 1, ROLE_MMA, CF::B_SEMPTY + b);
+          if (!ok) break;
+          ETA_TRACE(24);
+          tc_fence_after();
+          const uint64_t a_desc = smem_desc(sbase + CF::Q_OFF, 16, 1024);
+          const uint64_t b_desc = smem_desc(sbase + CF::K_OFF + kslot * CF::KH_TILE, 16, 1024);
+          const uint32_t d_tmem = tmem + b * BN;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t a_off = ((ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32) >> 4;
+            const uint32_t b_off = ((ks / 4) * CF::KH_BOX + (ks % 4) * 32) >> 4;
+            pair::mma_ss_elect(d_tmem, a_desc + a_off, b_desc + b_off, CF::IDESC_S, ks > 0 ? 1u : 0u);
+          }
+          ETA_TRACE(25);
+          pair::mma_commit_multicast_elect(BAR(CF::B_SFULL + b), both);
+          pair::mma_commit_multicast_elect(BAR(CF::B_KEMPTY + kslot), both);
+        }
+      } else {
+        for (int it = 0; ok && it < sch.n_it; ++it) {
+          const int b = it % CF::NS;
+          const int vslot = it % CF::VS;
+          ETA_TRACE(20);
+          ok = wd.wait(BAR(CF::B_PFULL + b), (it / CF::NS) & 1, ROLE_MMA, CF::B_PFULL + b);
+          ETA_TRACE(21);
+          if (ok) ok = wd.wait(BAR(CF::B_VFULL + vslot), (it / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
+          if (!ok) break;
+          ETA_TRACE(22);
+          tc_fence_after();
+          const uint64_t b_desc = smem_desc(sbase + CF::V_OFF + vslot * CF::VH_TILE, SW_CHUNK_BYTES, 1024);
+          const uint32_t a_tmem = tmem + CF::P_COL + b * (BN / 2);
+#pragma unroll
+          for (int ks = 0; ks < BN / 16; ++ks)
+            pair::mma_ts_elect(tmem + CF::O_COL, a_tmem + 8 * ks, b_desc + ((ks * 16 * 128) >> 4), CF::IDESC_PV,
+                               (it > 0 || ks > 0) ? 1u : 0u);
+          ETA_TRACE(23);
+          pair::mma_commit_multicast_elect(BAR(CF::B_VEMPTY + vslot), both);
+        }
+        if (ok && sch.n_it > 0) pair::mma_commit_multicast_elect(BAR(CF::B_OFULL), both);
+      }
+      // Nothing may still be in flight on the tensor cores when tensor memory is freed.
+      pair::mma_commit_multicast_elect(BAR(drain_bar), 1);
+      wd.drain(BAR(drain_bar), 0, drain_bar);
+    } else if (warp == CF::LOAD_WARP && lane == 0) {
+      // ============================================================== TMA: Q, K halves
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      if (leader) mbar_arrive_expect_tx(BAR(CF::B_QFULL), 2 * CF::Q_TILE);
+      for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+        pair::tma_load_3d(sbase + CF::Q_OFF + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK, sch.qt * BM, sch.bh,
+                          LBAR(CF::B_QFULL));
+      for (int it = 0; it < sch.n_it; ++it) {
+        const int j = sch.hi_max - it;
+        const int ks = it % CF::KS;
+        if (!wd.wait1(BAR(CF::B_KEMPTY + ks), ((it / CF::KS) & 1) ^ 1, ROLE_LOAD, CF::B_KEMPTY + ks, false)) break;
+        if (p.fault == FAULT_SKIP_FIRST_K && it == 0) continue;  // test hook: a wait runs out
+        if (leader) mbar_arrive_expect_tx(BAR(CF::B_KFULL + ks), 2 * CF::KH_TILE);
+        for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+          pair::tma_load_3d(sbase + CF::K_OFF + ks * CF::KH_TILE + kc * CF::KH_BOX, &tmK, kc * SW_CHUNK,
+                            j * BN + CF::KH_ROWS * static_cast<int>(rank), sch.bh, LBAR(CF::B_KFULL + ks));
+      }
+      if (wd.aborted()) settle_after_abort();
+    } else if (warp == CF::VLOAD_WARP && lane == 0) {
+      // ============================================================== TMA: V halves
+      tma_prefetch_desc(&tmV);
+      for (int it = 0; it < sch.n_it; ++it) {
+        const int j = sch.hi_max - it;
+        const int vs = it % CF::VS;
+        if (!wd.wait1(BAR(CF::B_VEMPTY + vs), ((it / CF::VS) & 1) ^ 1, ROLE_LOAD, CF::B_VEMPTY + vs, false)) break;
+        if (leader) mbar_arrive_expect_tx(BAR(CF::B_VFULL + vs), 2 * CF::VH_TILE);
+        pair::tma_load_3d(sbase + CF::V_OFF + vs * CF::VH_TILE, &tmV, CF::VH_COLS * static_cast<int>(rank),
+                          j * BN, sch.bh, LBAR(CF::B_VFULL + vs));
+      }
+      if (wd.aborted()) settle_after_abort();
+    }
+    __syncwarp();
+  }
+
+  // ------------------------------------------------------------------ teardown
+  // Neither CTA releases its tensor or shared memory while the pair's products may still
+  // read them: the even CTA's MMA warp has drained its products before it gets here.
+  tc_fence_before();
+  __syncthreads();
+  pair::cluster_sync();
+  tc_fence_after();
+  if (warp == CF::MMA_WARP) pair::tmem_dealloc(tmem, CF::TMEM_COLS);
+}
+
+// Launches the pair kernel: 2 CTAs (one cluster) per 256 query rows of each head.
+template <int D, int DV, bool CAUSAL>
+cudaError_t launch_attn_pair(const LaunchArgs &a) {
+  using CF = PairCfg<D, DV, CAUSAL>;
+  auto kern = attn_fwd_pair_kernel<D, DV, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_TOTAL);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, kern);
+  if (e != cudaSuccess) return e;
+  if (attr.numRegs * CF::THREADS < CF::REGS_NEEDED) return cudaErrorLaunchOutOfResources;
+  const unsigned clusters = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ctas_per_head);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters);
+  cfg.blockDim = dim3(CF::THREADS);
+  cfg.dynamicSmemBytes = CF::SMEM_TOTAL;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = 2;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kern, a.tmQ, a.tmK, a.tmV, a.p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace eta
