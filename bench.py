@@ -58,7 +58,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_HBM_GBS = 7900.0
 
 KERNEL_SOURCES = {
-    "forward": ["attn_fwd_kernel.cuh", "ptx.cuh"],
+    "forward": ["attn_fwd_kernel.cuh", "attn_fwd_pair_kernel.cuh", "ptx.cuh"],
     "split": ["attn_fwd_kernel.cuh", "attn_merge_kernel.cuh", "ptx.cuh"],
     "backward": ["attn_bwd_kernel.cuh", "attn_fwd_kernel.cuh", "ptx.cuh"],
 }

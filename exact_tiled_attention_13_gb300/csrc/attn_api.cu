@@ -325,14 +325,14 @@ int head_group(int BH, int Nk, int d, int d_v) {
   return g >= BH ? BH : (g < 1.0 ? 1 : static_cast<int>(g));
 }
 
-// The CTA-pair kernel (attn_fwd_pair_kernel.cuh) can serve the problems without a bias term
-// with 128 value columns, in one key range. It is not dispatched yet: one block per 128
-// query rows pays its start-up and drain per block, which keeps it at the speed of
-// attn_fwd_kernel (a persistent form that overlaps them is the next step).
+// The persistent CTA-pair kernel (attn_fwd_pair_kernel.cuh) serves the causal problems
+// without a bias term with 128 value columns, in one key range; everything else goes to
+// attn_fwd_kernel. The pair kernel computes S ahead of the softmax, so a tile that moves the
+// exponent reference waits for the previous P V before rescaling o; on unmasked rows of
+// large scores (many moves) that costs more than it gains, while attn_fwd_kernel, which
+// computes S(t) only after P(t-1) V, rescales without waiting.
 bool use_pair_kernel(const Problem &a, int n_splits) {
-  (void)a;
-  (void)n_splits;
-  return false;
+  return a.bias() == BIAS_NONE && a.causal() && a.d_v == 128 && n_splits == 1;
 }
 
 // Launches the attention kernel. With n_splits > 1 each CTA covers `split_tiles` K/V

@@ -6,37 +6,48 @@
 // 128-key tiles as in attn_fwd_kernel.cuh. What differs is how the work is laid on the
 // chip.
 //
-// A cluster of two CTAs on two SMs owns 256 query rows of one head, 128 in each CTA. The
-// tensor-core products are the pair's (.cta_group::2, M = 256): S = Q K^T with each CTA's
-// Q rows in its own shared memory and the K tile split between the two (64 keys each), and
-// o += P V with each CTA's P in its own tensor memory and the V tile split by columns (64
-// value columns each). So each SM stages and streams half of every K and V tile: half the
-// shared-memory operand traffic and half the L2 traffic per SM of one CTA doing all 128
-// keys, at the same tensor rate.
+// A cluster of two CTAs on two SMs owns 256 query rows of one head at a time (a unit), 128
+// in each CTA. The tensor-core products are the pair's (.cta_group::2, M = 256): S = Q K^T
+// with each CTA's Q rows in its own shared memory and the K tile split between the two (64
+// keys each), and o += P V with each CTA's P in its own tensor memory and the V tile split
+// by columns (64 value columns each). So each SM stages and streams half of every K and V
+// tile: half the shared-memory operand traffic and half the L2 traffic per SM of one CTA
+// doing all 128 keys, at the same tensor rate.
 //
 // One query tile per CTA leaves room in tensor memory (512 columns) for two S buffers, two
 // P buffers (bf16) and o. An S buffer is released as soon as the softmax has loaded it, so
-// the even CTA computes S(t+1) and S(t+2) while the softmax of S(t) runs, and the chain
-// softmax -> P -> P V -> next S no longer serialises the tensor cores (the products of one
-// query tile depend on its softmax only through P).
+// S(t+1) and S(t+2) are computed while the softmax of S(t) runs, and the chain softmax -> P
+// -> P V -> next S no longer serialises the tensor cores (the products of one query tile
+// depend on its softmax only through P).
 //
-// Warp roles (12 warps in each CTA):
-//   softmax, warps 0-7: two warpgroups that take the key tiles in turn (even tiles in the
-//     first, odd tiles in the second); thread = query row = tensor-memory lane, a whole row
-//     of 128 keys per tile. The two warpgroups run out of phase, so one's exponentials
-//     overlap the other's loads and maxima. The recurrence couples consecutive tiles only
-//     through the exponent reference: each warp passes the reference it settled on to the
-//     other warpgroup's warp of the same rows (a word per row in shared memory and an
-//     mbarrier), and keeps its own share of l; the shares are brought to the final
-//     reference and added in the epilogue. The warpgroup whose tile moves the reference
-//     rescales o (all 128 columns of its rows) once the previous P V has completed.
+// The grid is persistent: one cluster per pair of SMs, each taking units in a fixed order
+// (longest first, alternating direction every round of clusters, so the long units spread
+// evenly). Rings, buffers and barrier phases run on across units: the next unit's Q is
+// loaded into the second Q buffer, and its first S products and softmax tiles run while the
+// current unit's epilogue runs; its first P V waits only for the epilogue to have read o.
+//
+// Warp roles (16 warps in each CTA):
+//   softmax, warps 0-7: two warpgroups that take the key tiles in turn (tiles are numbered
+//     across units; even tiles in the first warpgroup, odd ones in the second); thread =
+//     query row = tensor-memory lane, a whole row of 128 keys per tile. The two warpgroups
+//     run out of phase, so one's exponentials overlap the other's loads and maxima. The
+//     recurrence couples consecutive tiles only through the exponent reference: each warp
+//     passes the reference it settled on to the other warpgroup's warp of the same rows (a
+//     word per row in shared memory and an mbarrier), and keeps its own share of l; the
+//     shares are brought to the final reference and added by the epilogue warps. The
+//     warpgroup whose tile moves the reference rescales o (all 128 columns of its rows) once
+//     the previous P V has completed.
+//   epilogue, warps 12-15: per unit, O = o / l staged through the unit's idle Q buffer and
+//     stored as whole 256-byte row segments, and LSE; o is released to the next unit's first
+//     P V as soon as it is in registers, while the softmax warps are already on that unit.
 //   MMA, warps 8 (S products) and 11 (P V products) of the even CTA: issue the pair's
 //     products; each commit signals the mbarrier at the same offset in both CTAs
 //     (multicast). S(t) waits for the softmax to have loaded S(t-2) from its buffer.
 //   Q/K load (warp 9) and V load (warp 10) of both CTAs: TMA copies of this CTA's halves;
 //     completion is signalled on the even CTA's full barriers, whose expected byte count
-//     covers both halves, so the MMA warp waits once per tile.
-// Every mbarrier wait is bounded in time, as in attn_fwd_kernel.cuh.
+//     covers both halves, so an MMA warp waits once per tile.
+// Every wait is an mbarrier wait bounded in time, as in attn_fwd_kernel.cuh (no named
+// barriers: a warp that gave up cannot leave another waiting forever).
 #pragma once
 
 #include "attn_fwd_kernel.cuh"
@@ -48,6 +59,8 @@ struct PairCfg {
   static_assert(D == 64 || D == 128, "d must be 64 or 128");
   static_assert(DV == 128, "the pair kernel splits 128 value columns in two 128-byte halves");
   static constexpr int Q_TILE = BM * D * 2;       // this CTA's 128 query rows
+  static constexpr int STAGE = 4 * 32 * 256;      // epilogue stage: 32 rows x 256 bytes per epilogue warp
+  static constexpr int Q_BUF = Q_TILE > STAGE ? Q_TILE : STAGE;
   static constexpr int KH_ROWS = BN / 2;          // keys of a K tile held by one CTA
   static constexpr int KH_BOX = KH_ROWS * 128;    // one 64-row x 128-byte box
   static constexpr int KH_TILE = KH_ROWS * D * 2;
@@ -57,44 +70,48 @@ struct PairCfg {
   static constexpr int KS = 4;
   static constexpr int VS = 4;
   static_assert(VS >= 3, "the softmax tells P(t) V apart by the phase of its V slot");
-  static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + Q_TILE;
+  static constexpr int Q_OFF = 0;                 // two Q buffers: unit k uses buffer k % 2
+  static constexpr int K_OFF = Q_OFF + 2 * Q_BUF;
   static constexpr int V_OFF = K_OFF + KS * KH_TILE;
-  static constexpr int RX_OFF = V_OFF + VS * VH_TILE;     // references passed on, 2 x 128 fp32
-  static constexpr int LX_OFF = RX_OFF + 2 * BM * 4;       // shares of l, 2 x 2 x 128 fp32
-  static constexpr int BAR_OFF = LX_OFF + 2 * 2 * BM * 4;
-  static constexpr int B_QFULL = 0;
-  static constexpr int B_KFULL = 1;
+  static constexpr int RX_OFF = V_OFF + VS * VH_TILE;  // references passed on, 2 x 128 fp32
+  static constexpr int LX_OFF = RX_OFF + 2 * BM * 4;    // per unit % 2: [m, l, l'][2 warpgroups][128 rows]
+  static constexpr int BAR_OFF = LX_OFF + 2 * 3 * 2 * BM * 4;
+  static constexpr int B_QFULL = 0;               // 2: Q of the unit in buffer 0 / 1 landed (both CTAs)
+  static constexpr int B_QEMPTY = B_QFULL + 2;    // 2: buffer read by its unit's last S and used by its epilogue (5)
+  static constexpr int B_KFULL = B_QEMPTY + 2;
   static constexpr int B_KEMPTY = B_KFULL + KS;
   static constexpr int B_VFULL = B_KEMPTY + KS;
   static constexpr int B_VEMPTY = B_VFULL + VS;   // P(t) V done (V slot free, P buffer free, o holds P(t) V)
   static constexpr int B_SFULL = B_VEMPTY + VS;   // S(t) computed (both CTAs)
   static constexpr int B_SEMPTY = B_SFULL + NS;   // S(t) loaded by the 4 softmax warps of each CTA (even CTA)
   static constexpr int B_PFULL = B_SEMPTY + NS;   // P(t) written by the 4 softmax warps of each CTA (even CTA)
-  static constexpr int B_OFULL = B_PFULL + NS;    // last P V done
-  static constexpr int B_DRAIN = B_OFULL + 1;     // products of the S issuer drained
+  static constexpr int B_OFULL = B_PFULL + NS;    // a unit's last P V done
+  static constexpr int B_OEMPTY = B_OFULL + 1;    // o read by the unit's epilogue, 4 warps x 2 CTAs (even CTA)
+  static constexpr int B_DRAIN = B_OEMPTY + 1;    // products of the S issuer drained
   static constexpr int B_DRAIN2 = B_DRAIN + 1;    // products of the P V issuer drained
-  static constexpr int B_HREF = B_DRAIN2 + 1;      // reference passed on by warpgroup g, warp q: 4 g + q
-  static constexpr int NUM_BARS = B_HREF + 8;
+  static constexpr int B_HREF = B_DRAIN2 + 1;     // 8: reference passed on by warpgroup g, warp q (4 g + q)
+  static constexpr int B_LDONE = B_HREF + 8;      // 2: a unit's (m, l, l') per row written by the 8 softmax warps
+  static constexpr int B_LEMPTY = B_LDONE + 2;    // 2: read by the 4 epilogue warps
+  static constexpr int NUM_BARS = B_LEMPTY + 2;
   static constexpr int TMEMPTR_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = TMEMPTR_OFF + 4;
   static constexpr int SMEM_USED = ABORT_OFF + 4;
   // At least 120 KB so one CTA holds an SM (it allocates all of the SM's tensor memory).
   static constexpr int SMEM_TOTAL = SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
   static_assert(SMEM_TOTAL <= 232448, "shared memory over the sm_103a per-CTA limit");
-  static_assert(KS * KH_TILE + VS * VH_TILE >= 8 * 32 * 128,
-                "the idle K and V rings stage 32 rows x 128 bytes per softmax warp");
 
-  static constexpr int MMA_WARP = 8;
+  static constexpr int MMA_WARP = 8;    // issues the S products
   static constexpr int LOAD_WARP = 9;   // Q and K
   static constexpr int VLOAD_WARP = 10; // V
-  static constexpr int PV_WARP = 11;    // issues the P V products (MMA_WARP issues S)
-  static constexpr int NUM_WARPS = 12;
+  static constexpr int PV_WARP = 11;    // issues the P V products
+  static constexpr int EPI_WARP0 = 12;  // warps 12-15: epilogue
+  static constexpr int NUM_WARPS = 16;
   static constexpr int THREADS = 32 * NUM_WARPS;
   static constexpr int LAUNCH_REGS = (65536 / THREADS) / 8 * 8;
-  static constexpr int REGS_SOFTMAX = 216;
-  static constexpr int REGS_CTRL = 72;
-  static constexpr int REGS_NEEDED = 128 * (2 * REGS_SOFTMAX + REGS_CTRL);
+  static constexpr int REGS_SOFTMAX = 176;
+  static constexpr int REGS_CTRL = 80;
+  static constexpr int REGS_EPI = 80;
+  static constexpr int REGS_NEEDED = 128 * (2 * REGS_SOFTMAX + REGS_CTRL + REGS_EPI);
   static_assert(REGS_NEEDED <= THREADS * LAUNCH_REGS,
                 "register split exceeds the registers the block is launched with");
   // Tensor memory: S(t) in buffer t % 2, P(t) (bf16 pairs, 64 columns) in its own buffer
@@ -109,16 +126,16 @@ struct PairCfg {
   static constexpr uint32_t IDESC_PV = idesc_bf16_f32(2 * BM, DV, true);
 };
 
-// The pair's schedule: query rows [256 pt, 256 pt + 256) of head bh, this CTA's 128 of them
-// in query tile qt; K/V tiles hi_max down to 0 (the pair's last row decides hi_max, so the
-// even CTA's rows may meet a last tile that is wholly above their causal limit: its scores
-// are all masked and its P is 0).
+// One unit: query rows [256 pt, 256 pt + 256) of head bh, this CTA's 128 of them in query
+// tile qt; K/V tiles hi_max down to 0 (the pair's last row decides hi_max, so the even
+// CTA's rows may meet a last tile that is wholly above their causal limit: its scores are
+// all masked and its P is 0).
 template <bool CAUSAL>
 struct PairSchedule {
   int bh, pt, qt, hi_max, n_it;
-  __device__ PairSchedule(const KernelParams &p, unsigned cluster, unsigned rank) {
+  __device__ PairSchedule(const KernelParams &p, unsigned unit, unsigned rank) {
     int r;
-    unit_of_block(cluster, p.BH, p.ctas_per_head, p.head_group, &bh, &r);
+    unit_of_block(unit, p.BH, p.ctas_per_head, p.head_group, &bh, &r);
     pt = p.ctas_per_head - 1 - r;  // longest first
     qt = 2 * pt + static_cast<int>(rank);
     const int top = p.nkv_tiles - 1;
@@ -131,6 +148,13 @@ struct PairSchedule {
     n_it = hi_max >= 0 ? hi_max + 1 : 0;
   }
 };
+
+// The k-th unit of cluster c among C: the units in grid order (longest first), taken a round
+// of C at a time, each round in the opposite direction to the one before. Returns a value
+// >= the number of units when cluster c has no k-th unit.
+__device__ __forceinline__ unsigned pair_unit(int k, unsigned c, unsigned C) {
+  return static_cast<unsigned>(k) * C + ((k & 1) ? (C - 1 - c) : c);
+}
 
 // Waits (bounded) about 20 us: after an abort, copies already issued by this CTA that
 // signal the other CTA's barriers cannot be observed here; give them time to land.
@@ -158,9 +182,10 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
   const int lane = threadIdx.x % 32;
   const uint32_t rank = pair::cluster_rank();
   const bool leader = rank == 0;
-  // The even CTA's copy of a barrier (the one the MMA warp waits on).
+  // The even CTA's copy of a barrier (the one the MMA warps wait on).
   auto LBAR = [&](int i) -> uint32_t { return pair::map_shared(BAR(i), 0); };
-  const PairSchedule<CAUSAL> sch(p, blockIdx.x >> 1, rank);
+  const unsigned cl = blockIdx.x >> 1, n_cl = gridDim.x >> 1;
+  const unsigned n_units = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.ctas_per_head);
   Watchdog wd{sbase + CF::ABORT_OFF, p};
 #ifdef ETA_PHASE_TRACE
   int trace_n = 0;
@@ -168,7 +193,10 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
 
   // ------------------------------------------------------------------ set-up
   if (threadIdx.x == 0) {
-    mbar_init(BAR(CF::B_QFULL), 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(BAR(CF::B_QFULL + q), 1);
+      mbar_init(BAR(CF::B_QEMPTY + q), 1 + 4);  // the last S's commit and this CTA's 4 epilogue warps
+    }
     for (int s = 0; s < CF::KS; ++s) {
       mbar_init(BAR(CF::B_KFULL + s), 1);
       mbar_init(BAR(CF::B_KEMPTY + s), 1);
@@ -183,9 +211,14 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
       mbar_init(BAR(CF::B_PFULL + b), 8);
     }
     mbar_init(BAR(CF::B_OFULL), 1);
+    mbar_init(BAR(CF::B_OEMPTY), 8);  // every epilogue warp of both CTAs
     mbar_init(BAR(CF::B_DRAIN), 1);
     mbar_init(BAR(CF::B_DRAIN2), 1);
     for (int h = 0; h < 8; ++h) mbar_init(BAR(CF::B_HREF + h), 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(BAR(CF::B_LDONE + q), 8);
+      mbar_init(BAR(CF::B_LEMPTY + q), 4);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -207,252 +240,313 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
   if (warp < CF::MMA_WARP) {
     // ================================================================ softmax
     regs_increase<CF::REGS_SOFTMAX>();
-    const int wg = warp / 4;  // this warpgroup takes the tiles it with it % 2 == wg
+    const int wg = warp / 4;  // this warpgroup takes the tiles t with t % 2 == wg
     const int wq = warp % 4;  // tensor-memory lanes [32 wq, 32 wq + 32)
     const int row = 32 * wq + lane;
-    const int q_row = sch.qt * BM + row;
     const uint32_t lane_off = static_cast<uint32_t>(32 * wq) << 16;
     const uint32_t t_o = tmem + lane_off + CF::O_COL;
+    const uint32_t t_s = tmem + lane_off + wg * BN;                 // S(t) for t % 2 == wg
+    const uint32_t t_p = tmem + lane_off + CF::P_COL + wg * (BN / 2);  // P(t) for t % 2 == wg
     float *rx = reinterpret_cast<float *>(smem + CF::RX_OFF);  // [2 warpgroups][128 rows]
-    float *lx = reinterpret_cast<float *>(smem + CF::LX_OFF);  // [2 sums][2 warpgroups][128 rows]
+    float *lx = reinterpret_cast<float *>(smem + CF::LX_OFF);  // [unit % 2][m, l, l'][2 warpgroups][128]
     const int h_mine = CF::B_HREF + 4 * wg + wq;
     const int h_other = CF::B_HREF + 4 * (wg ^ 1) + wq;
     const float sl2 = p.scale_log2;
-    float m_prev = -INFINITY;  // reference of this warpgroup's previous tile, log2(e)-scaled
-    float l = 0.0f;            // this warpgroup's share of l (fp32 p, for LSE), relative to m_prev
-    float lr = 0.0f;           // the same with each tile's largest p as rounded (for O)
     bool ok = true;
-    int j_mask = CAUSAL ? floor_div(sch.qt * BM + p.causal_off + 1, BN) : INT_MAX;
-    if (p.Nk % BN != 0) j_mask = cmin(j_mask, p.nkv_tiles - 1);
-    const int lim = CAUSAL ? cmin(q_row + p.causal_off, p.Nk - 1) : p.Nk - 1;
+    int g0 = 0;  // global number of this unit's first tile
 
-    for (int it = wg; it < sch.n_it; it += 2) {
-      const int b = it % CF::NS;  // = wg: each warpgroup has its S and P buffers
-      const int j = sch.hi_max - it;
-      const uint32_t t_s = tmem + lane_off + b * BN;
-      const uint32_t t_p = tmem + lane_off + CF::P_COL + b * (BN / 2);
-      ok = wd.wait(BAR(CF::B_SFULL + b), (it / CF::NS) & 1, ROLE_SOFTMAX, CF::B_SFULL + b);
-      if (!ok) break;
-      tc_fence_after();
-      ETA_TRACE(1);
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(t_s + 0, r0);
-      tmem_ld32(t_s + 32, r1);
-      tmem_ld32(t_s + 64, r2);
-      tmem_ld32(t_s + 96, r3);
-      tmem_wait_ld(r0);
-      tmem_wait_ld(r1);
-      tmem_wait_ld(r2);
-      tmem_wait_ld(r3);
-      // S(it) is in registers: its buffer may take S(it + 2).
-      tc_fence_before();
-      __syncwarp();
-      if (leader) mbar_arrive_elect(BAR(CF::B_SEMPTY + b));
-      else pair::mbar_arrive_cluster_elect(LBAR(CF::B_SEMPTY + b));
-      float x[BN];
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        x[c] = __uint_as_float(r0[c]);
-        x[32 + c] = __uint_as_float(r1[c]);
-        x[64 + c] = __uint_as_float(r2[c]);
-        x[96 + c] = __uint_as_float(r3[c]);
-      }
-      if (j >= j_mask) {
-        const int lim_j = lim - j * BN;
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c > lim_j) x[c] = -INFINITY;
-      }
-      const float bt = row_max128(x);
-      ETA_TRACE(2);
-      // The reference after tile it - 1, from the other warpgroup; then this tile's: moved
-      // to b_t only when b_t exceeds it by more than RESCALE_TAU (log2 units), as in
-      // attn_fwd_kernel.cuh. It is passed on at once: the other warpgroup's next tile waits
-      // for it, and nothing else.
-      float m_in = -INFINITY;
-      if (it > 0) {
-        ok = wd.wait(BAR(h_other), ((it - 1) >> 1) & 1, ROLE_SOFTMAX, h_other);
-        if (!ok) break;
-        m_in = rx[(wg ^ 1) * BM + row];
-      }
-      const float bs = bt * sl2;
-      const bool move = bs > m_in + RESCALE_TAU;  // also the first allowed key (m_in = -inf)
-      const float m_new = move ? bs : m_in;
-      rx[wg * BM + row] = m_new;
-      __syncwarp();
-      mbar_arrive_elect(BAR(h_mine));
-      ETA_TRACE(3);
-      // No allowed key seen yet: every p is 0; use 0 as reference.
-      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-      // P buffer b was last read by P(it-2) V. (VS >= 3: P(it-2-VS) V completed before this
-      // warpgroup's previous tile, P(it-2+VS) V needs a later P of its own.)
-      if (it >= CF::NS) {
-        const int pv = it - CF::NS;
-        ok = wd.wait(BAR(CF::B_VEMPTY + pv % CF::VS), (pv / CF::VS) & 1, ROLE_SOFTMAX, CF::B_VEMPTY + pv % CF::VS);
+    for (int k = 0; ok; ++k) {
+      const unsigned unit = pair_unit(k, cl, n_cl);
+      if (unit >= n_units) break;
+      const PairSchedule<CAUSAL> sch(p, unit, rank);
+      const int q_row = sch.qt * BM + row;
+      int j_mask = CAUSAL ? floor_div(sch.qt * BM + p.causal_off + 1, BN) : INT_MAX;
+      if (p.Nk % BN != 0) j_mask = cmin(j_mask, p.nkv_tiles - 1);
+      const int lim = CAUSAL ? cmin(q_row + p.causal_off, p.Nk - 1) : p.Nk - 1;
+      float m_prev = -INFINITY;  // reference of this warpgroup's previous tile, log2(e)-scaled
+      float l = 0.0f;            // this warpgroup's share of l (fp32 p, for LSE), relative to m_prev
+      float lr = 0.0f;           // the same with each tile's largest p as rounded (for O)
+
+      for (int t = g0 + ((wg - g0) & 1); t < g0 + sch.n_it; t += 2) {
+        const int j = sch.hi_max - (t - g0);
+        ok = wd.wait(BAR(CF::B_SFULL + wg), (t >> 1) & 1, ROLE_SOFTMAX, CF::B_SFULL + wg);
         if (!ok) break;
         tc_fence_after();
-      }
-      // p_ij = 2^(x scale log2e - m) as bf16 into the P buffer, 32 keys at a time; the row
-      // sum runs alongside in four independent packed chains.
-      const float neg_m = -m_use;
-      float s[8];
+        ETA_TRACE(1);
+        // The loads return each 32-key quarter's maximum with the values.
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        float mx0 = tmem_ld32_max(t_s + 0, r0);
+        float mx1 = tmem_ld32_max(t_s + 32, r1);
+        float mx2 = tmem_ld32_max(t_s + 64, r2);
+        float mx3 = tmem_ld32_max(t_s + 96, r3);
+        tmem_wait_ld_max(r0, mx0);
+        tmem_wait_ld_max(r1, mx1);
+        tmem_wait_ld_max(r2, mx2);
+        tmem_wait_ld_max(r3, mx3);
+        // S(t) is in registers: its buffer may take S(t + 2).
+        tc_fence_before();
+        __syncwarp();
+        if (leader) mbar_arrive_elect(BAR(CF::B_SEMPTY + wg));
+        else pair::mbar_arrive_cluster_elect(LBAR(CF::B_SEMPTY + wg));
+        float x[BN];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) s[k] = 0.0f;
-      uint32_t pk[32];
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-#pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          const int c = 32 * qq + 2 * c2;
-          float a0, a1;
-          fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg_m, neg_m);
-          const float p0 = ex2_approx(a0);
-          const float p1 = ex2_approx(a1);
-          const int k = 2 * (c2 & 3);
-          add2(s[k], s[k + 1], s[k], s[k + 1], p0, p1);
-          pk[16 * (qq & 1) + c2] = pack_bf16(p0, p1);
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(r0[c]);
+          x[32 + c] = __uint_as_float(r1[c]);
+          x[64 + c] = __uint_as_float(r2[c]);
+          x[96 + c] = __uint_as_float(r3[c]);
         }
-        if (qq & 1) tmem_st32(t_p + 32 * (qq / 2), pk);
+        float bt;
+        if (j >= j_mask) {  // the causal diagonal or the ragged last tile: mask, then the maximum
+          const int lim_j = lim - j * BN;
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c > lim_j) x[c] = -INFINITY;
+          bt = row_max128(x);
+        } else {
+          bt = fmaxf(fmax3(mx0, mx1, mx2), mx3);
+        }
+        ETA_TRACE(2);
+        // The reference after tile t - 1 (from the other warpgroup; none at a unit's first
+        // tile), then this tile's: moved to b_t only when b_t exceeds it by more than
+        // RESCALE_TAU (log2 units), as in attn_fwd_kernel.cuh. It is passed on at once: the
+        // other warpgroup's next tile waits for it, and nothing else. Every tile but the very
+        // first waits for its predecessor's, so the phases of the two barriers stay in step.
+        float m_in = -INFINITY;
+        if (t > 0) {
+          ok = wd.wait(BAR(h_other), ((t - 1) >> 1) & 1, ROLE_SOFTMAX, h_other);
+          if (!ok) break;
+          if (t > g0) m_in = rx[(wg ^ 1) * BM + row];
+        }
+        const float bs = bt * sl2;
+        const bool move = bs > m_in + RESCALE_TAU;  // also the first allowed key (m_in = -inf)
+        const float m_new = move ? bs : m_in;
+        rx[wg * BM + row] = m_new;
+        __syncwarp();
+        mbar_arrive_elect(BAR(h_mine));
+        ETA_TRACE(3);
+        // No allowed key seen yet: every p is 0; use 0 as reference.
+        const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+        // P buffer wg was last read by P(t-2) V. (VS >= 3: P(t-2-VS) V completed before this
+        // warpgroup's previous tile, P(t-2+VS) V needs a later P of its own.)
+        if (t >= CF::NS) {
+          const int pv = t - CF::NS;
+          ok = wd.wait(BAR(CF::B_VEMPTY + pv % CF::VS), (pv / CF::VS) & 1, ROLE_SOFTMAX, CF::B_VEMPTY + pv % CF::VS);
+          if (!ok) break;
+          tc_fence_after();
+        }
+        // p_ij = 2^(x scale log2e - m) as bf16 into the P buffer, 32 keys at a time; the row
+        // sum runs alongside in four independent packed chains.
+        const float neg_m = -m_use;
+        float s[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) s[c] = 0.0f;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c2 = 0; c2 < 16; ++c2) {
+            const int c = 32 * qq + 2 * c2;
+            float a0, a1;
+            fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg_m, neg_m);
+            const float p0 = ex2_approx(a0);
+            const float p1 = ex2_approx(a1);
+            const int e = 2 * (c2 & 3);
+            add2(s[e], s[e + 1], s[e], s[e + 1], p0, p1);
+            pk[c2] = pack_bf16(p0, p1);
+          }
+          tmem_st16(t_p + 16 * qq, pk);
+        }
+        if (__any_sync(0xFFFFFFFFu, move && m_in != -INFINITY)) {
+          // o (after P(t-1) V) is relative to m_in: o_t = alpha_t o_{t-1} needs that product
+          // complete, which the wait here overlaps with the exponentials above; P(t) V, which
+          // adds to o, waits for this tile's arrival below. Rows that saw no allowed key yet
+          // have o = 0. (VS >= 3: P(t-1-VS) V completed before P(t-2) V, waited above;
+          // P(t-1+VS) V needs a later P of this warpgroup.)
+          const int pv = t - 1;
+          ok = wd.wait(BAR(CF::B_VEMPTY + pv % CF::VS), (pv / CF::VS) & 1, ROLE_SOFTMAX, CF::B_VEMPTY + pv % CF::VS);
+          if (!ok) break;
+          tc_fence_after();
+          const float alpha_o = move ? ex2_approx(m_in - m_use) : 1.0f;
+#pragma unroll
+          for (int cc = 0; cc < DV / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(t_o + 32 * cc, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              float f0, f1;
+              mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), alpha_o, alpha_o);
+              o[c] = __float_as_uint(f0);
+              o[c + 1] = __float_as_uint(f1);
+            }
+            tmem_st32(t_o + 32 * cc, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (leader) mbar_arrive_elect(BAR(CF::B_PFULL + wg));
+        else pair::mbar_arrive_cluster_elect(LBAR(CF::B_PFULL + wg));
+        ETA_TRACE(4);
+
+        add2(s[0], s[1], s[0], s[1], s[2], s[3]);
+        add2(s[4], s[5], s[4], s[5], s[6], s[7]);
+        add2(s[0], s[1], s[0], s[1], s[4], s[5]);
+        const float tile_sum = s[0] + s[1];
+        // The tile's largest p as rounded to bf16 joins O's denominator (see
+        // attn_fwd_kernel.cuh); this warpgroup's shares move from m_prev to the new reference.
+        const float pmax = ex2_approx(fmaf(bt, sl2, neg_m));
+        const float corr = __uint_as_float(pack_bf16(pmax, pmax) << 16) - pmax;
+        const float alpha = ex2_approx(m_prev - m_use);  // 1 when the reference stayed; 0 from -inf
+        l = fmaf(alpha, l, tile_sum);
+        lr = fmaf(alpha, lr, tile_sum + corr);
+        m_prev = m_new;
+        ETA_TRACE(5);
       }
-      if (__any_sync(0xFFFFFFFFu, move && m_in != -INFINITY)) {
-        // o (after P(it-1) V) is relative to m_in: o_t = alpha_t o_{t-1} needs that product
-        // complete, which the wait here overlaps with the exponentials above; P(it) V, which
-        // adds to o, waits for this tile's arrival below. Rows that saw no allowed key yet
-        // have o = 0. (VS >= 3: P(it-1-VS) V completed before P(it-2) V, waited above;
-        // P(it-1+VS) V needs a later P of this warpgroup.)
-        const int pv = it - 1;
-        ok = wd.wait(BAR(CF::B_VEMPTY + pv % CF::VS), (pv / CF::VS) & 1, ROLE_SOFTMAX, CF::B_VEMPTY + pv % CF::VS);
+      if (!ok) break;
+
+      // The unit's row statistics go to the epilogue warps, which bring both warpgroups'
+      // shares of l to the final reference (the larger of the two: the reference only
+      // moves up) while these warps go on with the next unit.
+      if (k >= 2) {
+        ok = wd.wait(BAR(CF::B_LEMPTY + (k & 1)), ((k >> 1) & 1) ^ 1, ROLE_SOFTMAX, CF::B_LEMPTY + (k & 1));
+        if (!ok) break;
+      }
+      float *lxk = lx + (k & 1) * (3 * 2 * BM);
+      lxk[(0 * 2 + wg) * BM + row] = m_prev;
+      lxk[(1 * 2 + wg) * BM + row] = l;
+      lxk[(2 * 2 + wg) * BM + row] = lr;
+      __syncwarp();
+      mbar_arrive_elect(BAR(CF::B_LDONE + (k & 1)));
+      g0 += sch.n_it;
+    }
+  } else if (warp >= CF::EPI_WARP0) {
+    // ================================================================ epilogue
+    // O = o_T / l_T and LSE for each unit, in unit order: the rows of lanes [32 e, 32 e + 32).
+    regs_decrease<CF::REGS_EPI>();
+    const int e = warp - CF::EPI_WARP0;
+    const int row = 32 * e + lane;
+    const uint32_t t_o = tmem + (static_cast<uint32_t>(32 * e) << 16) + CF::O_COL;
+    const float *lx = reinterpret_cast<const float *>(smem + CF::LX_OFF);
+    bool ok = true;
+    int n_o = 0;  // units so far whose o was written (phases of B_OFULL / B_OEMPTY)
+    for (int k = 0; ok; ++k) {
+      const unsigned unit = pair_unit(k, cl, n_cl);
+      if (unit >= n_units) break;
+      const PairSchedule<CAUSAL> sch(p, unit, rank);
+      const int q_row = sch.qt * BM + row;
+      ok = wd.wait(BAR(CF::B_LDONE + (k & 1)), (k >> 1) & 1, ROLE_SOFTMAX, CF::B_LDONE + (k & 1));
+      if (!ok) break;
+      const float *lxk = lx + (k & 1) * (3 * 2 * BM);
+      const float m0 = lxk[(0 * 2 + 0) * BM + row], m1 = lxk[(0 * 2 + 1) * BM + row];
+      const float l0 = lxk[(1 * 2 + 0) * BM + row], l1 = lxk[(1 * 2 + 1) * BM + row];
+      const float lr0 = lxk[(2 * 2 + 0) * BM + row], lr1 = lxk[(2 * 2 + 1) * BM + row];
+      __syncwarp();
+      mbar_arrive_elect(BAR(CF::B_LEMPTY + (k & 1)));
+      const float m_last = fmaxf(m0, m1);
+      const float m_use = (m_last == -INFINITY) ? 0.0f : m_last;
+      const float f0 = ex2_approx(m0 - m_use), f1 = ex2_approx(m1 - m_use);  // 0 for a share of -inf
+      const float l_row = fmaf(l0, f0, l1 * f1);
+      const float lr_row = fmaf(lr0, f0, lr1 * f1);
+      const float inv_l = (lr_row > 0.0f) ? 1.0f / lr_row : 0.0f;  // no allowed key: O = 0
+      const int row0 = q_row - lane;
+      const int rows_ok = p.Nq - row0 < 32 ? (p.Nq - row0 > 0 ? p.Nq - row0 : 0) : 32;
+      const size_t obase = (static_cast<size_t>(sch.bh) * p.Nq + row0) * DV;
+      const int esz = p.out_f32 ? 4 : 2;
+      if (sch.n_it == 0) {
+        // A unit whose rows see no key: O = 0, written directly (its Q copy, which no product
+        // waited for, may still be landing in the buffer the others stage through).
+        if (q_row < p.Nq) {
+          uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(p.O) + (obase + static_cast<size_t>(lane) * DV) * esz);
+          for (int v = 0; v < DV * esz / 16; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else {
+        ok = wd.wait(BAR(CF::B_OFULL), n_o & 1, ROLE_SOFTMAX, CF::B_OFULL);
         if (!ok) break;
         tc_fence_after();
-        const float alpha_o = move ? ex2_approx(m_in - m_use) : 1.0f;
+        // The unit's Q buffer is idle once its last S completed (and is reloaded only after
+        // this epilogue releases it): each warp stages 32 rows x 256 bytes there at a time, in
+        // 16-byte units at (unit ^ row % 8) so neither side has bank conflicts, and stores them
+        // as whole 256-byte row segments, two rows per instruction.
+        uint8_t *stage = smem + CF::Q_OFF + (k & 1) * CF::Q_BUF + e * (32 * 256);
+        uint4 *srow = reinterpret_cast<uint4 *>(stage + lane * 256);
+        const int sub = lane % 16;
+        auto store_stage = [&](uint8_t *g, int row_bytes) {
+          __syncwarp();
 #pragma unroll
-        for (int cc = 0; cc < DV / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(t_o + 32 * cc, o);
+          for (int quarter = 0; quarter < 4; ++quarter) {
+            uint4 val[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = 8 * quarter + 2 * i + lane / 16;
+              val[i] = *reinterpret_cast<const uint4 *>(stage + rr * 256 + 16 * (sub ^ (rr & 7)));
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int rr = 8 * quarter + 2 * i + lane / 16;
+              if (rr < rows_ok)
+                *reinterpret_cast<uint4 *>(g + static_cast<size_t>(rr) * row_bytes + 16 * sub) = val[i];
+            }
+          }
+          __syncwarp();
+        };
+        // o / l for 32 columns, in place.
+        auto load_o = [&](int col, uint32_t (&o)[32]) {
+          tmem_ld32(t_o + col, o);
           tmem_wait_ld(o);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             float f0, f1;
-            mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), alpha_o, alpha_o);
+            mul2(f0, f1, __uint_as_float(o[c]), __uint_as_float(o[c + 1]), inv_l, inv_l);
             o[c] = __float_as_uint(f0);
             o[c + 1] = __float_as_uint(f1);
           }
-          tmem_st32(t_o + 32 * cc, o);
-        }
-      }
-
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (leader) mbar_arrive_elect(BAR(CF::B_PFULL + b));
-      else pair::mbar_arrive_cluster_elect(LBAR(CF::B_PFULL + b));
-      ETA_TRACE(4);
-
-      add2(s[0], s[1], s[0], s[1], s[2], s[3]);
-      add2(s[4], s[5], s[4], s[5], s[6], s[7]);
-      add2(s[0], s[1], s[0], s[1], s[4], s[5]);
-      const float tile_sum = s[0] + s[1];
-      // The tile's largest p as rounded to bf16 joins O's denominator (see
-      // attn_fwd_kernel.cuh); this warpgroup's shares move from m_prev to the new reference.
-      const float pmax = ex2_approx(fmaf(bt, sl2, neg_m));
-      const float corr = __uint_as_float(pack_bf16(pmax, pmax) << 16) - pmax;
-      const float alpha = ex2_approx(m_prev - m_use);  // 1 when the reference stayed; 0 from -inf
-      l = fmaf(alpha, l, tile_sum);
-      lr = fmaf(alpha, lr, tile_sum + corr);
-      m_prev = m_new;
-      ETA_TRACE(5);
-    }
-
-    // ------------------------------------------------ epilogue: O = o_T / l_T, LSE
-    // The reference after the last tile (passed on by the other warpgroup when the last
-    // tile was its), both shares of l brought to it and added.
-    float m_last = m_prev;
-    if (ok && sch.n_it > 0 && ((sch.n_it - 1) & 1) != wg) {
-      ok = wd.wait(BAR(h_other), ((sch.n_it - 1) >> 1) & 1, ROLE_SOFTMAX, h_other);
-      if (ok) m_last = rx[(wg ^ 1) * BM + row];
-    }
-    {
-      const float f = ex2_approx(m_prev - (m_last == -INFINITY ? 0.0f : m_last));
-      l *= f;
-      lr *= f;
-    }
-    if (ok && sch.n_it > 0) ok = wd.wait(BAR(CF::B_OFULL), 0, ROLE_SOFTMAX, CF::B_OFULL);
-    lx[(0 * 2 + wg) * BM + row] = l;
-    lx[(1 * 2 + wg) * BM + row] = lr;
-    const int half = wg;  // this warpgroup stores O's columns [64 half, 64 half + 64)
-    if (pair::bar_and(1 + wq, 64, ok)) {
-      if (sch.n_it > 0) tc_fence_after();
-      const float l_row = l + lx[(0 * 2 + (wg ^ 1)) * BM + row];
-      const float lr_row = lr + lx[(1 * 2 + (wg ^ 1)) * BM + row];
-      const float inv_l = (lr_row > 0.0f) ? 1.0f / lr_row : 0.0f;  // no allowed key: O = 0
-      const uint32_t t_oh = t_o + 64 * half;
-      // The K and V rings are idle once the last product completed: each warp stages 32 rows x 128
-      // bytes there at a time, in 16-byte units at (unit ^ row % 8) so neither side has bank
-      // conflicts, and stores them as whole 128-byte row segments, four rows per instruction.
-      uint8_t *stage = smem + CF::K_OFF + warp * (32 * 128);
-      uint4 *srow = reinterpret_cast<uint4 *>(stage + lane * 128);
-      const int row0 = q_row - lane;
-      const int rows_ok = p.Nq - row0 < 32 ? (p.Nq - row0 > 0 ? p.Nq - row0 : 0) : 32;
-      const size_t obase = (static_cast<size_t>(sch.bh) * p.Nq + row0) * DV + 64 * half;
-      const int sub = lane % 8;
-      auto store_stage = [&](uint8_t *g0, int row_bytes) {
-        __syncwarp();
-        uint4 val[8];
+        };
+        // Once o is in registers, the next unit's first P V may overwrite it.
+        auto release_o = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (leader) mbar_arrive_elect(BAR(CF::B_OEMPTY));
+          else pair::mbar_arrive_cluster_elect(LBAR(CF::B_OEMPTY));
+        };
+        if (p.out_f32) {
+#pragma unroll 1
+          for (int pass = 0; pass < 2; ++pass) {  // value columns [64 pass, 64 pass + 64)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + lane / 8;
-          val[i] = *reinterpret_cast<const uint4 *>(stage + rr * 128 + 16 * (sub ^ (rr & 7)));
-        }
-        __syncwarp();
+            for (int h = 0; h < 2; ++h) {
+              uint32_t f[32];
+              load_o(64 * pass + 32 * h, f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int rr = 4 * i + lane / 8;
-          if (rr < rows_ok)
-            *reinterpret_cast<uint4 *>(g0 + static_cast<size_t>(rr) * row_bytes + 16 * sub) = val[i];
-        }
-      };
-      // o of a pair that visited no tile was never written: its rows get O = 0.
-      auto load_o = [&](int col, float (&f)[32]) {
-        uint32_t o[32];
-        if (sch.n_it > 0) {
-          tmem_ld32(t_oh + col, o);
-          tmem_wait_ld(o);
+              for (int v = 0; v < 8; ++v)
+                srow[(8 * h + v) ^ (lane & 7)] = make_uint4(f[4 * v + 0], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
+            }
+            if (pass == 1) release_o();
+            store_stage(reinterpret_cast<uint8_t *>(static_cast<float *>(p.O) + obase + 64 * pass), DV * 4);
+          }
         } else {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) o[c] = 0u;
+          for (int h = 0; h < 4; ++h) {
+            uint32_t f[32];
+            load_o(32 * h, f);
+            auto bf = [&](int c) { return pack_bf16(__uint_as_float(f[c]), __uint_as_float(f[c + 1])); };
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              srow[(4 * h + v) ^ (lane & 7)] = make_uint4(bf(8 * v + 0), bf(8 * v + 2), bf(8 * v + 4), bf(8 * v + 6));
+          }
+          release_o();
+          store_stage(reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.O) + obase), DV * 2);
         }
-#pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          mul2(f[c], f[c + 1], __uint_as_float(o[c]), __uint_as_float(o[c + 1]), inv_l, inv_l);
-      };
-      if (p.out_f32) {
-#pragma unroll 1
-        for (int cc = 0; cc < 2; ++cc) {
-          float f[32];
-          load_o(32 * cc, f);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            srow[v ^ (lane & 7)] = make_uint4(__float_as_uint(f[4 * v + 0]), __float_as_uint(f[4 * v + 1]),
-                                              __float_as_uint(f[4 * v + 2]), __float_as_uint(f[4 * v + 3]));
-          store_stage(reinterpret_cast<uint8_t *>(static_cast<float *>(p.O) + obase + 32 * cc), DV * 4);
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float f[32];
-          load_o(32 * h, f);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            srow[(4 * h + v) ^ (lane & 7)] =
-                make_uint4(pack_bf16(f[8 * v + 0], f[8 * v + 1]), pack_bf16(f[8 * v + 2], f[8 * v + 3]),
-                           pack_bf16(f[8 * v + 4], f[8 * v + 5]), pack_bf16(f[8 * v + 6], f[8 * v + 7]));
-        }
-        store_stage(reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.O) + obase), DV * 2);
+        ++n_o;
       }
       // LSE_i = m_i + ln l_i, from the log2-scaled reference.
-      if (half == 0 && q_row < p.Nq && p.LSE != nullptr)
+      if (q_row < p.Nq && p.LSE != nullptr)
         p.LSE[static_cast<size_t>(sch.bh) * p.Nq + q_row] =
             (l_row > 0.0f) ? (m_last + lg2_approx(l_row)) * LN2 : -INFINITY;
+      // The stage's generic writes come before the next TMA copy into this Q buffer.
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      mbar_arrive_elect(BAR(CF::B_QEMPTY + (k & 1)));
     }
   } else {
     regs_decrease<CF::REGS_CTRL>();
@@ -461,58 +555,78 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
       // Two issuing warps, one for the S products and one for the P V products. The tensor
       // cores take few instructions ahead, so an issuing thread blocks on every product;
       // with one issuer, its waits and commits between products left the pipe idle. Each
-      // commit covers the products of its own thread, so S(it) waits for P(it - NS) V,
-      // which last read its buffer, instead of relying on one thread's issue order.
+      // commit covers the products of its own thread.
       const uint16_t both = 3;
       const bool s_role = warp == CF::MMA_WARP;
       const int drain_bar = s_role ? CF::B_DRAIN : CF::B_DRAIN2;
-      bool ok = wd.wait(BAR(CF::B_QFULL), 0, ROLE_MMA, CF::B_QFULL);
-      if (ok) tc_fence_after();
-      if (s_role) {
-        for (int it = 0; ok && it < sch.n_it; ++it) {
-          const int kslot = it % CF::KS;
-          const int b = it % CF::NS;
-          ok = wd.wait(BAR(CF::B_KFULL + kslot), (it / CF::KS) & 1, ROLE_MMA, CF::B_KFULL + kslot);
-          // Buffer b is free once both CTAs' softmax warps have loaded S(it - NS).
-          if (ok && it >= CF::NS)
-            ok = wd.wait(BAR(CF::B_SEMPTY + b), ((it / CF::NS) & 1) ^ 1, ROLE_MMA, CF::B_SEMPTY + b);
-          if (!ok) break;
-          ETA_TRACE(24);
-          tc_fence_after();
-          const uint64_t a_desc = smem_desc(sbase + CF::Q_OFF, 16, 1024);
-          const uint64_t b_desc = smem_desc(sbase + CF::K_OFF + kslot * CF::KH_TILE, 16, 1024);
-          const uint32_t d_tmem = tmem + b * BN;
+      bool ok = true;
+      int g0 = 0, n_o = 0;
+      for (int k = 0; ok; ++k) {
+        const unsigned unit = pair_unit(k, cl, n_cl);
+        if (unit >= n_units) break;
+        const PairSchedule<CAUSAL> sch(p, unit, rank);
+        const int qb = k & 1;
+        if (s_role) {
+          ok = wd.wait(BAR(CF::B_QFULL + qb), (k >> 1) & 1, ROLE_MMA, CF::B_QFULL + qb);
+          if (ok) tc_fence_after();
+          for (int i = 0; ok && i < sch.n_it; ++i) {
+            const int t = g0 + i;
+            const int kslot = t % CF::KS;
+            const int b = t & 1;
+            ok = wd.wait(BAR(CF::B_KFULL + kslot), (t / CF::KS) & 1, ROLE_MMA, CF::B_KFULL + kslot);
+            // Buffer b is free once both CTAs' softmax warps have loaded S(t - 2).
+            if (ok && t >= CF::NS)
+              ok = wd.wait(BAR(CF::B_SEMPTY + b), ((t >> 1) & 1) ^ 1, ROLE_MMA, CF::B_SEMPTY + b);
+            if (!ok) break;
+            ETA_TRACE(24);
+            tc_fence_after();
+            const uint64_t a_desc = smem_desc(sbase + CF::Q_OFF + qb * CF::Q_BUF, 16, 1024);
+            const uint64_t b_desc = smem_desc(sbase + CF::K_OFF + kslot * CF::KH_TILE, 16, 1024);
+            const uint32_t d_tmem = tmem + b * BN;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t a_off = ((ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32) >> 4;
-            const uint32_t b_off = ((ks / 4) * CF::KH_BOX + (ks % 4) * 32) >> 4;
-            pair::mma_ss_elect(d_tmem, a_desc + a_off, b_desc + b_off, CF::IDESC_S, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < D / 16; ++ks) {
+              const uint32_t a_off = ((ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32) >> 4;
+              const uint32_t b_off = ((ks / 4) * CF::KH_BOX + (ks % 4) * 32) >> 4;
+              pair::mma_ss_elect(d_tmem, a_desc + a_off, b_desc + b_off, CF::IDESC_S, ks > 0 ? 1u : 0u);
+            }
+            ETA_TRACE(25);
+            pair::mma_commit_multicast_elect(BAR(CF::B_SFULL + b), both);
+            pair::mma_commit_multicast_elect(BAR(CF::B_KEMPTY + kslot), both);
           }
-          ETA_TRACE(25);
-          pair::mma_commit_multicast_elect(BAR(CF::B_SFULL + b), both);
-          pair::mma_commit_multicast_elect(BAR(CF::B_KEMPTY + kslot), both);
-        }
-      } else {
-        for (int it = 0; ok && it < sch.n_it; ++it) {
-          const int b = it % CF::NS;
-          const int vslot = it % CF::VS;
-          ETA_TRACE(20);
-          ok = wd.wait(BAR(CF::B_PFULL + b), (it / CF::NS) & 1, ROLE_MMA, CF::B_PFULL + b);
-          ETA_TRACE(21);
-          if (ok) ok = wd.wait(BAR(CF::B_VFULL + vslot), (it / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
-          if (!ok) break;
-          ETA_TRACE(22);
-          tc_fence_after();
-          const uint64_t b_desc = smem_desc(sbase + CF::V_OFF + vslot * CF::VH_TILE, SW_CHUNK_BYTES, 1024);
-          const uint32_t a_tmem = tmem + CF::P_COL + b * (BN / 2);
+          // The unit's Q buffer is no longer read (its epilogue then stages O there).
+          if (ok) pair::mma_commit_multicast_elect(BAR(CF::B_QEMPTY + qb), both);
+        } else {
+          for (int i = 0; ok && i < sch.n_it; ++i) {
+            const int t = g0 + i;
+            const int b = t & 1;
+            const int vslot = t % CF::VS;
+            // V and o are usually ready long before P: P, the wait on the critical path, is
+            // taken last so that the product is issued as soon as P arrives.
+            ETA_TRACE(20);
+            ok = wd.wait(BAR(CF::B_VFULL + vslot), (t / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
+            // The unit's first product overwrites o: the previous unit's epilogue has read it.
+            if (ok && i == 0 && n_o > 0)
+              ok = wd.wait(BAR(CF::B_OEMPTY), (n_o - 1) & 1, ROLE_MMA, CF::B_OEMPTY);
+            ETA_TRACE(21);
+            if (ok) ok = wd.wait(BAR(CF::B_PFULL + b), (t >> 1) & 1, ROLE_MMA, CF::B_PFULL + b);
+            if (!ok) break;
+            ETA_TRACE(22);
+            tc_fence_after();
+            const uint64_t b_desc = smem_desc(sbase + CF::V_OFF + vslot * CF::VH_TILE, SW_CHUNK_BYTES, 1024);
+            const uint32_t a_tmem = tmem + CF::P_COL + b * (BN / 2);
 #pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks)
-            pair::mma_ts_elect(tmem + CF::O_COL, a_tmem + 8 * ks, b_desc + ((ks * 16 * 128) >> 4), CF::IDESC_PV,
-                               (it > 0 || ks > 0) ? 1u : 0u);
-          ETA_TRACE(23);
-          pair::mma_commit_multicast_elect(BAR(CF::B_VEMPTY + vslot), both);
+            for (int ks = 0; ks < BN / 16; ++ks)
+              pair::mma_ts_elect(tmem + CF::O_COL, a_tmem + 8 * ks, b_desc + ((ks * 16 * 128) >> 4), CF::IDESC_PV,
+                                 (i > 0 || ks > 0) ? 1u : 0u);
+            ETA_TRACE(23);
+            pair::mma_commit_multicast_elect(BAR(CF::B_VEMPTY + vslot), both);
+          }
+          if (ok && sch.n_it > 0) {
+            pair::mma_commit_multicast_elect(BAR(CF::B_OFULL), both);
+            ++n_o;
+          }
         }
-        if (ok && sch.n_it > 0) pair::mma_commit_multicast_elect(BAR(CF::B_OFULL), both);
+        g0 += sch.n_it;
       }
       // Nothing may still be in flight on the tensor cores when tensor memory is freed.
       pair::mma_commit_multicast_elect(BAR(drain_bar), 1);
@@ -521,31 +635,55 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
       // ============================================================== TMA: Q, K halves
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
-      if (leader) mbar_arrive_expect_tx(BAR(CF::B_QFULL), 2 * CF::Q_TILE);
-      for (int kc = 0; kc < D / SW_CHUNK; ++kc)
-        pair::tma_load_3d(sbase + CF::Q_OFF + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK, sch.qt * BM, sch.bh,
-                          LBAR(CF::B_QFULL));
-      for (int it = 0; it < sch.n_it; ++it) {
-        const int j = sch.hi_max - it;
-        const int ks = it % CF::KS;
-        if (!wd.wait1(BAR(CF::B_KEMPTY + ks), ((it / CF::KS) & 1) ^ 1, ROLE_LOAD, CF::B_KEMPTY + ks, false)) break;
-        if (p.fault == FAULT_SKIP_FIRST_K && it == 0) continue;  // test hook: a wait runs out
-        if (leader) mbar_arrive_expect_tx(BAR(CF::B_KFULL + ks), 2 * CF::KH_TILE);
+      bool ok = true;
+      int g0 = 0;
+      for (int k = 0; ok; ++k) {
+        const unsigned unit = pair_unit(k, cl, n_cl);
+        if (unit >= n_units) break;
+        const PairSchedule<CAUSAL> sch(p, unit, rank);
+        const int qb = k & 1;
+        // Q buffer qb was last used by unit k - 2 (its last S and its epilogue).
+        ok = wd.wait1(BAR(CF::B_QEMPTY + qb), ((k >> 1) & 1) ^ 1, ROLE_LOAD, CF::B_QEMPTY + qb, false);
+        if (!ok) break;
+        if (leader) mbar_arrive_expect_tx(BAR(CF::B_QFULL + qb), 2 * CF::Q_TILE);
         for (int kc = 0; kc < D / SW_CHUNK; ++kc)
-          pair::tma_load_3d(sbase + CF::K_OFF + ks * CF::KH_TILE + kc * CF::KH_BOX, &tmK, kc * SW_CHUNK,
-                            j * BN + CF::KH_ROWS * static_cast<int>(rank), sch.bh, LBAR(CF::B_KFULL + ks));
+          pair::tma_load_3d(sbase + CF::Q_OFF + qb * CF::Q_BUF + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK,
+                            sch.qt * BM, sch.bh, LBAR(CF::B_QFULL + qb));
+        for (int i = 0; i < sch.n_it; ++i) {
+          const int t = g0 + i;
+          const int j = sch.hi_max - i;
+          const int ks = t % CF::KS;
+          ok = wd.wait1(BAR(CF::B_KEMPTY + ks), ((t / CF::KS) & 1) ^ 1, ROLE_LOAD, CF::B_KEMPTY + ks, false);
+          if (!ok) break;
+          if (p.fault == FAULT_SKIP_FIRST_K && t == 0) continue;  // test hook: a wait runs out
+          if (leader) mbar_arrive_expect_tx(BAR(CF::B_KFULL + ks), 2 * CF::KH_TILE);
+          for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+            pair::tma_load_3d(sbase + CF::K_OFF + ks * CF::KH_TILE + kc * CF::KH_BOX, &tmK, kc * SW_CHUNK,
+                              j * BN + CF::KH_ROWS * static_cast<int>(rank), sch.bh, LBAR(CF::B_KFULL + ks));
+        }
+        g0 += sch.n_it;
       }
       if (wd.aborted()) settle_after_abort();
     } else if (warp == CF::VLOAD_WARP && lane == 0) {
       // ============================================================== TMA: V halves
       tma_prefetch_desc(&tmV);
-      for (int it = 0; it < sch.n_it; ++it) {
-        const int j = sch.hi_max - it;
-        const int vs = it % CF::VS;
-        if (!wd.wait1(BAR(CF::B_VEMPTY + vs), ((it / CF::VS) & 1) ^ 1, ROLE_LOAD, CF::B_VEMPTY + vs, false)) break;
-        if (leader) mbar_arrive_expect_tx(BAR(CF::B_VFULL + vs), 2 * CF::VH_TILE);
-        pair::tma_load_3d(sbase + CF::V_OFF + vs * CF::VH_TILE, &tmV, CF::VH_COLS * static_cast<int>(rank),
-                          j * BN, sch.bh, LBAR(CF::B_VFULL + vs));
+      bool ok = true;
+      int g0 = 0;
+      for (int k = 0; ok; ++k) {
+        const unsigned unit = pair_unit(k, cl, n_cl);
+        if (unit >= n_units) break;
+        const PairSchedule<CAUSAL> sch(p, unit, rank);
+        for (int i = 0; i < sch.n_it; ++i) {
+          const int t = g0 + i;
+          const int j = sch.hi_max - i;
+          const int vs = t % CF::VS;
+          ok = wd.wait1(BAR(CF::B_VEMPTY + vs), ((t / CF::VS) & 1) ^ 1, ROLE_LOAD, CF::B_VEMPTY + vs, false);
+          if (!ok) break;
+          if (leader) mbar_arrive_expect_tx(BAR(CF::B_VFULL + vs), 2 * CF::VH_TILE);
+          pair::tma_load_3d(sbase + CF::V_OFF + vs * CF::VH_TILE, &tmV, CF::VH_COLS * static_cast<int>(rank),
+                            j * BN, sch.bh, LBAR(CF::B_VFULL + vs));
+        }
+        g0 += sch.n_it;
       }
       if (wd.aborted()) settle_after_abort();
     }
@@ -554,7 +692,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
 
   // ------------------------------------------------------------------ teardown
   // Neither CTA releases its tensor or shared memory while the pair's products may still
-  // read them: the even CTA's MMA warp has drained its products before it gets here.
+  // read them: the even CTA's MMA warps have drained their products before they get here.
   tc_fence_before();
   __syncthreads();
   pair::cluster_sync();
@@ -562,7 +700,34 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
   if (warp == CF::MMA_WARP) pair::tmem_dealloc(tmem, CF::TMEM_COLS);
 }
 
-// Launches the pair kernel: 2 CTAs (one cluster) per 256 query rows of each head.
+// Clusters that can be resident at once for an instance (looked up once per device).
+template <int D, int DV, bool CAUSAL>
+int pair_max_clusters(int dev) {
+  using CF = PairCfg<D, DV, CAUSAL>;
+  static int cached[64] = {0};
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(CF::THREADS);
+  cfg.dynamicSmemBytes = CF::SMEM_TOTAL;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_fwd_pair_kernel<D, DV, CAUSAL>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    return 0;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+// Launches the persistent pair kernel: min(units, resident clusters) clusters of 2 CTAs.
 template <int D, int DV, bool CAUSAL>
 cudaError_t launch_attn_pair(const LaunchArgs &a) {
   using CF = PairCfg<D, DV, CAUSAL>;
@@ -573,7 +738,13 @@ cudaError_t launch_attn_pair(const LaunchArgs &a) {
   e = cudaFuncGetAttributes(&attr, kern);
   if (e != cudaSuccess) return e;
   if (attr.numRegs * CF::THREADS < CF::REGS_NEEDED) return cudaErrorLaunchOutOfResources;
-  const unsigned clusters = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ctas_per_head);
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int resident = pair_max_clusters<D, DV, CAUSAL>(dev);
+  if (resident < 1) return cudaErrorLaunchOutOfResources;
+  const unsigned units = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ctas_per_head);
+  const unsigned clusters = units < static_cast<unsigned>(resident) ? units : static_cast<unsigned>(resident);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(CF::THREADS);
