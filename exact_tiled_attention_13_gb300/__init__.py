@@ -8,7 +8,7 @@ computation runs in the library's kernel.
 """
 from __future__ import annotations
 
-from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_INVALID_ARG,
+from ._lib import (ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_BIAS_SHARED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_INVALID_ARG,
                    ATTN_ERR_LAUNCH, ATTN_ERR_NO_DEVICE, ATTN_ERR_UNSUPPORTED,
                    ATTN_ERR_UNSUPPORTED_DEVICE, ATTN_FAULT_NONE, ATTN_FAULT_SKIP_FIRST_K,
                    ATTN_MASK_CAUSAL, ATTN_MASK_NONE, ATTN_OK, ATTN_OUT_BF16, ATTN_OUT_F32,
@@ -25,7 +25,7 @@ __all__ = [
     "attn_bwd_host_raw", "attn_bwd_host_staging_bytes", "bwd_host_staging", "attn_bwd",
     "attn_bwd_raw", "attn_bwd_workspace_bytes", "bwd_workspace", "attn_strerror", "attn_device_status", "attn_set_wait_timeout_ns",
     "attn_set_fault_injection", "attn_version", "AttnError", "load", "library_path", "ATTN_MASK_NONE", "ATTN_MASK_CAUSAL",
-    "ATTN_BIAS_DENSE", "ATTN_BIAS_KEY", "ATTN_OUT_BF16", "ATTN_OUT_F32",
+    "ATTN_BIAS_DENSE", "ATTN_BIAS_KEY", "ATTN_BIAS_SHARED", "ATTN_OUT_BF16", "ATTN_OUT_F32",
 ]
 
 attn_strerror = strerror
@@ -45,7 +45,7 @@ def attn_fwd(Q, K, V, mode, C, scale, O, LSE=None, stream=None):
     """Launch O = softmax(Q K^T * scale + C) V (and LSE) through the C ABI.
 
     Q, K: bf16 CUDA tensors [BH, N, d]; V: bf16 [BH, N, d_v]; C: fp32 [BH, N, N] for
-    mode ATTN_BIAS_DENSE, else None; O: bf16 or fp32 [BH, N, d_v]; LSE: fp32 [BH, N] or
+    mode ATTN_BIAS_DENSE ([N, N] with ATTN_BIAS_SHARED), else None; O: bf16 or fp32 [BH, N, d_v]; LSE: fp32 [BH, N] or
     None. All contiguous. `stream`: torch.cuda.Stream, a raw handle, or None for the
     current stream. Raises AttnError with the library's code on failure.
     """
@@ -65,8 +65,9 @@ def attn_fwd(Q, K, V, mode, C, scale, O, LSE=None, stream=None):
     out_dtype = ATTN_OUT_F32 if O.dtype == torch.float32 else ATTN_OUT_BF16
     c_ptr = None
     if C is not None:
-        if C.dtype != torch.float32 or tuple(C.shape) != (BH, N, N) or not C.is_contiguous():
-            raise ValueError("C must be a contiguous fp32 [BH, N, N] tensor")
+        c_shape = (N, N) if mode & ATTN_BIAS_SHARED else (BH, N, N)
+        if C.dtype != torch.float32 or tuple(C.shape) != c_shape or not C.is_contiguous():
+            raise ValueError(f"C must be a contiguous fp32 {list(c_shape)} tensor")
         c_ptr = C.data_ptr()
     lse_ptr = None
     if LSE is not None:
@@ -80,7 +81,7 @@ def attn_fwd(Q, K, V, mode, C, scale, O, LSE=None, stream=None):
     return O, LSE
 
 
-def _marshal_ex(Q, K, V, C, ckey, O, LSE):
+def _marshal_ex(Q, K, V, C, ckey, O, LSE, mode=0):
     """Shape/dtype checks of the Nq x Nk entry points; returns the integers they take."""
     import torch
 
@@ -100,8 +101,9 @@ def _marshal_ex(Q, K, V, C, ckey, O, LSE):
     out_dtype = ATTN_OUT_F32 if O.dtype == torch.float32 else ATTN_OUT_BF16
     c_ptr = k_ptr = lse_ptr = None
     if C is not None:
-        if C.dtype != torch.float32 or tuple(C.shape) != (BH, Nq, Nk) or not C.is_contiguous():
-            raise ValueError("C must be a contiguous fp32 [BH, Nq, Nk] tensor")
+        c_shape = (Nq, Nk) if mode & ATTN_BIAS_SHARED else (BH, Nq, Nk)
+        if C.dtype != torch.float32 or tuple(C.shape) != c_shape or not C.is_contiguous():
+            raise ValueError(f"C must be a contiguous fp32 {list(c_shape)} tensor")
         c_ptr = C.data_ptr()
     if ckey is not None:
         if ckey.dtype != torch.float32 or tuple(ckey.shape) != (BH, Nk) or not ckey.is_contiguous():
@@ -118,10 +120,11 @@ def attn_fwd_ex(Q, K, V, mode, C, ckey, scale, O, LSE=None, stream=None):
     """attn_fwd with Nq queries and Nk keys and the per-key bias term, through the C ABI.
 
     Q: bf16 [BH, Nq, d]; K: bf16 [BH, Nk, d]; V: bf16 [BH, Nk, d_v]; mode: bit set of
-    ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, ATTN_BIAS_KEY; C: fp32 [BH, Nq, Nk] or None;
+    ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_BIAS_SHARED; C: fp32 [BH, Nq, Nk]
+    ([Nq, Nk] with ATTN_BIAS_SHARED: one bias for every head) or None;
     ckey: fp32 [BH, Nk] or None; O: bf16/fp32 [BH, Nq, d_v]; LSE: fp32 [BH, Nq] or None.
     """
-    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE)
+    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE, mode)
     code = attn_fwd_ex_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), mode, c_ptr, k_ptr, BH, Nq, Nk,
                            d, dv, scale, O.data_ptr(), out_dtype, lse_ptr, _stream_handle(stream))
     if code != ATTN_OK:
@@ -147,7 +150,7 @@ def attn_fwd_splitkv(Q, K, V, mode, C, ckey, scale, O, LSE=None, workspace=None,
     by a second kernel (include/attn.h, attn_fwd_splitkv). `workspace`: a contiguous CUDA
     tensor of at least the planned bytes (see splitkv_workspace), or None when the plan
     has one range; n_splits = 0 lets the library choose."""
-    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE)
+    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE, mode)
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         if not workspace.is_contiguous():
@@ -178,7 +181,7 @@ def attn_fwd_host(Q, K, V, mode, C, ckey, scale, O, LSE=None, staging=None, head
     the shapes and dtypes of attn_fwd_ex (page-locked for the copies to overlap); staging:
     a CUDA tensor of at least attn_fwd_host_staging_bytes (see host_staging). The call is
     asynchronous on `stream`."""
-    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE)
+    BH, Nq, Nk, d, dv, out_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE, mode)
     if staging is None or not staging.is_cuda or not staging.is_contiguous():
         raise ValueError("staging must be a contiguous CUDA tensor (see host_staging)")
     code = attn_fwd_host_raw(Q.data_ptr(), K.data_ptr(), V.data_ptr(), mode, c_ptr, k_ptr, BH, Nq, Nk,
@@ -206,7 +209,7 @@ def attn_bwd(Q, K, V, O, dO, LSE, mode, C, ckey, scale, dQ, dK, dV, workspace, s
     O), through the C ABI (include/attn.h, attn_bwd). `workspace`: see bwd_workspace."""
     import torch
 
-    BH, Nq, Nk, d, dv, o_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE)
+    BH, Nq, Nk, d, dv, o_dtype, c_ptr, k_ptr, lse_ptr = _marshal_ex(Q, K, V, C, ckey, O, LSE, mode)
     if LSE is None:
         raise ValueError("the backward pass needs the forward LSE")
     if dO.dtype != torch.bfloat16 or tuple(dO.shape) != (BH, Nq, dv) or not dO.is_contiguous():

@@ -11,6 +11,7 @@ ATTN_MASK_NONE = 0
 ATTN_MASK_CAUSAL = 1
 ATTN_BIAS_DENSE = 2
 ATTN_BIAS_KEY = 4
+ATTN_BIAS_SHARED = 8
 ATTN_OUT_BF16 = 0
 ATTN_OUT_F32 = 1
 
@@ -24,7 +25,7 @@ ATTN_ERR_DEVICE_TIMEOUT = -6
 ATTN_ERR_CUDA = -7
 ATTN_ERR_SCRATCH_LIMIT = -8
 ATTN_STATIC_SCRATCH_BYTES = 33554432
-ATTN_ABI_VERSION = 106
+ATTN_ABI_VERSION = 107
 
 ATTN_FAULT_NONE = 0
 ATTN_FAULT_SKIP_FIRST_K = 1

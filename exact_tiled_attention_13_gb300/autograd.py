@@ -47,13 +47,14 @@ _FN = None
 def attention(q, k, v, causal: bool = False, bias=None, key_bias=None, scale: float | None = None):
     """softmax(q k^T * scale + C) v for bf16 CUDA tensors q [BH, Nq, d], k [BH, Nk, d],
     v [BH, Nk, d_v], differentiable in q, k and v. C is the causal mask (aligned at the
-    last key) and/or `bias` (fp32 [BH, Nq, Nk]) or `key_bias` (fp32 [BH, Nk]); scale
+    last key) and/or `bias` (fp32 [BH, Nq, Nk], or [Nq, Nk] for one bias shared by every head)
+    or `key_bias` (fp32 [BH, Nk]); scale
     defaults to 1 / sqrt(d). Returns O in bf16. The backward pass is first-order only (no
     double backward), and a bias that requires grad is rejected with ValueError."""
     global _FN
     if _FN is None:
         _FN = _function()
-    from . import ATTN_BIAS_DENSE, ATTN_BIAS_KEY
+    from . import ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_BIAS_SHARED
 
     for name, t in (("bias", bias), ("key_bias", key_bias)):
         if t is not None and t.requires_grad:
@@ -61,6 +62,8 @@ def attention(q, k, v, causal: bool = False, bias=None, key_bias=None, scale: fl
     mode = ATTN_MASK_CAUSAL if causal else ATTN_MASK_NONE
     if bias is not None:
         mode |= ATTN_BIAS_DENSE
+        if bias.dim() == 2:  # one [Nq, Nk] bias for every head
+            mode |= ATTN_BIAS_SHARED
     if key_bias is not None:
         mode |= ATTN_BIAS_KEY
     if scale is None:

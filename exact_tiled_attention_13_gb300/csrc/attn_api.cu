@@ -264,6 +264,10 @@ struct Problem {
   void *stream;
   bool causal() const { return (mode & ATTN_MASK_CAUSAL) != 0; }
   bool dense() const { return (mode & ATTN_BIAS_DENSE) != 0; }
+  bool shared() const { return (mode & ATTN_BIAS_SHARED) != 0; }
+  size_t c_bytes() const {
+    return C ? static_cast<size_t>(shared() ? 1 : BH) * Nq * static_cast<size_t>(Nk) * 4 : 0;
+  }
   bool key() const { return (mode & ATTN_BIAS_KEY) != 0; }
   int bias() const {
     if (dense()) return (Nk % 4 == 0) ? BIAS_DENSE_TMA : BIAS_DENSE_DIRECT;
@@ -284,8 +288,9 @@ constexpr int kEmpty = 1;  // check_shape: a valid call with nothing to do
 
 // Checks of mode, sizes and scale (no pointer is looked at).
 int check_shape(int mode, int BH, int Nq, int Nk, int d, int d_v, int out_dtype, float scale) {
-  if (mode & ~(ATTN_MASK_CAUSAL | ATTN_BIAS_DENSE | ATTN_BIAS_KEY)) return ATTN_ERR_INVALID_ARG;
+  if (mode & ~(ATTN_MASK_CAUSAL | ATTN_BIAS_DENSE | ATTN_BIAS_KEY | ATTN_BIAS_SHARED)) return ATTN_ERR_INVALID_ARG;
   if ((mode & ATTN_BIAS_DENSE) && (mode & ATTN_BIAS_KEY)) return ATTN_ERR_INVALID_ARG;
+  if ((mode & ATTN_BIAS_SHARED) && !(mode & ATTN_BIAS_DENSE)) return ATTN_ERR_INVALID_ARG;
   if (out_dtype != ATTN_OUT_BF16 && out_dtype != ATTN_OUT_F32) return ATTN_ERR_INVALID_ARG;
   if (BH < 1 || Nq < 0 || Nk < 0) return ATTN_ERR_INVALID_ARG;
   if (!(scale > 0.0f) || !std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
@@ -305,8 +310,7 @@ int check_pointers(const Problem &a) {
   const size_t qrows = static_cast<size_t>(a.BH) * static_cast<size_t>(a.Nq);
   const size_t krows = static_cast<size_t>(a.BH) * static_cast<size_t>(a.Nk);
   const void *ins[5] = {a.Q, a.K, a.V, a.C, a.ckey};
-  const size_t in_bytes[5] = {qrows * a.d * 2, krows * a.d * 2, krows * a.d_v * 2,
-                              a.C ? qrows * static_cast<size_t>(a.Nk) * 4 : 0,
+  const size_t in_bytes[5] = {qrows * a.d * 2, krows * a.d * 2, krows * a.d_v * 2, a.c_bytes(),
                               a.ckey ? krows * 4 : 0};
   for (int i = 0; i < 5; ++i) {
     if (ranges_overlap(a.O, a.o_bytes(), ins[i], in_bytes[i]) ||
@@ -353,7 +357,7 @@ int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int s
   // softmax warps read it directly.
   const int bias = a.bias();
   if (bias == BIAS_DENSE_TMA &&
-      encode_3d(&la.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.C, nk, nq, bh, CCHUNK, BM) != ATTN_OK)
+      encode_3d(&la.tmC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.C, nk, nq, a.shared() ? 1 : bh, CCHUNK, BM) != ATTN_OK)
     return ATTN_ERR_CUDA;
 
   la.p.BH = a.BH;
@@ -371,6 +375,7 @@ int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int s
   la.p.O = O_dst;
   la.p.LSE = LSE_dst;
   la.p.C = a.C;
+  la.p.c_shared = a.shared() ? 1 : 0;
   la.p.ckey = a.ckey;
   la.p.status = watchdog;
   la.p.timeout_ns = g_timeout_ns.load();
@@ -518,9 +523,8 @@ extern "C" int attn_fwd_splitkv(const void *Q, const void *K, const void *V, int
     if (!workspace || !aligned(workspace, 16) || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
     const void *bufs[7] = {Q, K, V, C, ckey, O, LSE};
     const size_t qrows = static_cast<size_t>(BH) * Nq, krows = static_cast<size_t>(BH) * Nk;
-    const size_t sizes[7] = {qrows * d * 2, krows * d * 2, krows * d_v * 2,
-                             C ? qrows * static_cast<size_t>(Nk) * 4 : 0, ckey ? krows * 4 : 0,
-                             a.o_bytes(), a.lse_bytes()};
+    const size_t sizes[7] = {qrows * d * 2, krows * d * 2, krows * d_v * 2, a.c_bytes(),
+                             ckey ? krows * 4 : 0, a.o_bytes(), a.lse_bytes()};
     for (int i = 0; i < 7; ++i)
       if (ranges_overlap(workspace, need, bufs[i], sizes[i])) return ATTN_ERR_INVALID_ARG;
   }
@@ -622,9 +626,10 @@ extern "C" int attn_bwd(const void *Q, const void *K, const void *V, const void 
     return ATTN_ERR_INVALID_ARG;
   // Outputs (dQ, dK, dV, workspace) overlap no input and no other output.
   const void *ins[8] = {Q, K, V, O, dO, LSE, C, ckey};
+  const size_t c_rows = (mode & ATTN_BIAS_SHARED) ? static_cast<size_t>(Nq) : qrows;
   const size_t in_bytes[8] = {qrows * d * 2, krows * d * 2, krows * d_v * 2,
                               qrows * d_v * (o_dtype == ATTN_OUT_F32 ? 4 : 2), qrows * d_v * 2,
-                              qrows * 4, C ? qrows * static_cast<size_t>(Nk) * 4 : 0,
+                              qrows * 4, C ? c_rows * static_cast<size_t>(Nk) * 4 : 0,
                               ckey ? krows * 4 : 0};
   const void *outs[4] = {dQ, dK, dV, no_queries ? nullptr : workspace};
   const size_t out_bytes[4] = {qrows * d * 4, krows * d * 4, krows * d_v * 4, need};
@@ -679,6 +684,7 @@ extern "C" int attn_bwd(const void *Q, const void *K, const void *V, const void 
   pp.Lp = Lp;
   pp.Dd = Dd;
   pp.C = C;
+  pp.c_shared = (mode & ATTN_BIAS_SHARED) ? 1 : 0;
   pp.ckey = ckey;
   pp.dQ = dQ;
   pp.dK = dK;

@@ -49,6 +49,7 @@ struct BwdParams {
   const float *Lp;    // [BH][nqp] -LSE * log2(e), -inf where p must be 0
   const float *Dd;    // [BH][nqp] D_i = dO_i . O_i
   const float *C;     // dense bias [BH][Nq][Nk] or null
+  int c_shared;       // 1: C is one [Nq][Nk] array for every head (head index 0)
   const float *ckey;  // per-key bias [BH][Nk] or null
   float *dQ;          // [BH][Nq][d]
   float *dK;          // [BH][Nk][d]
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::A_THREADS, 1)
             if (BIAS == BWD_BIAS_KEY) b[v] += kb;
             if (BIAS == BWD_BIAS_DENSE) {
               const int q = i * BM + c0 + c + v;
-              b[v] += (key_ok && q < p.Nq) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
+              b[v] += (key_ok && q < p.Nq) ? __ldg(p.C + (static_cast<size_t>(p.c_shared ? 0 : bh) * p.Nq + q) * p.Nk + key) * LOG2E
                                            : 0.0f;
             }
           }
@@ -714,7 +715,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
             if (BIAS == BWD_BIAS_KEY)
               x += key < p.Nk ? __ldg(p.ckey + static_cast<size_t>(bh) * p.Nk + key) * LOG2E : 0.0f;
             if (BIAS == BWD_BIAS_DENSE)
-              x += (q_ok && key < p.Nk) ? __ldg(p.C + (static_cast<size_t>(bh) * p.Nq + q) * p.Nk + key) * LOG2E
+              x += (q_ok && key < p.Nk) ? __ldg(p.C + (static_cast<size_t>(p.c_shared ? 0 : bh) * p.Nq + q) * p.Nk + key) * LOG2E
                                         : 0.0f;
             const float pr = ex2_approx(x);
             const float dpv = __uint_as_float(h == 0 ? da[c + v] : db[c + v]);

@@ -97,6 +97,7 @@ struct KernelParams {
   void *O;    // with n_splits > 1: fp32 partial outputs [n_splits][BH][Nq][d_v]
   float *LSE; // with n_splits > 1: partial LSE [n_splits][BH][Nq]
   const float *C;           // dense bias [BH][Nq][Nk], read directly when it cannot go through TMA
+  int c_shared;             // 1: C is one [Nq][Nk] array for every head (head index 0)
   const float *ckey;        // per-key bias [BH][Nk]
   unsigned int *status;     // watchdog word (device memory)
   unsigned long long timeout_ns;
@@ -484,7 +485,8 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
             if (!ok) break;
           } else {
             const bool row_ok = q_row < p.Nq;
-            const float *crow = p.C + (static_cast<size_t>(sch.bh) * p.Nq + (row_ok ? q_row : 0)) *
+            const int c_bh = p.c_shared ? 0 : sch.bh;
+            const float *crow = p.C + (static_cast<size_t>(c_bh) * p.Nq + (row_ok ? q_row : 0)) *
                                           static_cast<size_t>(p.Nk);
 #pragma unroll
             for (int c = 0; c < BN; ++c) {
@@ -903,7 +905,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
               if (!ok) break;
               mbar_arrive_expect_tx(BAR(CF::B_CFULL + slot), CCHUNK_BYTES);
               tma_load_3d(sbase + CF::C_OFF + slot * CCHUNK_BYTES, &tmC, j * BN + cc * CCHUNK,
-                          sch.q_tile(0) * BM, sch.bh, BAR(CF::B_CFULL + slot));
+                          sch.q_tile(0) * BM, p.c_shared ? 0 : sch.bh, BAR(CF::B_CFULL + slot));
               ++issued;
             }
           }

@@ -56,6 +56,9 @@ extern "C" {
 #define ATTN_BIAS_DENSE 2  /* a dense fp32 [BH][Nq][Nk] array C */
 #define ATTN_BIAS_KEY 4    /* a per-key fp32 [BH][Nk] vector c, the same for every query row
                               (attn_fwd_ex only; key padding is c_j = -inf) */
+#define ATTN_BIAS_SHARED 8 /* with ATTN_BIAS_DENSE only: C is one fp32 [Nq][Nk] array that
+                              every head adds (a bias broadcast over the heads), instead of
+                              [BH][Nq][Nk]; rejected by the host-streaming calls */
 
 /* Output element types (argument `out_dtype`). */
 #define ATTN_OUT_BF16 0
@@ -81,8 +84,10 @@ extern "C" {
  *   K     bf16, contiguous row-major [BH][N][d]      keys
  *   V     bf16, contiguous row-major [BH][N][d_v]    values
  *   mode  ATTN_MASK_NONE, ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, or
- *         ATTN_MASK_CAUSAL | ATTN_BIAS_DENSE (causal mask and dense bias together)
- *   C     fp32, contiguous row-major [BH][N][N] when mode has ATTN_BIAS_DENSE, else NULL.
+ *         ATTN_MASK_CAUSAL | ATTN_BIAS_DENSE (causal mask and dense bias together); with
+ *         ATTN_BIAS_DENSE also ATTN_BIAS_SHARED (one C for all heads)
+ *   C     fp32, contiguous row-major [BH][N][N] when mode has ATTN_BIAS_DENSE ([N][N] with
+ *         ATTN_BIAS_SHARED: the same bias for every head), else NULL.
  *         Entries are finite or -inf; C is added after the scaling and is not scaled.
  *   BH    number of heads (batch times heads), >= 1
  *   N     sequence length (queries = keys), >= 0; N == 0 is a successful no-op in which
@@ -116,9 +121,10 @@ ATTN_API int attn_fwd(const void *Q, const void *K, const void *V, int mode, con
  * attn_fwd_ex -- the same operation with Nq queries and Nk keys per head, and the
  * per-key bias term. Everything not listed here is as for attn_fwd.
  *   Q     bf16 [BH][Nq][d];  K bf16 [BH][Nk][d];  V bf16 [BH][Nk][d_v]
- *   mode  bit set of ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, ATTN_BIAS_KEY (DENSE and KEY
- *         together are rejected: add the vector into C instead)
- *   C     fp32 [BH][Nq][Nk] with ATTN_BIAS_DENSE, else NULL
+ *   mode  bit set of ATTN_MASK_CAUSAL, ATTN_BIAS_DENSE, ATTN_BIAS_KEY, ATTN_BIAS_SHARED
+ *         (DENSE and KEY together are rejected: add the vector into C instead; SHARED needs
+ *         DENSE)
+ *   C     fp32 [BH][Nq][Nk] with ATTN_BIAS_DENSE ([Nq][Nk] with ATTN_BIAS_SHARED), else NULL
  *   ckey  fp32 [BH][Nk] with ATTN_BIAS_KEY, else NULL; 4-byte aligned; finite or -inf
  *   Nq    >= 0 (0: no-op); Nk >= 1 when Nq >= 1
  *   O     [BH][Nq][d_v];  LSE fp32 [BH][Nq] or NULL
@@ -349,8 +355,9 @@ ATTN_API int attn_set_fault_injection(int fault);
 /* ABI version of this header (major * 100 + minor): 1.00 attn_fwd; 1.01 attn_fwd_ex;
  * 1.02 attn_fwd_splitkv, attn_fwd_splitkv_plan; 1.03 attn_fwd_splitkv_static;
  * 1.04 attn_bwd, attn_bwd_workspace_bytes; 1.05 attn_fwd_host, attn_fwd_host_staging_bytes;
- * 1.06 attn_bwd_host, attn_bwd_host_staging_bytes. attn_version() returns the library's. */
-#define ATTN_ABI_VERSION 106
+ * 1.06 attn_bwd_host, attn_bwd_host_staging_bytes; 1.07 ATTN_BIAS_SHARED (one dense bias for
+ * all heads). attn_version() returns the library's. */
+#define ATTN_ABI_VERSION 107
 ATTN_API int attn_version(void);
 
 #ifdef __cplusplus

@@ -28,6 +28,7 @@ BASE_SEED = 20261202
 TENSOR_ID = {"Q": 0, "K": 1, "V": 2, "C": 3, "mask": 4, "ckey": 5, "dO": 6}
 
 MODE_NONE, MODE_CAUSAL, MODE_DENSE, MODE_KEY = 0, 1, 2, 4
+MODE_SHARED = 8  # with MODE_DENSE: one [Nq, Nk] bias for every head (the inputs are the same)
 MODE_NAMES = {MODE_NONE: "none", MODE_CAUSAL: "causal", MODE_DENSE: "dense_bias",
               MODE_KEY: "key_bias", MODE_CAUSAL | MODE_DENSE: "causal_dense_bias",
               MODE_CAUSAL | MODE_KEY: "causal_key_bias"}

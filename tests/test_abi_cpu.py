@@ -63,7 +63,7 @@ def test_strerror_and_version():
     for code in range(-7, 1):
         assert eta.attn_strerror(code)
     assert "unknown" in eta.attn_strerror(-99)
-    assert eta.attn_version() == _lib.ATTN_ABI_VERSION == 106
+    assert eta.attn_version() == _lib.ATTN_ABI_VERSION == 107
 
 
 def test_timeout_setting_roundtrip():
@@ -211,6 +211,27 @@ def test_splitkv_zero_queries_is_noop():
 @pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
 def test_valid_splitkv_call_without_gpu_reports_no_device():
     assert call_split(Nk=1000) == eta.ATTN_ERR_NO_DEVICE
+
+
+def test_shared_bias_needs_the_dense_bias():
+    # ATTN_BIAS_SHARED (one [Nq][Nk] bias for every head) qualifies ATTN_BIAS_DENSE only.
+    assert call_ex(mode=_lib.ATTN_BIAS_SHARED, C=CP) == eta.ATTN_ERR_INVALID_ARG
+    assert call_ex(mode=_lib.ATTN_BIAS_SHARED | _lib.ATTN_BIAS_KEY, ckey=KP) == eta.ATTN_ERR_INVALID_ARG
+    assert call_ex(mode=_lib.ATTN_BIAS_SHARED | _lib.ATTN_BIAS_DENSE, C=None) == eta.ATTN_ERR_INVALID_ARG
+    code, _ = eta.attn_fwd_host_staging_bytes(_lib.ATTN_BIAS_SHARED | _lib.ATTN_BIAS_DENSE, 2, 64, 64,
+                                              64, 64, 1, 0)
+    assert code == eta.ATTN_ERR_INVALID_ARG  # the host-streaming calls slice C per head
+
+
+@pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
+def test_shared_bias_is_one_array_for_the_overlap_checks():
+    # A shared C of Nq x Nk fp32 ends before O here; read as [BH][Nq][Nk] it would overlap O.
+    a = dict(GOOD_EX)
+    c_bytes = a["Nq"] * a["Nk"] * 4
+    o = 0x7000000
+    shared = call_ex(mode=_lib.ATTN_BIAS_SHARED | _lib.ATTN_BIAS_DENSE, C=o - c_bytes, O=o)
+    full = call_ex(mode=_lib.ATTN_BIAS_DENSE, C=o - c_bytes, O=o)
+    assert shared == eta.ATTN_ERR_NO_DEVICE and full == eta.ATTN_ERR_INVALID_ARG
 
 
 @pytest.mark.skipif(_gpu_present(), reason="a GPU is present")
