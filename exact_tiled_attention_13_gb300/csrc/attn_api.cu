@@ -390,6 +390,10 @@ int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int s
     // CTA pairs: each CTA copies 64 keys of every K tile (one 64 x 64 box per 128-byte span).
     if (encode_3d(&la.tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.K, a.d, nk, bh, SW_CHUNK, BN / 2) != ATTN_OK)
       return ATTN_ERR_CUDA;
+    // Its epilogue stores O with TMA, 32 rows x 128 bytes per box.
+    const int rc_o = out_f32 ? encode_3d(&la.tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, O_dst, a.d_v, nq, bh, 32, 32)
+                             : encode_3d(&la.tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, O_dst, a.d_v, nq, bh, 64, 32);
+    if (rc_o != ATTN_OK) return ATTN_ERR_CUDA;
     if (a.d == 64) e = causal ? launch_attn_pair<64, 128, true>(la) : launch_attn_pair<64, 128, false>(la);
     else e = causal ? launch_attn_pair<128, 128, true>(la) : launch_attn_pair<128, 128, false>(la);
   } else if (a.d == 64 && a.d_v == 64) e = dispatch<64, 64>(causal, bias, la);

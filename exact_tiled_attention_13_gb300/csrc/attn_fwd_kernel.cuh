@@ -957,6 +957,7 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 // ---------------------------------------------------------------------- host side
 struct LaunchArgs {
   CUtensorMap tmQ, tmK, tmV, tmC;
+  CUtensorMap tmO;  // O as stored by the CTA-pair kernel: 32-row boxes of 128 bytes
   KernelParams p;
   cudaStream_t stream;
 };

@@ -167,7 +167,8 @@ __device__ __forceinline__ void settle_after_abort() {
 template <int D, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
     attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ KernelParams p) {
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                         const __grid_constant__ KernelParams p) {
   using CF = PairCfg<D, DV, CAUSAL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -419,6 +420,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
       lxk[(2 * 2 + wg) * BM + row] = lr;
       __syncwarp();
       mbar_arrive_elect(BAR(CF::B_LDONE + (k & 1)));
+      ETA_TRACE(45);
       g0 += sch.n_it;
     }
   } else if (warp >= CF::EPI_WARP0) {
@@ -438,6 +440,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
       const int q_row = sch.qt * BM + row;
       ok = wd.wait(BAR(CF::B_LDONE + (k & 1)), (k >> 1) & 1, ROLE_SOFTMAX, CF::B_LDONE + (k & 1));
       if (!ok) break;
+      ETA_TRACE(41);
       const float *lxk = lx + (k & 1) * (3 * 2 * BM);
       const float m0 = lxk[(0 * 2 + 0) * BM + row], m1 = lxk[(0 * 2 + 1) * BM + row];
       const float l0 = lxk[(1 * 2 + 0) * BM + row], l1 = lxk[(1 * 2 + 1) * BM + row];
@@ -451,7 +454,6 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
       const float lr_row = fmaf(lr0, f0, lr1 * f1);
       const float inv_l = (lr_row > 0.0f) ? 1.0f / lr_row : 0.0f;  // no allowed key: O = 0
       const int row0 = q_row - lane;
-      const int rows_ok = p.Nq - row0 < 32 ? (p.Nq - row0 > 0 ? p.Nq - row0 : 0) : 32;
       const size_t obase = (static_cast<size_t>(sch.bh) * p.Nq + row0) * DV;
       const int esz = p.out_f32 ? 4 : 2;
       if (sch.n_it == 0) {
@@ -465,29 +467,25 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
         ok = wd.wait(BAR(CF::B_OFULL), n_o & 1, ROLE_SOFTMAX, CF::B_OFULL);
         if (!ok) break;
         tc_fence_after();
+        ETA_TRACE(42);
         // The unit's Q buffer is idle once its last S completed (and is reloaded only after
-        // this epilogue releases it): each warp stages 32 rows x 256 bytes there at a time, in
-        // 16-byte units at (unit ^ row % 8) so neither side has bank conflicts, and stores them
-        // as whole 256-byte row segments, two rows per instruction.
-        uint8_t *stage = smem + CF::Q_OFF + (k & 1) * CF::Q_BUF + e * (32 * 256);
-        uint4 *srow = reinterpret_cast<uint4 *>(stage + lane * 256);
-        const int sub = lane % 16;
-        auto store_stage = [&](uint8_t *g, int row_bytes) {
+        // this epilogue releases it): each warp stages its 32 rows there as boxes of 32 rows x
+        // 128 bytes in the tensor map's 128-byte swizzle (16-byte unit u of row r at u ^ r % 8,
+        // so the writes have no bank conflicts), and one lane stores them with TMA; rows past
+        // Nq are clipped by the copy.
+        const uint32_t stage = sbase + CF::Q_OFF + (k & 1) * CF::Q_BUF + e * (32 * 256);
+        const uint32_t srow = stage + lane * 128;
+        auto put = [&](int box, int u, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+          st_shared_v4(srow + box * 4096 + ((u ^ (lane & 7)) << 4), a0, a1, a2, a3);
+        };
+        auto store_boxes = [&](int x0, int x1) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
-#pragma unroll
-          for (int quarter = 0; quarter < 4; ++quarter) {
-            uint4 val[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int rr = 8 * quarter + 2 * i + lane / 16;
-              val[i] = *reinterpret_cast<const uint4 *>(stage + rr * 256 + 16 * (sub ^ (rr & 7)));
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int rr = 8 * quarter + 2 * i + lane / 16;
-              if (rr < rows_ok)
-                *reinterpret_cast<uint4 *>(g + static_cast<size_t>(rr) * row_bytes + 16 * sub) = val[i];
-            }
+          if (lane == 0) {
+            tma_store_3d(&tmO, stage, x0, row0, sch.bh);
+            tma_store_3d(&tmO, stage + 4096, x1, row0, sch.bh);
+            bulk_commit();
+            bulk_wait_read();  // the boxes are read before this warp writes the stage again
           }
           __syncwarp();
         };
@@ -509,33 +507,35 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
           __syncwarp();
           if (leader) mbar_arrive_elect(BAR(CF::B_OEMPTY));
           else pair::mbar_arrive_cluster_elect(LBAR(CF::B_OEMPTY));
+          ETA_TRACE(43);
         };
         if (p.out_f32) {
 #pragma unroll 1
-          for (int pass = 0; pass < 2; ++pass) {  // value columns [64 pass, 64 pass + 64)
+          for (int pass = 0; pass < 2; ++pass) {  // value columns [64 pass, 64 pass + 64): two boxes of 32
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               uint32_t f[32];
               load_o(64 * pass + 32 * h, f);
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
-                srow[(8 * h + v) ^ (lane & 7)] = make_uint4(f[4 * v + 0], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
+              for (int v = 0; v < 8; ++v) put(h, v, f[4 * v + 0], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
             }
             if (pass == 1) release_o();
-            store_stage(reinterpret_cast<uint8_t *>(static_cast<float *>(p.O) + obase + 64 * pass), DV * 4);
+            store_boxes(64 * pass, 64 * pass + 32);
           }
         } else {
+          // All 128 columns as bf16 pairs in registers first, so o is released early.
+          uint32_t b[64];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             uint32_t f[32];
             load_o(32 * h, f);
-            auto bf = [&](int c) { return pack_bf16(__uint_as_float(f[c]), __uint_as_float(f[c + 1])); };
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              srow[(4 * h + v) ^ (lane & 7)] = make_uint4(bf(8 * v + 0), bf(8 * v + 2), bf(8 * v + 4), bf(8 * v + 6));
+            for (int c = 0; c < 16; ++c) b[16 * h + c] = pack_bf16(__uint_as_float(f[2 * c]), __uint_as_float(f[2 * c + 1]));
           }
           release_o();
-          store_stage(reinterpret_cast<uint8_t *>(static_cast<uint16_t *>(p.O) + obase), DV * 2);
+#pragma unroll
+          for (int v = 0; v < 16; ++v) put(v / 8, v % 8, b[4 * v + 0], b[4 * v + 1], b[4 * v + 2], b[4 * v + 3]);
+          store_boxes(0, 64);
         }
         ++n_o;
       }
@@ -547,6 +547,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       mbar_arrive_elect(BAR(CF::B_QEMPTY + (k & 1)));
+      ETA_TRACE(44);
     }
   } else {
     regs_decrease<CF::REGS_CTRL>();
@@ -759,7 +760,7 @@ cudaError_t launch_attn_pair(const LaunchArgs &a) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, kern, a.tmQ, a.tmK, a.tmV, a.p);
+  e = cudaLaunchKernelEx(&cfg, kern, a.tmQ, a.tmK, a.tmV, a.tmO, a.p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

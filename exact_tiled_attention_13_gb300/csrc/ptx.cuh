@@ -75,6 +75,21 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// 3-D tiled tensor store from shared memory (box of the tensor map at x, y, z; rows and
+// columns outside the tensor are not written). Tracked by the issuing thread's bulk groups:
+// bulk_commit() closes a group, bulk_wait_read() returns once every committed group has
+// finished reading shared memory (the source may then be overwritten).
+__device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // 3-D tiled tensor load into shared memory; completion is signalled on `bar` as
 // transaction bytes. x is the innermost (contiguous) coordinate, in elements.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
