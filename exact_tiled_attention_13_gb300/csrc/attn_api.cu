@@ -30,13 +30,17 @@ ETA_DECLARE(128, 64)
 ETA_DECLARE(128, 128)
 #undef ETA_DECLARE
 #undef ETA_DECLARE_C
-// CTA-pair forward kernels (attn_pair_inst.cu).
-template <int D, int DV, bool CAUSAL>
+// CTA-pair forward kernels (attn_pair_inst.cu, attn_pair_dense_inst.cu).
+template <int D, int DV, bool CAUSAL, int BIAS>
 cudaError_t launch_attn_pair(const LaunchArgs &);
-extern template cudaError_t launch_attn_pair<64, 128, false>(const LaunchArgs &);
-extern template cudaError_t launch_attn_pair<64, 128, true>(const LaunchArgs &);
-extern template cudaError_t launch_attn_pair<128, 128, false>(const LaunchArgs &);
-extern template cudaError_t launch_attn_pair<128, 128, true>(const LaunchArgs &);
+#define ETA_DECLARE_PAIR(D, C)                                                          \
+  extern template cudaError_t launch_attn_pair<D, 128, C, BIAS_NONE>(const LaunchArgs &); \
+  extern template cudaError_t launch_attn_pair<D, 128, C, BIAS_DENSE_TMA>(const LaunchArgs &);
+ETA_DECLARE_PAIR(64, false)
+ETA_DECLARE_PAIR(64, true)
+ETA_DECLARE_PAIR(128, false)
+ETA_DECLARE_PAIR(128, true)
+#undef ETA_DECLARE_PAIR
 #define ETA_DECLARE_BWD_C(D, DV, C)                                                       \
   extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_NONE>(const BwdLaunchArgs &);  \
   extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_DENSE>(const BwdLaunchArgs &); \
@@ -329,14 +333,27 @@ int head_group(int BH, int Nk, int d, int d_v) {
   return g >= BH ? BH : (g < 1.0 ? 1 : static_cast<int>(g));
 }
 
-// The persistent CTA-pair kernel (attn_fwd_pair_kernel.cuh) serves the causal problems
-// without a bias term with 128 value columns, in one key range; everything else goes to
-// attn_fwd_kernel. The pair kernel computes S ahead of the softmax, so a tile that moves the
-// exponent reference waits for the previous P V before rescaling o; on unmasked rows of
-// large scores (many moves) that costs more than it gains, while attn_fwd_kernel, which
-// computes S(t) only after P(t-1) V, rescales without waiting.
+// The persistent CTA-pair kernel (attn_fwd_pair_kernel.cuh) serves problems with 128 value
+// columns in one key range: causal ones without a bias term, and every one with a dense bias
+// read through TMA (there attn_fwd_kernel holds one query tile per CTA and its chain
+// softmax -> P V -> next S is exposed). Everything else goes to attn_fwd_kernel. The pair
+// kernel computes S ahead of the softmax, so a tile that moves the exponent reference waits
+// for the previous P V before rescaling o; on unmasked rows of large scores (many moves, as
+// with the x4 scores of the unmasked benchmark) that costs more than it gains, while
+// attn_fwd_kernel, which computes S(t) only after P(t-1) V, rescales without waiting. With
+// a per-key bias at d = 64 the softmax bounds both kernels and the pair kernel's hand-off of
+// the reference between its warpgroups made it slower (73.5 against 60.4 us on 8 heads of
+// N = 4096).
 bool use_pair_kernel(const Problem &a, int n_splits) {
-  return a.bias() == BIAS_NONE && a.causal() && a.d_v == 128 && n_splits == 1;
+  if (a.d_v != 128 || n_splits != 1) return false;
+  const int bias = a.bias();
+  return bias == BIAS_DENSE_TMA || (bias == BIAS_NONE && a.causal());
+}
+
+template <int D, bool C>
+cudaError_t dispatch_pair(int bias, const LaunchArgs &a) {
+  return bias == BIAS_DENSE_TMA ? launch_attn_pair<D, 128, C, BIAS_DENSE_TMA>(a)
+                                : launch_attn_pair<D, 128, C, BIAS_NONE>(a);
 }
 
 // Launches the attention kernel. With n_splits > 1 each CTA covers `split_tiles` K/V
@@ -394,8 +411,10 @@ int launch_forward(const Problem &a, unsigned int *watchdog, int n_splits, int s
     const int rc_o = out_f32 ? encode_3d(&la.tmO, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, O_dst, a.d_v, nq, bh, 32, 32)
                              : encode_3d(&la.tmO, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, O_dst, a.d_v, nq, bh, 64, 32);
     if (rc_o != ATTN_OK) return ATTN_ERR_CUDA;
-    if (a.d == 64) e = causal ? launch_attn_pair<64, 128, true>(la) : launch_attn_pair<64, 128, false>(la);
-    else e = causal ? launch_attn_pair<128, 128, true>(la) : launch_attn_pair<128, 128, false>(la);
+    // Units of 256 query rows (a query tile in each CTA of the pair), whatever the bias.
+    la.p.ctas_per_head = (la.p.nq_tiles + 1) / 2;
+    if (a.d == 64) e = causal ? dispatch_pair<64, true>(bias, la) : dispatch_pair<64, false>(bias, la);
+    else e = causal ? dispatch_pair<128, true>(bias, la) : dispatch_pair<128, false>(bias, la);
   } else if (a.d == 64 && a.d_v == 64) e = dispatch<64, 64>(causal, bias, la);
   else if (a.d == 64) e = dispatch<64, 128>(causal, bias, la);
   else if (a.d_v == 64) e = dispatch<128, 64>(causal, bias, la);

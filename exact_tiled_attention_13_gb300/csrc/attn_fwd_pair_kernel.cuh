@@ -54,12 +54,15 @@
 
 namespace eta {
 
-template <int D, int DV, bool CAUSAL>
+template <int D, int DV, bool CAUSAL, int BIAS>
 struct PairCfg {
   static_assert(D == 64 || D == 128, "d must be 64 or 128");
   static_assert(DV == 128, "the pair kernel splits 128 value columns in two 128-byte halves");
+  static_assert(BIAS == BIAS_NONE || BIAS == BIAS_DENSE_TMA, "bias kind");
+  static constexpr bool DENSE = BIAS == BIAS_DENSE_TMA;  // [Nq][Nk] bias rows through a TMA ring
+  static constexpr bool BIASED = DENSE;
   static constexpr int Q_TILE = BM * D * 2;       // this CTA's 128 query rows
-  static constexpr int STAGE = 4 * 32 * 256;      // epilogue stage: 32 rows x 256 bytes per epilogue warp
+  static constexpr int STAGE = 4 * 32 * 128;      // epilogue stage: one 32-row x 128-byte box per epilogue warp
   static constexpr int Q_BUF = Q_TILE > STAGE ? Q_TILE : STAGE;
   static constexpr int KH_ROWS = BN / 2;          // keys of a K tile held by one CTA
   static constexpr int KH_BOX = KH_ROWS * 128;    // one 64-row x 128-byte box
@@ -67,15 +70,26 @@ struct PairCfg {
   static constexpr int VH_COLS = DV / 2;          // value columns held by one CTA
   static constexpr int VH_TILE = BN * VH_COLS * 2;
   static constexpr int NS = 2;                    // S buffers (and P buffers) in tensor memory
-  static constexpr int KS = 4;
-  static constexpr int VS = 4;
+  // The dense bias stream takes the room of the deeper K/V rings and of the second Q buffer
+  // (a unit's Q copy then waits for the previous unit's epilogue, which stages through it).
+  static constexpr int KS = DENSE ? 2 : 4;
+  static constexpr int VS = DENSE ? 3 : 4;
+  static constexpr int NQB = DENSE ? 1 : 2;       // Q buffers: unit k uses buffer k % NQB
   static_assert(VS >= 3, "the softmax tells P(t) V apart by the phase of its V slot");
-  static constexpr int Q_OFF = 0;                 // two Q buffers: unit k uses buffer k % 2
-  static constexpr int K_OFF = Q_OFF + 2 * Q_BUF;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + NQB * Q_BUF;
   static constexpr int V_OFF = K_OFF + KS * KH_TILE;
   static constexpr int RX_OFF = V_OFF + VS * VH_TILE;  // references passed on, 2 x 128 fp32
   static constexpr int LX_OFF = RX_OFF + 2 * BM * 4;    // per unit % 2: [m, l, l'][2 warpgroups][128 rows]
-  static constexpr int BAR_OFF = LX_OFF + 2 * 3 * 2 * BM * 4;
+  static constexpr int C_OFF = (LX_OFF + 2 * 3 * 2 * BM * 4 + 1023) / 1024 * 1024;  // dense bias rings (128-byte swizzle)
+  static constexpr int BAR_RESERVE = 1024;               // barriers, tensor-memory address, abort flag
+  // Two dense-bias rings of RS chunks, one per softmax warpgroup, each consumed in order by
+  // its warpgroup only (a ring shared by both could let one warpgroup wait on a slot whose
+  // previous fill has not landed yet, and a parity wait cannot tell those phases apart).
+  static constexpr int RS = DENSE ? cmin(4, (232448 - 1024 - BAR_RESERVE - C_OFF) / (2 * CCHUNK_BYTES)) : 0;
+  static constexpr int CS = 2 * RS;
+  static_assert(!DENSE || RS >= 2, "need two bias chunks in flight per warpgroup");
+  static constexpr int BAR_OFF = C_OFF + CS * CCHUNK_BYTES;
   static constexpr int B_QFULL = 0;               // 2: Q of the unit in buffer 0 / 1 landed (both CTAs)
   static constexpr int B_QEMPTY = B_QFULL + 2;    // 2: buffer read by its unit's last S and used by its epilogue (5)
   static constexpr int B_KFULL = B_QEMPTY + 2;
@@ -92,7 +106,10 @@ struct PairCfg {
   static constexpr int B_HREF = B_DRAIN2 + 1;     // 8: reference passed on by warpgroup g, warp q (4 g + q)
   static constexpr int B_LDONE = B_HREF + 8;      // 2: a unit's (m, l, l') per row written by the 8 softmax warps
   static constexpr int B_LEMPTY = B_LDONE + 2;    // 2: read by the 4 epilogue warps
-  static constexpr int NUM_BARS = B_LEMPTY + 2;
+  static constexpr int B_CFULL = B_LEMPTY + 2;    // CS: a 128 x 32 bias chunk landed
+  static constexpr int B_CEMPTY = B_CFULL + CS;   // CS: read by the tile's 4 softmax warps
+  static constexpr int NUM_BARS = B_CEMPTY + CS;
+  static_assert(NUM_BARS * 8 + 8 <= BAR_RESERVE, "barrier region");
   static constexpr int TMEMPTR_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = TMEMPTR_OFF + 4;
   static constexpr int SMEM_USED = ABORT_OFF + 4;
@@ -164,12 +181,12 @@ __device__ __forceinline__ void settle_after_abort() {
   }
 }
 
-template <int D, int DV, bool CAUSAL>
-__global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
+template <int D, int DV, bool CAUSAL, int BIAS>
+__global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-                         const __grid_constant__ KernelParams p) {
-  using CF = PairCfg<D, DV, CAUSAL>;
+                         const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmC,
+                         const __grid_constant__ CUtensorMap tmO, const __grid_constant__ KernelParams p) {
+  using CF = PairCfg<D, DV, CAUSAL, BIAS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -195,6 +212,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
   // ------------------------------------------------------------------ set-up
   if (threadIdx.x == 0) {
     for (int q = 0; q < 2; ++q) {
+      if (q >= CF::NQB) break;
       mbar_init(BAR(CF::B_QFULL + q), 1);
       mbar_init(BAR(CF::B_QEMPTY + q), 1 + 4);  // the last S's commit and this CTA's 4 epilogue warps
     }
@@ -219,6 +237,10 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
     for (int q = 0; q < 2; ++q) {
       mbar_init(BAR(CF::B_LDONE + q), 8);
       mbar_init(BAR(CF::B_LEMPTY + q), 4);
+    }
+    for (int s = 0; s < CF::CS; ++s) {
+      mbar_init(BAR(CF::B_CFULL + s), 1);
+      mbar_init(BAR(CF::B_CEMPTY + s), 4);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -253,6 +275,10 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
     const int h_mine = CF::B_HREF + 4 * wg + wq;
     const int h_other = CF::B_HREF + 4 * (wg ^ 1) + wq;
     const float sl2 = p.scale_log2;
+    // x is raw S without a bias (exponents x scale log2 e) and scale S + C with one
+    // (exponents x log2 e).
+    const float scale = sl2 * LN2;
+    const float xs = CF::BIASED ? LOG2E : sl2;
     bool ok = true;
     int g0 = 0;  // global number of this unit's first tile
 
@@ -297,12 +323,37 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
           x[64 + c] = __uint_as_float(r2[c]);
           x[96 + c] = __uint_as_float(r3[c]);
         }
+        if constexpr (CF::DENSE) {
+          // x = scale S + C: this row's 32 biases of each chunk, 16-byte unit u of row r at
+          // u ^ r % 8 (the copy's 128-byte swizzle), so the reads have no bank conflicts.
+#pragma unroll
+          for (int cc = 0; cc < BN / CCHUNK; ++cc) {
+            const int cpos = (BN / CCHUNK) * (t >> 1) + cc;  // position in this warpgroup's ring
+            const int slot = wg * CF::RS + cpos % CF::RS;
+            ok = wd.wait(BAR(CF::B_CFULL + slot), (cpos / CF::RS) & 1, ROLE_SOFTMAX, CF::B_CFULL + slot);
+            if (!ok) break;
+            const uint8_t *chunk = smem + CF::C_OFF + slot * CCHUNK_BYTES + row * 128;
+#pragma unroll
+            for (int u = 0; u < CCHUNK / 4; ++u) {
+              const float4 cv = *reinterpret_cast<const float4 *>(chunk + ((u ^ (row & 7)) << 4));
+              const int c = cc * CCHUNK + 4 * u;
+              fma2(x[c + 0], x[c + 1], x[c + 0], x[c + 1], scale, scale, cv.x, cv.y);
+              fma2(x[c + 2], x[c + 3], x[c + 2], x[c + 3], scale, scale, cv.z, cv.w);
+            }
+            __syncwarp();
+            mbar_arrive_elect(BAR(CF::B_CEMPTY + slot));
+          }
+          if (!ok) break;
+        }
+        // bt: the tile's row maximum of x (raw S without a bias, scale S + C with one).
         float bt;
         if (j >= j_mask) {  // the causal diagonal or the ragged last tile: mask, then the maximum
           const int lim_j = lim - j * BN;
 #pragma unroll
           for (int c = 0; c < BN; ++c)
             if (c > lim_j) x[c] = -INFINITY;
+          bt = row_max128(x);
+        } else if constexpr (CF::BIASED) {
           bt = row_max128(x);
         } else {
           bt = fmaxf(fmax3(mx0, mx1, mx2), mx3);
@@ -319,7 +370,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
           if (!ok) break;
           if (t > g0) m_in = rx[(wg ^ 1) * BM + row];
         }
-        const float bs = bt * sl2;
+        const float bs = bt * xs;
         const bool move = bs > m_in + RESCALE_TAU;  // also the first allowed key (m_in = -inf)
         const float m_new = move ? bs : m_in;
         rx[wg * BM + row] = m_new;
@@ -349,7 +400,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
           for (int c2 = 0; c2 < 16; ++c2) {
             const int c = 32 * qq + 2 * c2;
             float a0, a1;
-            fma2(a0, a1, x[c], x[c + 1], sl2, sl2, neg_m, neg_m);
+            fma2(a0, a1, x[c], x[c + 1], xs, xs, neg_m, neg_m);
             const float p0 = ex2_approx(a0);
             const float p1 = ex2_approx(a1);
             const int e = 2 * (c2 & 3);
@@ -397,7 +448,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
         const float tile_sum = s[0] + s[1];
         // The tile's largest p as rounded to bf16 joins O's denominator (see
         // attn_fwd_kernel.cuh); this warpgroup's shares move from m_prev to the new reference.
-        const float pmax = ex2_approx(fmaf(bt, sl2, neg_m));
+        const float pmax = ex2_approx(fmaf(bt, xs, neg_m));
         const float corr = __uint_as_float(pack_bf16(pmax, pmax) << 16) - pmax;
         const float alpha = ex2_approx(m_prev - m_use);  // 1 when the reference stayed; 0 from -inf
         l = fmaf(alpha, l, tile_sum);
@@ -469,24 +520,26 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
         tc_fence_after();
         ETA_TRACE(42);
         // The unit's Q buffer is idle once its last S completed (and is reloaded only after
-        // this epilogue releases it): each warp stages its 32 rows there as boxes of 32 rows x
-        // 128 bytes in the tensor map's 128-byte swizzle (16-byte unit u of row r at u ^ r % 8,
-        // so the writes have no bank conflicts), and one lane stores them with TMA; rows past
-        // Nq are clipped by the copy.
-        const uint32_t stage = sbase + CF::Q_OFF + (k & 1) * CF::Q_BUF + e * (32 * 256);
-        const uint32_t srow = stage + lane * 128;
-        auto put = [&](int box, int u, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
-          st_shared_v4(srow + box * 4096 + ((u ^ (lane & 7)) << 4), a0, a1, a2, a3);
+        // this epilogue releases it): each warp stages its 32 rows there one box of 32 rows x
+        // 128 bytes at a time, in the tensor map's 128-byte swizzle (16-byte unit u of row r
+        // at u ^ r % 8, so the writes have no bank conflicts), and one lane stores it with
+        // TMA; rows past Nq are clipped by the copy.
+        const uint32_t stage = sbase + CF::Q_OFF + (k % CF::NQB) * CF::Q_BUF + e * (32 * 128);
+        auto put = [&](int u, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+          st_shared_v4(stage + lane * 128 + ((u ^ (lane & 7)) << 4), a0, a1, a2, a3);
         };
-        auto store_boxes = [&](int x0, int x1) {
+        auto store_box = [&](int x) {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&tmO, stage, x0, row0, sch.bh);
-            tma_store_3d(&tmO, stage + 4096, x1, row0, sch.bh);
+            tma_store_3d(&tmO, stage, x, row0, sch.bh);
             bulk_commit();
-            bulk_wait_read();  // the boxes are read before this warp writes the stage again
           }
+          __syncwarp();
+        };
+        // The previous box has been read out of the stage.
+        auto stage_free = [&]() {
+          if (lane == 0) bulk_wait_read();
           __syncwarp();
         };
         // o / l for 32 columns, in place.
@@ -510,33 +563,40 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
           ETA_TRACE(43);
         };
         if (p.out_f32) {
-#pragma unroll 1
-          for (int pass = 0; pass < 2; ++pass) {  // value columns [64 pass, 64 pass + 64): two boxes of 32
+          // Four boxes of 32 fp32 columns; each column block is loaded while the previous
+          // box is still being read out of the stage.
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t f[32];
-              load_o(64 * pass + 32 * h, f);
+          for (int h = 0; h < 4; ++h) {
+            uint32_t f[32];
+            load_o(32 * h, f);
+            if (h == 3) release_o();
+            if (h > 0) stage_free();
 #pragma unroll
-              for (int v = 0; v < 8; ++v) put(h, v, f[4 * v + 0], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
-            }
-            if (pass == 1) release_o();
-            store_boxes(64 * pass, 64 * pass + 32);
+            for (int v = 0; v < 8; ++v) put(v, f[4 * v + 0], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
+            store_box(32 * h);
           }
         } else {
-          // All 128 columns as bf16 pairs in registers first, so o is released early.
-          uint32_t b[64];
+          // All 128 columns as bf16 pairs in registers first, so o is released early; then
+          // two boxes of 64 columns.
+          uint32_t bv[64];
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             uint32_t f[32];
             load_o(32 * h, f);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) b[16 * h + c] = pack_bf16(__uint_as_float(f[2 * c]), __uint_as_float(f[2 * c + 1]));
+            for (int c = 0; c < 16; ++c) bv[16 * h + c] = pack_bf16(__uint_as_float(f[2 * c]), __uint_as_float(f[2 * c + 1]));
           }
           release_o();
 #pragma unroll
-          for (int v = 0; v < 16; ++v) put(v / 8, v % 8, b[4 * v + 0], b[4 * v + 1], b[4 * v + 2], b[4 * v + 3]);
-          store_boxes(0, 64);
+          for (int box = 0; box < 2; ++box) {
+            if (box > 0) stage_free();
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              put(v, bv[32 * box + 4 * v + 0], bv[32 * box + 4 * v + 1], bv[32 * box + 4 * v + 2], bv[32 * box + 4 * v + 3]);
+            store_box(64 * box);
+          }
         }
+        stage_free();
         ++n_o;
       }
       // LSE_i = m_i + ln l_i, from the log2-scaled reference.
@@ -546,7 +606,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
       // The stage's generic writes come before the next TMA copy into this Q buffer.
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      mbar_arrive_elect(BAR(CF::B_QEMPTY + (k & 1)));
+      mbar_arrive_elect(BAR(CF::B_QEMPTY + k % CF::NQB));
       ETA_TRACE(44);
     }
   } else {
@@ -566,9 +626,9 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
         const unsigned unit = pair_unit(k, cl, n_cl);
         if (unit >= n_units) break;
         const PairSchedule<CAUSAL> sch(p, unit, rank);
-        const int qb = k & 1;
+        const int qb = k % CF::NQB;
         if (s_role) {
-          ok = wd.wait(BAR(CF::B_QFULL + qb), (k >> 1) & 1, ROLE_MMA, CF::B_QFULL + qb);
+          ok = wd.wait(BAR(CF::B_QFULL + qb), (k / CF::NQB) & 1, ROLE_MMA, CF::B_QFULL + qb);
           if (ok) tc_fence_after();
           for (int i = 0; ok && i < sch.n_it; ++i) {
             const int t = g0 + i;
@@ -642,9 +702,9 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
         const unsigned unit = pair_unit(k, cl, n_cl);
         if (unit >= n_units) break;
         const PairSchedule<CAUSAL> sch(p, unit, rank);
-        const int qb = k & 1;
-        // Q buffer qb was last used by unit k - 2 (its last S and its epilogue).
-        ok = wd.wait1(BAR(CF::B_QEMPTY + qb), ((k >> 1) & 1) ^ 1, ROLE_LOAD, CF::B_QEMPTY + qb, false);
+        const int qb = k % CF::NQB;
+        // Q buffer qb was last used by unit k - NQB (its last S and its epilogue).
+        ok = wd.wait1(BAR(CF::B_QEMPTY + qb), ((k / CF::NQB) & 1) ^ 1, ROLE_LOAD, CF::B_QEMPTY + qb, false);
         if (!ok) break;
         if (leader) mbar_arrive_expect_tx(BAR(CF::B_QFULL + qb), 2 * CF::Q_TILE);
         for (int kc = 0; kc < D / SW_CHUNK; ++kc)
@@ -668,6 +728,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
     } else if (warp == CF::VLOAD_WARP && lane == 0) {
       // ============================================================== TMA: V halves
       tma_prefetch_desc(&tmV);
+      if constexpr (CF::DENSE) tma_prefetch_desc(&tmC);
       bool ok = true;
       int g0 = 0;
       for (int k = 0; ok; ++k) {
@@ -683,6 +744,20 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
           if (leader) mbar_arrive_expect_tx(BAR(CF::B_VFULL + vs), 2 * CF::VH_TILE);
           pair::tma_load_3d(sbase + CF::V_OFF + vs * CF::VH_TILE, &tmV, CF::VH_COLS * static_cast<int>(rank),
                             j * BN, sch.bh, LBAR(CF::B_VFULL + vs));
+          if constexpr (CF::DENSE) {
+            // This CTA's 128 bias rows of the tile, as four 128 x 32 chunks (columns past Nk
+            // and rows past Nq arrive as zeros and are masked or not stored).
+            for (int cc = 0; ok && cc < BN / CCHUNK; ++cc) {
+              const int cpos = (BN / CCHUNK) * (t >> 1) + cc;  // tile t goes to warpgroup t % 2's ring
+              const int slot = (t & 1) * CF::RS + cpos % CF::RS;
+              ok = wd.wait1(BAR(CF::B_CEMPTY + slot), ((cpos / CF::RS) & 1) ^ 1, ROLE_CLOAD, CF::B_CEMPTY + slot, false);
+              if (!ok) break;
+              mbar_arrive_expect_tx(BAR(CF::B_CFULL + slot), CCHUNK_BYTES);
+              tma_load_3d(sbase + CF::C_OFF + slot * CCHUNK_BYTES, &tmC, j * BN + cc * CCHUNK, sch.qt * BM,
+                          p.c_shared ? 0 : sch.bh, BAR(CF::B_CFULL + slot));
+            }
+            if (!ok) break;
+          }
         }
         g0 += sch.n_it;
       }
@@ -702,9 +777,9 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL>::THREADS, 1)
 }
 
 // Clusters that can be resident at once for an instance (looked up once per device).
-template <int D, int DV, bool CAUSAL>
+template <int D, int DV, bool CAUSAL, int BIAS>
 int pair_max_clusters(int dev) {
-  using CF = PairCfg<D, DV, CAUSAL>;
+  using CF = PairCfg<D, DV, CAUSAL, BIAS>;
   static int cached[64] = {0};
   if (dev < 0 || dev >= 64) return 0;
   if (cached[dev] > 0) return cached[dev];
@@ -720,7 +795,7 @@ int pair_max_clusters(int dev) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attn_fwd_pair_kernel<D, DV, CAUSAL>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, attn_fwd_pair_kernel<D, DV, CAUSAL, BIAS>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     return 0;
   }
@@ -729,10 +804,10 @@ int pair_max_clusters(int dev) {
 }
 
 // Launches the persistent pair kernel: min(units, resident clusters) clusters of 2 CTAs.
-template <int D, int DV, bool CAUSAL>
+template <int D, int DV, bool CAUSAL, int BIAS>
 cudaError_t launch_attn_pair(const LaunchArgs &a) {
-  using CF = PairCfg<D, DV, CAUSAL>;
-  auto kern = attn_fwd_pair_kernel<D, DV, CAUSAL>;
+  using CF = PairCfg<D, DV, CAUSAL, BIAS>;
+  auto kern = attn_fwd_pair_kernel<D, DV, CAUSAL, BIAS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_TOTAL);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes attr;
@@ -742,7 +817,7 @@ cudaError_t launch_attn_pair(const LaunchArgs &a) {
   int dev = 0;
   e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int resident = pair_max_clusters<D, DV, CAUSAL>(dev);
+  const int resident = pair_max_clusters<D, DV, CAUSAL, BIAS>(dev);
   if (resident < 1) return cudaErrorLaunchOutOfResources;
   const unsigned units = static_cast<unsigned>(a.p.BH) * static_cast<unsigned>(a.p.ctas_per_head);
   const unsigned clusters = units < static_cast<unsigned>(resident) ? units : static_cast<unsigned>(resident);
@@ -760,7 +835,7 @@ cudaError_t launch_attn_pair(const LaunchArgs &a) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, kern, a.tmQ, a.tmK, a.tmV, a.tmO, a.p);
+  e = cudaLaunchKernelEx(&cfg, kern, a.tmQ, a.tmK, a.tmV, a.tmC, a.tmO, a.p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
