@@ -27,6 +27,12 @@ CASES = [
     (2, 512, 256, 128, 128, NONE, True, 0.0),
     (1, 1000, 2000, 128, 128, CAUSAL | KEY, False, 0.3),
     (1, 640, 384, 64, 64, CAUSAL | KEY, True, 0.2),
+    # Dense bias with 128 value columns (Nk % 4 == 0): the CTA-pair kernel's bias rings,
+    # ragged query and key tails, Nq != Nk with the causal offset, several units per pair.
+    (2, 300, 520, 128, 128, DENSE, False, 0.3),
+    (1, 96, 1024, 64, 128, CAUSAL | DENSE, True, 0.3),
+    (3, 1000, 1000, 128, 128, DENSE, True, 0.1),
+    (2, 777, 388, 64, 128, CAUSAL | DENSE, False, 0.3),
 ]
 
 
