@@ -725,41 +725,55 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         g0 += sch.n_it;
       }
       if (wd.aborted()) settle_after_abort();
-    } else if (warp == CF::VLOAD_WARP && lane == 0) {
-      // ============================================================== TMA: V halves
-      tma_prefetch_desc(&tmV);
-      if constexpr (CF::DENSE) tma_prefetch_desc(&tmC);
+    } else if (warp == CF::VLOAD_WARP && (lane == 0 || (CF::DENSE && lane <= 2))) {
+      // ============================================================== TMA: V halves (lane 0)
+      // and, with a dense bias, lane 1 + w filling warpgroup w's bias ring: three threads of
+      // one warp, each waiting only on its own ring, so neither stream holds up the others.
       bool ok = true;
       int g0 = 0;
-      for (int k = 0; ok; ++k) {
-        const unsigned unit = pair_unit(k, cl, n_cl);
-        if (unit >= n_units) break;
-        const PairSchedule<CAUSAL> sch(p, unit, rank);
-        for (int i = 0; i < sch.n_it; ++i) {
-          const int t = g0 + i;
-          const int j = sch.hi_max - i;
-          const int vs = t % CF::VS;
-          ok = wd.wait1(BAR(CF::B_VEMPTY + vs), ((t / CF::VS) & 1) ^ 1, ROLE_LOAD, CF::B_VEMPTY + vs, false);
-          if (!ok) break;
-          if (leader) mbar_arrive_expect_tx(BAR(CF::B_VFULL + vs), 2 * CF::VH_TILE);
-          pair::tma_load_3d(sbase + CF::V_OFF + vs * CF::VH_TILE, &tmV, CF::VH_COLS * static_cast<int>(rank),
-                            j * BN, sch.bh, LBAR(CF::B_VFULL + vs));
-          if constexpr (CF::DENSE) {
-            // This CTA's 128 bias rows of the tile, as four 128 x 32 chunks (columns past Nk
-            // and rows past Nq arrive as zeros and are masked or not stored).
-            for (int cc = 0; ok && cc < BN / CCHUNK; ++cc) {
-              const int cpos = (BN / CCHUNK) * (t >> 1) + cc;  // tile t goes to warpgroup t % 2's ring
-              const int slot = (t & 1) * CF::RS + cpos % CF::RS;
+      if (lane == 0) {
+        tma_prefetch_desc(&tmV);
+        for (int k = 0; ok; ++k) {
+          const unsigned unit = pair_unit(k, cl, n_cl);
+          if (unit >= n_units) break;
+          const PairSchedule<CAUSAL> sch(p, unit, rank);
+          for (int i = 0; i < sch.n_it; ++i) {
+            const int t = g0 + i;
+            const int j = sch.hi_max - i;
+            const int vs = t % CF::VS;
+            ok = wd.wait1(BAR(CF::B_VEMPTY + vs), ((t / CF::VS) & 1) ^ 1, ROLE_LOAD, CF::B_VEMPTY + vs, false);
+            if (!ok) break;
+            if (leader) mbar_arrive_expect_tx(BAR(CF::B_VFULL + vs), 2 * CF::VH_TILE);
+            pair::tma_load_3d(sbase + CF::V_OFF + vs * CF::VH_TILE, &tmV, CF::VH_COLS * static_cast<int>(rank),
+                              j * BN, sch.bh, LBAR(CF::B_VFULL + vs));
+          }
+          g0 += sch.n_it;
+        }
+      } else if constexpr (CF::DENSE) {
+        // This CTA's 128 bias rows of each of warpgroup w's tiles, as four 128 x 32 chunks
+        // (columns past Nk and rows past Nq arrive as zeros and are masked or not stored).
+        const int w = lane - 1;
+        if (w == 0) tma_prefetch_desc(&tmC);
+        for (int k = 0; ok; ++k) {
+          const unsigned unit = pair_unit(k, cl, n_cl);
+          if (unit >= n_units) break;
+          const PairSchedule<CAUSAL> sch(p, unit, rank);
+          for (int i = 0; ok && i < sch.n_it; ++i) {
+            const int t = g0 + i;
+            if ((t & 1) != w) continue;
+            const int j = sch.hi_max - i;
+            for (int cc = 0; cc < BN / CCHUNK; ++cc) {
+              const int cpos = (BN / CCHUNK) * (t >> 1) + cc;
+              const int slot = w * CF::RS + cpos % CF::RS;
               ok = wd.wait1(BAR(CF::B_CEMPTY + slot), ((cpos / CF::RS) & 1) ^ 1, ROLE_CLOAD, CF::B_CEMPTY + slot, false);
               if (!ok) break;
               mbar_arrive_expect_tx(BAR(CF::B_CFULL + slot), CCHUNK_BYTES);
               tma_load_3d(sbase + CF::C_OFF + slot * CCHUNK_BYTES, &tmC, j * BN + cc * CCHUNK, sch.qt * BM,
                           p.c_shared ? 0 : sch.bh, BAR(CF::B_CFULL + slot));
             }
-            if (!ok) break;
           }
+          g0 += sch.n_it;
         }
-        g0 += sch.n_it;
       }
       if (wd.aborted()) settle_after_abort();
     }
