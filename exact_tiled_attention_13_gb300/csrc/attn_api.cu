@@ -334,20 +334,18 @@ int head_group(int BH, int Nk, int d, int d_v) {
 }
 
 // The persistent CTA-pair kernel (attn_fwd_pair_kernel.cuh) serves problems with 128 value
-// columns in one key range: causal ones without a bias term, and every one with a dense bias
-// read through TMA (there attn_fwd_kernel holds one query tile per CTA and its chain
-// softmax -> P V -> next S is exposed). Everything else goes to attn_fwd_kernel. The pair
-// kernel computes S ahead of the softmax, so a tile that moves the exponent reference waits
-// for the previous P V before rescaling o; on unmasked rows of large scores (many moves, as
-// with the x4 scores of the unmasked benchmark) that costs more than it gains, while
-// attn_fwd_kernel, which computes S(t) only after P(t-1) V, rescales without waiting. With
-// a per-key bias at d = 64 the softmax bounds both kernels and the pair kernel's hand-off of
-// the reference between its warpgroups made it slower (73.5 against 60.4 us on 8 heads of
-// N = 4096).
+// columns in one key range without a bias term (causal or not) or with a dense bias read
+// through TMA (there attn_fwd_kernel holds one query tile per CTA and its chain
+// softmax -> P V -> next S is exposed). Everything else goes to attn_fwd_kernel. Measured on
+// 16 heads of N = 16384 without a mask, the pair kernel is 4 % faster with scores x 4 and 8 %
+// with plain scores, although a tile that moves a row's exponent reference there waits for
+// the previous P V before rescaling o. With a per-key bias at d = 64 the softmax bounds
+// both kernels and the pair kernel's hand-off of the reference between its warpgroups made
+// it slower (73.5 against 60.4 us on 8 heads of N = 4096).
 bool use_pair_kernel(const Problem &a, int n_splits) {
   if (a.d_v != 128 || n_splits != 1) return false;
   const int bias = a.bias();
-  return bias == BIAS_DENSE_TMA || (bias == BIAS_NONE && a.causal());
+  return bias == BIAS_DENSE_TMA || bias == BIAS_NONE;
 }
 
 template <int D, bool C>
