@@ -1,5 +1,5 @@
-// Exact attention forward pass on CTA pairs, for sm_103a (no bias term: the plain and the
-// causal mask, d = 64 or 128, d_v = 128).
+// Exact attention forward pass on CTA pairs, for sm_103a: no bias term or a dense bias read
+// through TMA, with or without the causal mask, d = 64 or 128, d_v = 128.
 //
 // The recurrence is the one in "Compilers and kernels", section "FlashAttention rewrites
 // the algorithm around IO" (b_t, m_t, alpha_t, l_t, o_t, O_i = o_T / l_T), evaluated over
@@ -26,6 +26,11 @@
 // loaded into the second Q buffer, and its first S products and softmax tiles run while the
 // current unit's epilogue runs; its first P V waits only for the epilogue to have read o.
 //
+// With a dense bias each CTA streams its own 128 rows of C: four 128 x 32 fp32 chunks per
+// key tile through two TMA rings, one per softmax warpgroup (each consumed in order by its
+// warpgroup alone), filled by two lanes of the V copy warp; the rings take the room of the
+// deeper K/V rings and of the second Q buffer.
+//
 // Warp roles (16 warps in each CTA):
 //   softmax, warps 0-7: two warpgroups that take the key tiles in turn (tiles are numbered
 //     across units; even tiles in the first warpgroup, odd ones in the second); thread =
@@ -37,15 +42,17 @@
 //     shares are brought to the final reference and added by the epilogue warps. The
 //     warpgroup whose tile moves the reference rescales o (all 128 columns of its rows) once
 //     the previous P V has completed.
-//   epilogue, warps 12-15: per unit, O = o / l staged through the unit's idle Q buffer and
-//     stored as whole 256-byte row segments, and LSE; o is released to the next unit's first
-//     P V as soon as it is in registers, while the softmax warps are already on that unit.
+//   epilogue, warps 12-15: per unit, O = o / l and LSE; o is released to the next unit's
+//     first P V as soon as it is in registers (all 128 columns packed to bf16 first for bf16
+//     output), while the softmax warps are already on that unit; each warp stages its 32 rows
+//     in the unit's idle Q buffer one 32 x 128-byte box at a time and stores them with TMA.
 //   MMA, warps 8 (S products) and 11 (P V products) of the even CTA: issue the pair's
 //     products; each commit signals the mbarrier at the same offset in both CTAs
 //     (multicast). S(t) waits for the softmax to have loaded S(t-2) from its buffer.
-//   Q/K load (warp 9) and V load (warp 10) of both CTAs: TMA copies of this CTA's halves;
-//     completion is signalled on the even CTA's full barriers, whose expected byte count
-//     covers both halves, so an MMA warp waits once per tile.
+//   Q/K load (warp 9) and V load (warp 10, lane 0; lanes 1-2 the bias rings) of both CTAs:
+//     TMA copies of this CTA's halves; completion is signalled on the even CTA's full
+//     barriers, whose expected byte count covers both halves, so an MMA warp waits once per
+//     tile.
 // Every wait is an mbarrier wait bounded in time, as in attn_fwd_kernel.cuh (no named
 // barriers: a warp that gave up cannot leave another waiting forever).
 #pragma once
