@@ -33,6 +33,11 @@ CASES = [
     (1, 96, 1024, 64, 128, CAUSAL | DENSE, True, 0.3),
     (3, 1000, 1000, 128, 128, DENSE, True, 0.1),
     (2, 777, 388, 64, 128, CAUSAL | DENSE, False, 0.3),
+    # No bias, 128 value columns (the CTA-pair kernel): causal with Nq > Nk (units whose rows
+    # see no key), unmasked with ragged query and key tails, d = 64.
+    (2, 900, 300, 128, 128, CAUSAL, False, 0.0),
+    (1, 513, 1000, 64, 128, NONE, True, 0.0),
+    (3, 130, 1030, 128, 128, NONE, False, 0.0),
 ]
 
 
