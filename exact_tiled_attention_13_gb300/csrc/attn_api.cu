@@ -279,7 +279,7 @@ struct Problem {
   }
   int nkv_tiles() const { return (Nk + BN - 1) / BN; }
   int ctas_per_head() const {
-    const int nqc = q_tiles_per_cta(bias());
+    const int nqc = q_tiles_per_cta(bias(), d_v);
     return ((Nq + BM - 1) / BM + nqc - 1) / nqc;
   }
   size_t o_bytes() const {

@@ -10,7 +10,9 @@
 //
 // One CTA owns NQ query tiles of 128 rows of one head (NQ = 2 without a dense bias,
 // so one tile's softmax overlaps the other tile's matrix products; NQ = 1 with a
-// dense bias, whose time is the bias bytes). Warp roles (12 or 8 warps):
+// dense bias, whose time is the bias bytes, and for d_v = 128 without a bias, where
+// this kernel runs only split launches: those cover a few query tiles, and the 32 KB
+// of the second Q slot deepen the K/V rings instead). Warp roles (12 or 8 warps):
 //   softmax warpgroup q (warps 4q..4q+3): thread = query row = tensor-memory lane.
 //     Reads its row of S from tensor memory, masks, takes the tile max b_t, the new
 //     exponent reference and alpha_t, writes P as bf16 back over S, rescales its row of o
@@ -122,7 +124,7 @@ struct Cfg {
   static constexpr bool C_RING = BIAS == BIAS_DENSE_TMA;
   static constexpr bool KEY = BIAS == BIAS_KEY;
   static constexpr bool BIASED = DENSE || KEY;  // scores carry an additive bias
-  static constexpr int NQ = DENSE ? 1 : 2;
+  static constexpr int NQ = (DENSE || (BIAS == BIAS_NONE && DV == 128)) ? 1 : 2;
   static constexpr int Q_TILE = BM * D * 2;
   static constexpr int K_TILE = BN * D * 2;
   static constexpr int V_TILE = BN * DV * 2;
@@ -963,8 +965,8 @@ struct LaunchArgs {
 };
 
 // Number of query tiles one CTA owns (the host sizes the grid with it).
-constexpr int q_tiles_per_cta(int bias) {
-  return (bias == BIAS_DENSE_TMA || bias == BIAS_DENSE_DIRECT) ? 1 : 2;
+constexpr int q_tiles_per_cta(int bias, int d_v) {
+  return (bias == BIAS_DENSE_TMA || bias == BIAS_DENSE_DIRECT || (bias == BIAS_NONE && d_v == 128)) ? 1 : 2;
 }
 
 template <int D, int DV, bool CAUSAL, int BIAS>

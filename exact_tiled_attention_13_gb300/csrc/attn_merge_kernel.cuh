@@ -12,7 +12,7 @@
 //     LSE = M + ln sum_s w_s,
 //
 // since l_s exp(m_s - M) = exp(LSE_s - M). The sum runs over s in increasing order in
-// one thread per output element, so the result is deterministic (no atomics). A row
+// one lane per output element, so the result is deterministic (no atomics). A row
 // whose every range is empty gets O = 0 and LSE = -inf.
 #pragma once
 
@@ -20,74 +20,98 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
 namespace eta {
 
-// One thread per output element: a block of d_v threads per query row, so that every
-// (range, element) load of the whole grid can be in flight at once (the work is a few
-// loads per thread; it is bound by memory latency, not by bandwidth or arithmetic).
+// One warp per query row; lane i holds columns [i*VEC, i*VEC + VEC) of the row (VEC = DV/32
+// consecutive floats, one vector load per range), so a row's partials are read as whole
+// 16-byte (DV = 128) or 8-byte (DV = 64) pieces. The ranges' LSE values are spread over the
+// lanes (range s on lane s mod 32): each weight is computed once and passed on by shuffle.
+// The per-element sums still run over s in increasing order. The merge is a few loads per
+// lane and bound by memory latency, so a lane issues the loads of a whole batch of up to 32
+// ranges before it uses the first.
 // O_part: [S][rows][DV] fp32; L_part: [S][rows] fp32; O: [rows][DV] (fp32 or bf16);
 // LSE: [rows] or null.
 template <int DV>
-__global__ void __launch_bounds__(DV)
+__global__ void __launch_bounds__(128)
     attn_merge_kernel(const float *__restrict__ O_part, const float *__restrict__ L_part,
                       int n_splits, long long rows, void *O, int out_f32, float *LSE) {
-  const long long row = blockIdx.x;
-  const int col = threadIdx.x;
+  static_assert(DV == 64 || DV == 128, "d_v of the merge");
+  constexpr int VEC = DV / 32;
+  constexpr int UNROLL = 32;
+  using vec_t = typename std::conditional<VEC == 4, float4, float2>::type;
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   grid_dep_wait();  // the attention kernel's partials
-  if (col == 0) grid_dep_launch();
+  if (threadIdx.x == 0) grid_dep_launch();
+  if (row >= rows) return;
 
-  // The ranges' loads are independent and issued in batches of 32, so for up to 32
-  // ranges each pass is one memory round trip (the partials usually come from DRAM).
-  constexpr int B = 32;
   float M = -INFINITY;
-  for (int s0 = 0; s0 < n_splits; s0 += B) {
-    float w[B];
+  for (int s0 = 0; s0 < n_splits; s0 += 32)
+    if (s0 + lane < n_splits) M = fmaxf(M, __ldg(L_part + (s0 + lane) * rows + row));
 #pragma unroll
-    for (int k = 0; k < B; ++k) w[k] = __ldg(L_part + (s0 + k < n_splits ? s0 + k : s0) * rows + row);
-#pragma unroll
-    for (int k = 0; k < B; ++k) M = fmaxf(M, w[k]);  // the clamped repeats change nothing
-  }
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
 
-  float acc = 0.0f, wsum = 0.0f;
+  float acc[VEC] = {};
+  float wsum = 0.0f;
   if (M != -INFINITY) {
-    for (int s0 = 0; s0 < n_splits; s0 += B) {
-      float w[B], v[B];
+    const vec_t *src = reinterpret_cast<const vec_t *>(O_part) + row * (DV / VEC) + lane;
+    const long long range_stride = rows * (DV / VEC);
+    for (int s0 = 0; s0 < n_splits; s0 += 32) {
+      // Weight of range s0 + lane (0 past the last range; exp(-inf) = 0 for an empty one).
+      const float wl = s0 + lane < n_splits ? expf(__ldg(L_part + (s0 + lane) * rows + row) - M) : 0.0f;
+      const int n = n_splits - s0 < 32 ? n_splits - s0 : 32;
+      for (int k0 = 0; k0 < n; k0 += UNROLL) {
+        vec_t v[UNROLL];
 #pragma unroll
-      for (int k = 0; k < B; ++k) {
-        const int s = s0 + k < n_splits ? s0 + k : n_splits - 1;  // clamped: weight 0 below
-        w[k] = __ldg(L_part + s * rows + row);
-        v[k] = __ldg(O_part + (s * rows + row) * DV + col);
-      }
-      // In increasing range order, as the sums are defined.
+        for (int k = 0; k < UNROLL; ++k) {
+          const int s = s0 + (k0 + k < n ? k0 + k : n - 1);  // clamped: weight 0 below
+          v[k] = __ldg(src + s * range_stride);
+        }
 #pragma unroll
-      for (int k = 0; k < B; ++k) {
-        const float wk = s0 + k < n_splits ? expf(w[k] - M) : 0.0f;  // 0 for an empty range
-        acc = fmaf(wk, v[k], acc);
-        wsum += wk;
+        for (int k = 0; k < UNROLL; ++k) {
+          const float wk = __shfl_sync(0xFFFFFFFFu, wl, (k0 + k) & 31);
+          const float w = k0 + k < n ? wk : 0.0f;
+          const float *x = reinterpret_cast<const float *>(&v[k]);
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) acc[j] = fmaf(w, x[j], acc[j]);
+          wsum += w;
+        }
       }
     }
   }
-  const float r = wsum > 0.0f ? acc * (1.0f / wsum) : 0.0f;
+  const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
   if (out_f32) {
-    static_cast<float *>(O)[row * DV + col] = r;
+    vec_t r;
+    float *x = reinterpret_cast<float *>(&r);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) x[j] = acc[j] * inv;
+    reinterpret_cast<vec_t *>(O)[row * (DV / VEC) + lane] = r;
   } else {
-    // Pairs of neighbouring columns are packed by the even thread of each pair.
-    const float hi = __shfl_down_sync(0xFFFFFFFFu, r, 1);
-    if ((col & 1) == 0)
-      *reinterpret_cast<uint32_t *>(static_cast<uint16_t *>(O) + row * DV + col) = pack_bf16(r, hi);
+    uint32_t packed[VEC / 2];
+#pragma unroll
+    for (int j = 0; j < VEC / 2; ++j) packed[j] = pack_bf16(acc[2 * j] * inv, acc[2 * j + 1] * inv);
+    uint16_t *dst = static_cast<uint16_t *>(O) + row * DV + lane * VEC;
+    if constexpr (VEC == 4)
+      *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+    else
+      *reinterpret_cast<uint32_t *>(dst) = packed[0];
   }
-  if (LSE != nullptr && col == 0) LSE[row] = wsum > 0.0f ? M + logf(wsum) : -INFINITY;
+  if (LSE != nullptr && lane == 0) LSE[row] = wsum > 0.0f ? M + logf(wsum) : -INFINITY;
 }
 
 template <int DV>
 cudaError_t launch_merge(const float *O_part, const float *L_part, int n_splits, long long rows,
                          void *O, int out_f32, float *LSE, cudaStream_t stream) {
-  if (rows > 0x7FFFFFFFll) return cudaErrorInvalidValue;  // one block per row
-  const cudaError_t e = launch_pdl(attn_merge_kernel<DV>, dim3(static_cast<unsigned>(rows)), dim3(DV), 0, stream,
-                                   O_part, L_part, n_splits, rows, O, out_f32, LSE);
+  constexpr int kRowsPerBlock = 4;  // one warp per row
+  const long long blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (blocks > 0x7FFFFFFFll) return cudaErrorInvalidValue;
+  const cudaError_t e = launch_pdl(attn_merge_kernel<DV>, dim3(static_cast<unsigned>(blocks)),
+                                   dim3(32 * kRowsPerBlock), 0, stream, O_part, L_part, n_splits, rows, O,
+                                   out_f32, LSE);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

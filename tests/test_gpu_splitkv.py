@@ -24,6 +24,9 @@ CASES = [
     (2, 5, 700, 64, 64, CAUSAL | KEY, False, 0.2, 50),
     (1, 256, 1024, 128, 128, DENSE, False, 0.0, 8),
     (8, 128, 8192, 128, 128, CAUSAL, False, 0.0, 0),
+    # More than 32 ranges: the merge takes the ranges' weights 32 at a time.
+    (1, 70, 8192, 64, 64, NONE, True, 0.0, 64),
+    (2, 130, 5000, 128, 128, CAUSAL, False, 0.0, 40),
 ]
 
 
