@@ -26,6 +26,7 @@ SOURCES = [
     "attn_inst_d128_dv128.cu",
     "attn_pair_inst.cu",
     "attn_pair_dense_inst.cu",
+    "attn_pair_key_inst.cu",
     "attn_static_scratch.cu",
     "attn_host_stream.cu",
     "attn_bwd_inst_d64_dv64.cu",

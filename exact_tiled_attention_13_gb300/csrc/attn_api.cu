@@ -30,7 +30,7 @@ ETA_DECLARE(128, 64)
 ETA_DECLARE(128, 128)
 #undef ETA_DECLARE
 #undef ETA_DECLARE_C
-// CTA-pair forward kernels (attn_pair_inst.cu, attn_pair_dense_inst.cu).
+// CTA-pair forward kernels (attn_pair_inst.cu, attn_pair_dense_inst.cu, attn_pair_key_inst.cu).
 template <int D, int DV, bool CAUSAL, int BIAS>
 cudaError_t launch_attn_pair(const LaunchArgs &);
 #define ETA_DECLARE_PAIR(D, C)                                                          \
@@ -41,6 +41,8 @@ ETA_DECLARE_PAIR(64, true)
 ETA_DECLARE_PAIR(128, false)
 ETA_DECLARE_PAIR(128, true)
 #undef ETA_DECLARE_PAIR
+extern template cudaError_t launch_attn_pair<64, 128, false, BIAS_KEY>(const LaunchArgs &);
+extern template cudaError_t launch_attn_pair<64, 128, true, BIAS_KEY>(const LaunchArgs &);
 #define ETA_DECLARE_BWD_C(D, DV, C)                                                       \
   extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_NONE>(const BwdLaunchArgs &);  \
   extern template cudaError_t launch_bwd<D, DV, C, BWD_BIAS_DENSE>(const BwdLaunchArgs &); \
@@ -334,22 +336,26 @@ int head_group(int BH, int Nk, int d, int d_v) {
 }
 
 // The persistent CTA-pair kernel (attn_fwd_pair_kernel.cuh) serves problems with 128 value
-// columns in one key range without a bias term (causal or not) or with a dense bias read
+// columns in one key range without a bias term (causal or not), with a dense bias read
 // through TMA (there attn_fwd_kernel holds one query tile per CTA and its chain
-// softmax -> P V -> next S is exposed). Everything else goes to attn_fwd_kernel. Measured on
-// 16 heads of N = 16384 without a mask, the pair kernel is 4 % faster with scores x 4 and 8 %
-// with plain scores, although a tile that moves a row's exponent reference there waits for
-// the previous P V before rescaling o. With a per-key bias at d = 64 the softmax bounds
-// both kernels and the pair kernel's hand-off of the reference between its warpgroups made
-// it slower (73.5 against 60.4 us on 8 heads of N = 4096).
+// softmax -> P V -> next S is exposed), and at d = 64 with a per-key bias, which it folds
+// into the score product. Everything else goes to attn_fwd_kernel. Measured on 16 heads of
+// N = 16384 without a mask, the pair kernel is 4 % faster with scores x 4 and 8 % with plain
+// scores, although a tile that moves a row's exponent reference there waits for the
+// previous P V before rescaling o. A per-key bias added by the pair kernel's softmax (as the
+// dense bias is) made it slower than attn_fwd_kernel (73.5 against 60.4 us on 8 heads of
+// N = 4096, d = 64): the add and the row maximum it then needs lengthen the hand-off of the
+// reference between its warpgroups; folded into the product, the softmax is the unbiased one.
 bool use_pair_kernel(const Problem &a, int n_splits) {
   if (a.d_v != 128 || n_splits != 1) return false;
   const int bias = a.bias();
-  return bias == BIAS_DENSE_TMA || bias == BIAS_NONE;
+  return bias == BIAS_DENSE_TMA || bias == BIAS_NONE || (bias == BIAS_KEY && a.d == 64);
 }
 
 template <int D, bool C>
 cudaError_t dispatch_pair(int bias, const LaunchArgs &a) {
+  if constexpr (D == 64)
+    if (bias == BIAS_KEY) return launch_attn_pair<D, 128, C, BIAS_KEY>(a);
   return bias == BIAS_DENSE_TMA ? launch_attn_pair<D, 128, C, BIAS_DENSE_TMA>(a)
                                 : launch_attn_pair<D, 128, C, BIAS_NONE>(a);
 }

@@ -65,15 +65,23 @@ template <int D, int DV, bool CAUSAL, int BIAS>
 struct PairCfg {
   static_assert(D == 64 || D == 128, "d must be 64 or 128");
   static_assert(DV == 128, "the pair kernel splits 128 value columns in two 128-byte halves");
-  static_assert(BIAS == BIAS_NONE || BIAS == BIAS_DENSE_TMA, "bias kind");
+  static_assert(BIAS == BIAS_NONE || BIAS == BIAS_DENSE_TMA || BIAS == BIAS_KEY, "bias kind");
   static constexpr bool DENSE = BIAS == BIAS_DENSE_TMA;  // [Nq][Nk] bias rows through a TMA ring
-  static constexpr bool BIASED = DENSE;
+  // A per-key bias c_j rides in the S product: one more 16-wide step of the contraction
+  // with ones on the query side and c_j / scale on the key side (bf16 high and low parts),
+  // so S holds q k + c / scale and the softmax takes the path without a bias.
+  static constexpr bool KEYB = BIAS == BIAS_KEY;
+  static_assert(!KEYB || D == 64, "the key-bias columns take a second 128-byte atom of each K slot (d = 64)");
+  static constexpr bool BIASED = DENSE;  // the softmax adds a bias to scale S itself
   static constexpr int Q_TILE = BM * D * 2;       // this CTA's 128 query rows
   static constexpr int STAGE = 4 * 32 * 128;      // epilogue stage: one 32-row x 128-byte box per epilogue warp
   static constexpr int Q_BUF = Q_TILE > STAGE ? Q_TILE : STAGE;
   static constexpr int KH_ROWS = BN / 2;          // keys of a K tile held by one CTA
   static constexpr int KH_BOX = KH_ROWS * 128;    // one 64-row x 128-byte box
-  static constexpr int KH_TILE = KH_ROWS * D * 2;
+  static constexpr int KH_TILE = KH_ROWS * D * 2;  // bytes of one CTA's K copy
+  // K slot: the K columns in D / 64 atoms of 64 rows x 128 bytes, then, with a per-key bias,
+  // one atom whose logical columns 0 and 1 hold the bias parts (8-15 zero, 16-63 unused).
+  static constexpr int KH_SLOT = KH_TILE + (KEYB ? KH_BOX : 0);
   static constexpr int VH_COLS = DV / 2;          // value columns held by one CTA
   static constexpr int VH_TILE = BN * VH_COLS * 2;
   static constexpr int NS = 2;                    // S buffers (and P buffers) in tensor memory
@@ -85,7 +93,7 @@ struct PairCfg {
   static_assert(VS >= 3, "the softmax tells P(t) V apart by the phase of its V slot");
   static constexpr int Q_OFF = 0;
   static constexpr int K_OFF = Q_OFF + NQB * Q_BUF;
-  static constexpr int V_OFF = K_OFF + KS * KH_TILE;
+  static constexpr int V_OFF = K_OFF + KS * KH_SLOT;
   static constexpr int RX_OFF = V_OFF + VS * VH_TILE;  // references passed on, 2 x 128 fp32
   static constexpr int LX_OFF = RX_OFF + 2 * BM * 4;    // per unit % 2: [m, l, l'][2 warpgroups][128 rows]
   static constexpr int C_OFF = (LX_OFF + 2 * 3 * 2 * BM * 4 + 1023) / 1024 * 1024;  // dense bias rings (128-byte swizzle)
@@ -96,10 +104,14 @@ struct PairCfg {
   static constexpr int RS = DENSE ? cmin(4, (232448 - 1024 - BAR_RESERVE - C_OFF) / (2 * CCHUNK_BYTES)) : 0;
   static constexpr int CS = 2 * RS;
   static_assert(!DENSE || RS >= 2, "need two bias chunks in flight per warpgroup");
-  static constexpr int BAR_OFF = C_OFF + CS * CCHUNK_BYTES;
+  // With a per-key bias: the query side of the bias step, 128 rows whose logical columns 0
+  // and 1 are 1 (8-15 zero), in the 128-byte swizzle of the other operands.
+  static constexpr int ONES_OFF = C_OFF;
+  static constexpr int ONES_BYTES = KEYB ? BM * 128 : 0;
+  static constexpr int BAR_OFF = C_OFF + CS * CCHUNK_BYTES + ONES_BYTES;
   static constexpr int B_QFULL = 0;               // 2: Q of the unit in buffer 0 / 1 landed (both CTAs)
   static constexpr int B_QEMPTY = B_QFULL + 2;    // 2: buffer read by its unit's last S and used by its epilogue (5)
-  static constexpr int B_KFULL = B_QEMPTY + 2;
+  static constexpr int B_KFULL = B_QEMPTY + 2;    // KS: K halves landed (and, with a per-key bias, both CTAs' bias columns)
   static constexpr int B_KEMPTY = B_KFULL + KS;
   static constexpr int B_VFULL = B_KEMPTY + KS;
   static constexpr int B_VEMPTY = B_VFULL + VS;   // P(t) V done (V slot free, P buffer free, o holds P(t) V)
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       mbar_init(BAR(CF::B_QEMPTY + q), 1 + 4);  // the last S's commit and this CTA's 4 epilogue warps
     }
     for (int s = 0; s < CF::KS; ++s) {
-      mbar_init(BAR(CF::B_KFULL + s), 1);
+      mbar_init(BAR(CF::B_KFULL + s), CF::KEYB ? 3 : 1);  // + each CTA's bias-column writer
       mbar_init(BAR(CF::B_KEMPTY + s), 1);
     }
     for (int s = 0; s < CF::VS; ++s) {
@@ -278,6 +290,22 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
+  }
+  if constexpr (CF::KEYB) {
+    // Logical 16-byte unit u of row r sits at unit u ^ (r % 8) of the row (128-byte swizzle).
+    // The ones tile: unit 0 = bf16 (1, 1, 0, ...), unit 1 = 0. Each K slot's bias atom:
+    // unit 1 = 0 here, unit 0 written for every tile.
+    for (int r = threadIdx.x; r < BM; r += CF::THREADS) {
+      uint8_t *row_p = smem + CF::ONES_OFF + r * 128;
+      *reinterpret_cast<uint4 *>(row_p + ((r & 7) << 4)) = make_uint4(0x3F803F80u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4 *>(row_p + ((1 ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int i = threadIdx.x; i < CF::KS * CF::KH_ROWS; i += CF::THREADS) {
+      const int r = i % CF::KH_ROWS;
+      uint8_t *row_p = smem + CF::K_OFF + (i / CF::KH_ROWS) * CF::KH_SLOT + CF::KH_TILE + r * 128;
+      *reinterpret_cast<uint4 *>(row_p + ((1 ^ (r & 7)) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   // The other CTA signals this CTA's barriers, so both CTAs initialise theirs first; and
   // the pair's tensor-memory allocation is one collective instruction of a warp in each
@@ -676,7 +704,7 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
             ETA_TRACE(24);
             tc_fence_after();
             const uint64_t a_desc = smem_desc(sbase + CF::Q_OFF + qb * CF::Q_BUF, 16, 1024);
-            const uint64_t b_desc = smem_desc(sbase + CF::K_OFF + kslot * CF::KH_TILE, 16, 1024);
+            const uint64_t b_desc = smem_desc(sbase + CF::K_OFF + kslot * CF::KH_SLOT, 16, 1024);
             const uint32_t d_tmem = tmem + b * BN;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
@@ -684,6 +712,9 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
               const uint32_t b_off = ((ks / 4) * CF::KH_BOX + (ks % 4) * 32) >> 4;
               pair::mma_ss_elect(d_tmem, a_desc + a_off, b_desc + b_off, CF::IDESC_S, ks > 0 ? 1u : 0u);
             }
+            if constexpr (CF::KEYB)  // S += ones x (c / scale): the bias step
+              pair::mma_ss_elect(d_tmem, smem_desc(sbase + CF::ONES_OFF, 16, 1024), b_desc + (CF::KH_TILE >> 4),
+                                 CF::IDESC_S, 1u);
             ETA_TRACE(25);
             pair::mma_commit_multicast_elect(BAR(CF::B_SFULL + b), both);
             pair::mma_commit_multicast_elect(BAR(CF::B_KEMPTY + kslot), both);
@@ -726,10 +757,24 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
       // Nothing may still be in flight on the tensor cores when tensor memory is freed.
       pair::mma_commit_multicast_elect(BAR(drain_bar), 1);
       wd.drain(BAR(drain_bar), 0, drain_bar);
-    } else if (warp == CF::LOAD_WARP && lane == 0) {
+    } else if (warp == CF::LOAD_WARP && (lane == 0 || CF::KEYB)) {
       // ============================================================== TMA: Q, K halves
-      tma_prefetch_desc(&tmQ);
-      tma_prefetch_desc(&tmK);
+      // Lane 0 issues the copies. With a per-key bias the whole warp runs the loop and also
+      // writes the bias columns of each K slot, two of this CTA's 64 keys a lane: v =
+      // c_j / scale as bf16 parts hi = bf16(v) and lo = bf16(v - hi) (v - hi is exact in
+      // fp32), so hi + lo carries v to about 2^-17 relative; c_j = -inf gives (-inf, 0),
+      // which the product turns into S = -inf (1 x -inf, never 0 x inf); keys past Nk get 0
+      // (their scores are masked). A tile's values are loaded as soon as the previous tile's
+      // columns are out, so the load overlaps the wait for the slot.
+      if (lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+      }
+      auto wait_slot = [&](int b, uint32_t parity) -> bool {
+        return CF::KEYB ? wd.wait(BAR(b), parity, ROLE_LOAD, b) : wd.wait1(BAR(b), parity, ROLE_LOAD, b, false);
+      };
+      const float inv_scale = 1.0f / (p.scale_log2 * LN2);
+      const int r0 = 2 * lane;
       bool ok = true;
       int g0 = 0;
       for (int k = 0; ok; ++k) {
@@ -738,23 +783,50 @@ __global__ void __launch_bounds__(PairCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         const PairSchedule<CAUSAL> sch(p, unit, rank);
         const int qb = k % CF::NQB;
         // Q buffer qb was last used by unit k - NQB (its last S and its epilogue).
-        ok = wd.wait1(BAR(CF::B_QEMPTY + qb), ((k / CF::NQB) & 1) ^ 1, ROLE_LOAD, CF::B_QEMPTY + qb, false);
+        ok = wait_slot(CF::B_QEMPTY + qb, ((k / CF::NQB) & 1) ^ 1);
         if (!ok) break;
-        if (leader) mbar_arrive_expect_tx(BAR(CF::B_QFULL + qb), 2 * CF::Q_TILE);
-        for (int kc = 0; kc < D / SW_CHUNK; ++kc)
-          pair::tma_load_3d(sbase + CF::Q_OFF + qb * CF::Q_BUF + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK,
-                            sch.qt * BM, sch.bh, LBAR(CF::B_QFULL + qb));
+        if (lane == 0) {
+          if (leader) mbar_arrive_expect_tx(BAR(CF::B_QFULL + qb), 2 * CF::Q_TILE);
+          for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+            pair::tma_load_3d(sbase + CF::Q_OFF + qb * CF::Q_BUF + kc * SW_CHUNK_BYTES, &tmQ, kc * SW_CHUNK,
+                              sch.qt * BM, sch.bh, LBAR(CF::B_QFULL + qb));
+        }
+        const float *ck = CF::KEYB ? p.ckey + static_cast<size_t>(sch.bh) * p.Nk : nullptr;
+        auto load_bias = [&](int i, float &c0, float &c1) {
+          const int key = (sch.hi_max - i) * BN + CF::KH_ROWS * static_cast<int>(rank) + r0;
+          c0 = key < p.Nk ? __ldg(ck + key) : 0.0f;
+          c1 = key + 1 < p.Nk ? __ldg(ck + key + 1) : 0.0f;
+        };
+        float c0 = 0.0f, c1 = 0.0f;
+        if (CF::KEYB && sch.n_it > 0) load_bias(0, c0, c1);
         for (int i = 0; i < sch.n_it; ++i) {
           const int t = g0 + i;
           const int j = sch.hi_max - i;
           const int ks = t % CF::KS;
-          ok = wd.wait1(BAR(CF::B_KEMPTY + ks), ((t / CF::KS) & 1) ^ 1, ROLE_LOAD, CF::B_KEMPTY + ks, false);
+          ok = wait_slot(CF::B_KEMPTY + ks, ((t / CF::KS) & 1) ^ 1);
           if (!ok) break;
-          if (p.fault == FAULT_SKIP_FIRST_K && t == 0) continue;  // test hook: a wait runs out
-          if (leader) mbar_arrive_expect_tx(BAR(CF::B_KFULL + ks), 2 * CF::KH_TILE);
-          for (int kc = 0; kc < D / SW_CHUNK; ++kc)
-            pair::tma_load_3d(sbase + CF::K_OFF + ks * CF::KH_TILE + kc * CF::KH_BOX, &tmK, kc * SW_CHUNK,
-                              j * BN + CF::KH_ROWS * static_cast<int>(rank), sch.bh, LBAR(CF::B_KFULL + ks));
+          // Test hook: the first K copy is never issued, so the S product's wait runs out.
+          if (lane == 0 && !(p.fault == FAULT_SKIP_FIRST_K && t == 0)) {
+            if (leader) mbar_arrive_expect_tx(BAR(CF::B_KFULL + ks), 2 * CF::KH_TILE);
+            for (int kc = 0; kc < D / SW_CHUNK; ++kc)
+              pair::tma_load_3d(sbase + CF::K_OFF + ks * CF::KH_SLOT + kc * CF::KH_BOX, &tmK, kc * SW_CHUNK,
+                                j * BN + CF::KH_ROWS * static_cast<int>(rank), sch.bh, LBAR(CF::B_KFULL + ks));
+          }
+          if constexpr (CF::KEYB) {
+            uint8_t *atom = smem + CF::K_OFF + ks * CF::KH_SLOT + CF::KH_TILE;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int r = r0 + e;
+              const float v = (e == 0 ? c0 : c1) * inv_scale;
+              const float hi = __uint_as_float(pack_bf16(0.0f, v) & 0xFFFF0000u);
+              const float lo = isinf(v) ? 0.0f : v - hi;
+              *reinterpret_cast<uint4 *>(atom + r * 128 + ((r & 7) << 4)) = make_uint4(pack_bf16(hi, lo), 0u, 0u, 0u);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) pair::mbar_arrive_cluster(LBAR(CF::B_KFULL + ks));
+            if (i + 1 < sch.n_it) load_bias(i + 1, c0, c1);
+          }
         }
         g0 += sch.n_it;
       }

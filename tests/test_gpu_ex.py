@@ -38,6 +38,13 @@ CASES = [
     (2, 900, 300, 128, 128, CAUSAL, False, 0.0),
     (1, 513, 1000, 64, 128, NONE, True, 0.0),
     (3, 130, 1030, 128, 128, NONE, False, 0.0),
+    # Per-key bias at d = 64 with 128 value columns (the CTA-pair kernel, bias folded into the
+    # score product): ragged tails, Nk not a multiple of 4, causal with Nq > Nk, heavy padding.
+    (2, 300, 520, 64, 128, KEY, False, 0.3),
+    (1, 1000, 1000, 64, 128, CAUSAL | KEY, True, 0.3),
+    (3, 130, 1030, 64, 128, KEY, True, 0.0),
+    (2, 900, 300, 64, 128, CAUSAL | KEY, False, 0.2),
+    (1, 600, 2048, 64, 128, KEY, True, 0.9),
 ]
 
 
@@ -93,3 +100,18 @@ def test_square_ex_matches_attn_fwd_bitwise():
     eta.attn_fwd_ex(Q, K, V, CAUSAL, None, None, c["scale"], O2)
     torch.cuda.synchronize()
     assert torch.equal(O1, O2)
+
+
+def test_key_bias_heads_with_no_allowed_key():
+    """Every key of head 0 padded out (-inf): its rows get O = 0 and LSE = -inf; head 1,
+    padded except for its last key, attends to that key alone. At d = 64 with 128 value
+    columns the bias enters the score product as 1 x (-inf) (never 0 x inf)."""
+    for d, dv in ((64, 128), (64, 64), (128, 128)):
+        c = synth.random_case_ex(4242 + d + dv, 3, 300, 700, d, dv, KEY, 1.0, 0.0)
+        c["ckey"][0, :] = -np.inf
+        c["ckey"][1, :-1] = -np.inf
+        O, L = run_ex(c, True)
+        O_ref, L_ref, _ = oracle.attention_ex(c["Q"], c["K"], c["V"], KEY, None, c["ckey"],
+                                              c["scale"])
+        assert np.all(O[0] == 0.0) and np.all(L[0] == -np.inf)
+        compare(O, L, O_ref, L_ref, label=f"padded heads d{d} dv{dv}")
