@@ -319,10 +319,11 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::A_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
-  // Set-up done: wait for the previous kernel on the stream (programmatic launch) before any
-  // global memory is touched, and let the next one start launching.
-  grid_dep_wait();
-  if (threadIdx.x == 0) grid_dep_launch();
+  // The kernel before this one on the stream is the pre-pass (attn_bwd), which waited for
+  // everything before it: Q, K, V, dO and the biases are final, and only the row statistics
+  // it writes are not. So the copy warp waits for it (programmatic launch) just before its
+  // first copy of the statistics, and only then lets the next kernel start launching (the
+  // dQ kernel relies on that order).
 
   if (warp < CF::A_EW_WARPS) {
     // ============================================================ elementwise
@@ -540,6 +541,7 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::A_THREADS, 1)
                     BAR(CF::BAR_FIXED));
     }
     int issued = 0;
+    bool waited = false;
     for (int it = 0; it < n_it; ++it) {
       const int i = i_lo + it;
       const int slot = it % CF::A_QS;
@@ -555,9 +557,18 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::A_THREADS, 1)
         tma_load_3d(sl + CF::Q_TILE + kc * SW_CHUNK_BYTES, &tmdO, kc * SW_CHUNK, i * BM, bh,
                     BAR(CF::BAR_FULL + slot));
       const size_t lrow = static_cast<size_t>(bh) * p.nqp + static_cast<size_t>(i) * BM;
+      if (!waited) {
+        grid_dep_wait();
+        grid_dep_launch();
+        waited = true;
+      }
       bulk_load(sl + CF::Q_TILE + CF::DO_TILE, p.Lp + lrow, BM * 4, BAR(CF::BAR_FULL + slot));
       bulk_load(sl + CF::Q_TILE + CF::DO_TILE + BM * 4, p.Dd + lrow, BM * 4, BAR(CF::BAR_FULL + slot));
       ++issued;
+    }
+    if (!waited) {  // no query tile (or an abort): the block still ends after the pre-pass
+      grid_dep_wait();
+      grid_dep_launch();
     }
     // The block the hardware will likely start next is about one wave ahead: warm L2 with
     // its K and V tiles (each unit's own) so that its first products do not wait on HBM.
@@ -660,9 +671,13 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_ptr;
-  // Set-up done: wait for the previous kernel on the stream (programmatic launch) before any
-  // global memory is touched, and let the next one start launching.
-  grid_dep_wait();
+  // Set-up done. The kernel before this one on the stream is the dK/dV kernel (launch_bwd),
+  // which writes nothing this kernel reads and lets it launch only once each of its blocks
+  // has waited for the pre-pass: the row statistics are complete by now. So blocks start
+  // beside the dK/dV kernel's last wave without waiting for it; the grid's last block does
+  // wait, so that this kernel completes only after that one (the next kernel on the stream
+  // waits for this one alone). The statistics are read through L2 (__ldcg).
+  if (blockIdx.x == gridDim.x - 1) grid_dep_wait();
   if (threadIdx.x == 0) grid_dep_launch();
 
   if (warp < 8) {
@@ -673,8 +688,8 @@ __global__ void __launch_bounds__(BwdCfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     const bool q_ok = q < p.Nq;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp % 4)) << 16;
     const size_t lrow = static_cast<size_t>(bh) * p.nqp + static_cast<size_t>(q);
-    const float nL = p.Lp[lrow];  // -LSE log2(e); -inf for padding rows and rows with no allowed key
-    const float Dr = p.Dd[lrow];
+    const float nL = __ldcg(p.Lp + lrow);  // -LSE log2(e); -inf for padding rows and rows with no allowed key
+    const float Dr = __ldcg(p.Dd + lrow);
     const int lim = CAUSAL ? q + p.causal_off : INT_MAX;  // last key this row may see
     bool ok = true;
     for (int t = 0; t < n_it; ++t) {
