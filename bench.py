@@ -6,7 +6,9 @@
 A step is one forward pass (one kernel launch) over the whole workload: by default
 batch 2 x 32 heads, N = 8192, d = d_v = 128, causal, bf16 output plus fp32 LSE.
 Inputs are seeded synthetic tensors already resident in device memory; they are
-larger than L2 (514 MiB vs 129 MB), so no flush runs between steps.
+larger than L2 (514 MiB vs 129 MB), so no flush runs between steps, and the steps run
+back to back with CUDA events only at the edges of 20 blocks of steps (an event between
+two launches would serialise them; see launch_timed).
 
 value     : TFLOP/s over the K timed steps (FLOPs 2 BH N^2 (d + d_v), halved for causal),
             summed over ranks, timed with CUDA events between barriers, max over ranks
@@ -257,7 +259,7 @@ def config_dict(w, world):
            "mask": synth.MODE_NAMES[w.mode], "out_dtype": w.out_dtype, "lse": "fp32",
            "qk_scale_mult": w.qk_mult, "key_pad_p": w.p_mask,
            "parallelism": f"replicas x{world} (heads independent, no collective)",
-           "l2": "inputs larger than L2 (no flush)" if not needs_flush(w)
+           "l2": "inputs larger than L2 (no flush; launches back to back, events at the edges of 20 blocks of steps)" if not needs_flush(w)
            else "L2 flushed between steps (a 256 MB write outside the timed launches)"}
     if w.Nkv != w.N:
         cfg["N_q"], cfg["N_k"] = w.N, w.Nkv
@@ -364,29 +366,60 @@ def run_reference(args):
     return 0
 
 
+TIMING_BLOCKS = 20
+
+
+def launch_timed(wl, stream, steps, flush):
+    """Enqueues `steps` steps of `wl` on `stream` inside CUDA events; returns a function that,
+    after a synchronize, gives (per-step times in ms, region time in ms).
+
+    With `flush` (inputs that fit in L2) a buffer twice the size of L2 is written before
+    every step, outside the events around the step's launches, and the per-step times are
+    those events. Without it the steps run back to back and events are recorded only at the
+    edges of TIMING_BLOCKS blocks of steps: an event between two launches serialises them
+    (each kernel may otherwise start its set-up under its predecessor's tail, through
+    programmatic dependent launch), so events around every launch would add a launch gap to
+    every step. The per-step times are then the blocks' mean step times."""
+    import torch
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    if flush is not None:
+        starts, ends = [ev() for _ in range(steps)], [ev() for _ in range(steps)]
+        r0, r1 = ev(), ev()
+        r0.record(stream)
+        for i in range(steps):
+            flush.fill_(float(i))
+            starts[i].record(stream)
+            wl.launch(stream)
+            ends[i].record(stream)
+        r1.record(stream)
+        return lambda: (np.array([a.elapsed_time(b) for a, b in zip(starts, ends)]), r0.elapsed_time(r1))
+    nb = max(1, min(TIMING_BLOCKS, steps))
+    edges = [round(b * steps / nb) for b in range(nb + 1)]
+    marks = [ev() for _ in range(nb + 1)]
+    marks[0].record(stream)
+    for b in range(nb):
+        for _ in range(edges[b], edges[b + 1]):
+            wl.launch(stream)
+        marks[b + 1].record(stream)
+    return lambda: (np.array([marks[b].elapsed_time(marks[b + 1]) / (edges[b + 1] - edges[b])
+                              for b in range(nb) if edges[b + 1] > edges[b]]),
+                    marks[0].elapsed_time(marks[nb]))
+
+
 def time_steps(wl, stream, steps, warmup, flush, device):
-    """Per-step CUDA-event times (ms) of `steps` launches of `wl` after `warmup` untimed
-    ones, and the time of the whole region. With `flush` (inputs that fit in L2) a buffer
-    twice the size of L2 is written before every timed launch, outside its events."""
+    """Step times (ms; see launch_timed) of `steps` steps of `wl` after `warmup` untimed
+    ones, and the time of the whole region."""
     import torch
 
     for _ in range(max(3, warmup)):
         wl.launch(stream)
     torch.cuda.synchronize(device)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
-    r0 = torch.cuda.Event(enable_timing=True)
-    r1 = torch.cuda.Event(enable_timing=True)
-    r0.record(stream)
-    for i in range(steps):
-        if flush is not None:
-            flush.fill_(float(i))
-        starts[i].record(stream)
-        wl.launch(stream)
-        ends[i].record(stream)
-    r1.record(stream)
+    result = launch_timed(wl, stream, steps, flush)
     torch.cuda.synchronize(device)
-    return np.array([a.elapsed_time(b) for a, b in zip(starts, ends)]), r0.elapsed_time(r1)
+    return result()
 
 
 def launch_floor_ms(stream, steps, flush, device):
@@ -464,7 +497,8 @@ def other_workloads(args, stream, device, local):
                  "algorithmic_flops": F, "algorithmic_bytes": B,
                  "l2": ("L2 flushed between steps (a 258 MB write outside each step's events); "
                         "step time = mean of the launches' own event times") if flush is not None
-                 else "inputs larger than L2, launches back to back; step time = region / steps",
+                 else ("inputs larger than L2, launches back to back (events at the edges of 20 blocks "
+                       "of steps); step time = region / steps, percentiles over the blocks' mean steps"),
                  "step_ms_percentiles": {"p10": float(np.percentile(per_step, 10)),
                                          "p50": float(np.percentile(per_step, 50)),
                                          "p90": float(np.percentile(per_step, 90))},
@@ -508,24 +542,13 @@ def run_ours(args):
     # twice the size of L2; the step time is then the sum of the launches' own times.
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device) if needs_flush(w) else None
     K = args.steps
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    region_start = torch.cuda.Event(enable_timing=True)
-    region_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     barrier(dist, device)
     torch.cuda.synchronize(device)
     t_wall0 = time.time()
-    region_start.record(stream)
-    for i in range(K):
-        if flush is not None:
-            flush.fill_(float(i))
-        starts[i].record(stream)
-        wl.launch(stream)
-        ends[i].record(stream)
-    region_end.record(stream)
+    timed = launch_timed(wl, stream, K, flush)
     torch.cuda.synchronize(device)
     t_wall1 = time.time()
     barrier(dist, device)
@@ -534,10 +557,9 @@ def run_ours(args):
     if code != eta.ATTN_OK:
         raise SystemExit(f"watchdog tripped in the timed region: {word:#x}")
 
-    region_ms = region_start.elapsed_time(region_end)
-    per_step = np.array([s.elapsed_time(e) for s, e in zip(starts, ends)])
-    kernel_ms = float(np.mean(per_step))
-    step_ms = reduce_max(dist, kernel_ms if flush is not None else region_ms / K, device)
+    per_step, region_ms = timed()
+    kernel_ms = float(np.mean(per_step)) if flush is not None else region_ms / K
+    step_ms = reduce_max(dist, kernel_ms, device)
     value = world * F / (step_ms * 1e-3) / 1e12
 
     # End to end through the public call: pinned host inputs in, host outputs out.
