@@ -153,9 +153,13 @@ struct Cfg {
   static constexpr int B_CEMPTY = B_CFULL + CS;
   static constexpr int B_KBFULL = B_CEMPTY + CS;
   static constexpr int B_KBEMPTY = B_KBFULL + KB;
-  static constexpr int B_SFULL = B_KBEMPTY + KB;  // S_q ready (and the previous P_q V done)
-  static constexpr int B_PFULL = B_SFULL + NQ;    // P_q written and o_q rescaled
-  static constexpr int B_OFULL = B_PFULL + NQ;    // last P_q V done
+  // S buffers in tensor memory: one per query tile, or two with one query tile, so that
+  // S(t + 1) is computed while the softmax works on S(t).
+  static constexpr bool DBUF = NQ == 1;
+  static constexpr int NSB = DBUF ? 2 : NQ;
+  static constexpr int B_SFULL = B_KBEMPTY + KB;  // S buffer ready (with two query tiles: and the previous P_q V done)
+  static constexpr int B_PFULL = B_SFULL + NSB;   // P written over S buffer b and o rescaled
+  static constexpr int B_OFULL = B_PFULL + NSB;   // last P_q V done
   static constexpr int B_DRAIN = B_OFULL + NQ;
   static constexpr int NUM_BARS = B_DRAIN + 1;
   static constexpr int TMEMPTR_OFF = BAR_OFF + NUM_BARS * 8;
@@ -190,10 +194,10 @@ struct Cfg {
                 "register split exceeds the registers the block is launched with");
   static_assert(!SPLIT_REGS || (REGS_SOFTMAX >= LAUNCH_REGS && REGS_CTRL <= LAUNCH_REGS),
                 "softmax warpgroups grow, the control warpgroup shrinks");
-  // tensor memory: S_q at columns [q*128, q*128+128), o_q after all S tiles
+  // tensor memory: S buffer b at columns [b*128, b*128+128), o_q after all S buffers
   static constexpr int S_COL = 0;
-  static constexpr int O_COL = NQ * BN;
-  static constexpr int TMEM_COLS = pow2_at_least(NQ * (BN + DV));
+  static constexpr int O_COL = NSB * BN;
+  static constexpr int TMEM_COLS = pow2_at_least(NSB * BN + NQ * DV);
   static_assert(TMEM_COLS <= 512, "tensor memory holds 512 columns");
 
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);
@@ -375,11 +379,11 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         mbar_init(BAR(CF::B_KBEMPTY + s), consumers > 0 ? consumers : 1);
       }
     }
-    for (int q = 0; q < NQ; ++q) {
-      mbar_init(BAR(CF::B_SFULL + q), 1);
-      mbar_init(BAR(CF::B_PFULL + q), 4);  // one arrival per softmax warp
-      mbar_init(BAR(CF::B_OFULL + q), 1);
+    for (int b = 0; b < CF::NSB; ++b) {
+      mbar_init(BAR(CF::B_SFULL + b), 1);
+      mbar_init(BAR(CF::B_PFULL + b), 4);  // one arrival per softmax warp
     }
+    for (int q = 0; q < NQ; ++q) mbar_init(BAR(CF::B_OFULL + q), 1);
     mbar_init(BAR(CF::B_DRAIN), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -433,7 +437,11 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
     if (exists && has_keys) {
       for (int it = sch.first_it(q); it < sch.n_it; ++it) {
         const int j = sch.hi_max - it;
-        ok = wd.wait(BAR(CF::B_SFULL + q), s_phase, ROLE_SOFTMAX, CF::B_SFULL + q);
+        // This tile's S buffer: the query tile's own, or (one query tile) buffer it % 2.
+        const int sb = CF::DBUF ? (it & 1) : q;
+        const uint32_t t_sb = CF::DBUF ? t_s + static_cast<uint32_t>((it & 1) * BN) : t_s;
+        ok = wd.wait(BAR(CF::B_SFULL + sb), CF::DBUF ? static_cast<uint32_t>((it >> 1) & 1) : s_phase,
+                     ROLE_SOFTMAX, CF::B_SFULL + sb);
         s_phase ^= 1;
         if (!ok) break;
         tc_fence_after();
@@ -441,10 +449,10 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 
         // Row of S (raw Q K^T) for this thread's query, 128 keys.
         uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(t_s + 0, r0);
-        tmem_ld32(t_s + 32, r1);
-        tmem_ld32(t_s + 64, r2);
-        tmem_ld32(t_s + 96, r3);
+        tmem_ld32(t_sb + 0, r0);
+        tmem_ld32(t_sb + 32, r1);
+        tmem_ld32(t_sb + 64, r2);
+        tmem_ld32(t_sb + 96, r3);
         tmem_wait_ld(r0);
         tmem_wait_ld(r1);
         tmem_wait_ld(r2);
@@ -535,9 +543,18 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
         const float alpha = move ? ex2_approx(m2 - m_use) : 1.0f;
         if (__any_sync(0xFFFFFFFFu, move) && it > sch.first_it(q)) {
-          // o_t = alpha_t o_{t-1}: the previous P V has completed (the S tile just read was
-          // committed after it). Rare once a row has seen its largest scores. On a query
-          // tile's first K/V tile o holds no result yet (the first P V overwrites it).
+          // o_t = alpha_t o_{t-1} once the previous P V has completed: with two query tiles
+          // the S tile just read was committed after it; with two S buffers S(it) is issued
+          // before P(it-1) V, so wait for that product's commit on its V slot. (Every
+          // earlier P V completed before S(it), so the slot's phases cannot be confused.)
+          // Rare once a row has seen its largest scores. On a query tile's first K/V tile
+          // o holds no result yet (the first P V overwrites it).
+          if constexpr (CF::DBUF) {
+            const int pv = it - 1;
+            ok = wd.wait(BAR(CF::B_VEMPTY + pv % CF::VS), (pv / CF::VS) & 1, ROLE_SOFTMAX, CF::B_VEMPTY + pv % CF::VS);
+            if (!ok) break;
+            tc_fence_after();
+          }
 #pragma unroll
           for (int cc = 0; cc < DV / 32; ++cc) {
             uint32_t o[32];
@@ -578,12 +595,12 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
             add2(s[k], s[k + 1], s[k], s[k + 1], p0, p1);
             pk[16 * (qq & 1) + c2] = pack_bf16(p0, p1);
           }
-          if (qq & 1) tmem_st32(t_s + 32 * (qq / 2), pk);
+          if (qq & 1) tmem_st32(t_sb + 32 * (qq / 2), pk);
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        mbar_arrive_elect(BAR(CF::B_PFULL + q));
+        mbar_arrive_elect(BAR(CF::B_PFULL + sb));
         ETA_TRACE(4);
 
         // l_t = alpha_t l_{t-1} + sum_j p_ij.
@@ -752,21 +769,21 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
 
       // The descriptors' address field holds (address >> 4) in 14 bits; shared-memory
       // addresses stay below 2^18, so adding (offset >> 4) to a descriptor never carries.
-      auto issue_s = [&](int q, int kslot) {
+      auto issue_s = [&](int q, int kslot, int b) {  // S buffer b = Q_q K^T
         const uint64_t a_desc = smem_desc(sbase + CF::Q_OFF + q * CF::Q_TILE, 16, 1024);
         const uint64_t b_desc = smem_desc(sbase + CF::K_OFF + kslot * CF::K_TILE, 16, 1024);
-        const uint32_t d_tmem = tmem + CF::S_COL + q * BN;
+        const uint32_t d_tmem = tmem + CF::S_COL + b * BN;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = ((ks / 4) * SW_CHUNK_BYTES + (ks % 4) * 32) >> 4;
           mma_ss_elect(d_tmem, a_desc + off, b_desc + off, CF::IDESC_S, ks > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int q, int vslot, bool accumulate) {
+      auto issue_pv = [&](int q, int vslot, bool accumulate, int b) {  // o_q += P (S buffer b) V
         const uint64_t b_desc =
             smem_desc(sbase + CF::V_OFF + vslot * CF::V_TILE, SW_CHUNK_BYTES, 1024);
         const uint32_t d_tmem = tmem + CF::O_COL + q * DV;
-        const uint32_t a_tmem = tmem + CF::S_COL + q * BN;
+        const uint32_t a_tmem = tmem + CF::S_COL + b * BN;
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
           mma_ts_elect(d_tmem, a_tmem + ks * 8, b_desc + ((ks * 16 * 128) >> 4), CF::IDESC_PV,
@@ -779,49 +796,84 @@ __global__ void __launch_bounds__(Cfg<D, DV, CAUSAL, BIAS>::THREADS, 1)
         return r;
       };
 
-      for (int it = 0; ok && it < sch.n_it; ++it) {
-        const int kslot = it % CF::KS;
-        const int vprev = (it + CF::VS - 1) % CF::VS;
-        ok = wd.wait(BAR(CF::B_KFULL + kslot), (it / CF::KS) & 1, ROLE_MMA, CF::B_KFULL + kslot);
-        ETA_TRACE(20);
-        if (ok && it > 0)
-          ok = wd.wait(BAR(CF::B_VFULL + vprev), ((it - 1) / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vprev);
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          if (it < sch.first_it(q)) continue;
-          ETA_TRACE(21);
-          if (it > sch.first_it(q)) {
-            ok = wait_pv_inputs(q);
-            if (!ok) break;
-            ETA_TRACE(22 + q);
-            tc_fence_after();
-            issue_pv(q, vprev, it - 1 > sch.first_it(q));  // o_q += P_q V_{it-1}
-          }
-          issue_s(q, kslot);  // S_q = Q_q K_it^T
-          mma_commit_elect(BAR(CF::B_SFULL + q));
-          ETA_TRACE(24 + q);
-        }
-        if (!ok) break;
-        mma_commit_elect(BAR(CF::B_KEMPTY + kslot));
-        if (it > 0) mma_commit_elect(BAR(CF::B_VEMPTY + vprev));
-      }
-      if (ok && sch.n_it > 0) {
-        const int last = sch.n_it - 1;
-        const int vslot = last % CF::VS;
-        ok = wd.wait(BAR(CF::B_VFULL + vslot), (last / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
-        if (ok) tc_fence_after();
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          if (!ok || sch.first_it(q) >= sch.n_it) continue;
-          ok = wait_pv_inputs(q);
+      if constexpr (CF::DBUF) {
+        // One query tile, two S buffers: S(it) goes to buffer it % 2 as soon as K(it) has
+        // landed, ahead of P(it-1) V, whose P the softmax may still be writing. S(it)
+        // overwrites P(it-2), which P(it-2) V, issued before it, has read.
+        for (int it = 0; ok && it < sch.n_it; ++it) {
+          const int kslot = it % CF::KS;
+          ok = wd.wait(BAR(CF::B_KFULL + kslot), (it / CF::KS) & 1, ROLE_MMA, CF::B_KFULL + kslot);
           if (!ok) break;
           tc_fence_after();
-          issue_pv(q, vslot, last > sch.first_it(q));
-          mma_commit_elect(BAR(CF::B_OFULL + q));
+          issue_s(0, kslot, it & 1);  // S buffer it % 2 = Q K_it^T
+          mma_commit_elect(BAR(CF::B_SFULL + (it & 1)));
+          mma_commit_elect(BAR(CF::B_KEMPTY + kslot));
+          if (it > 0) {
+            const int pv = it - 1, vslot = pv % CF::VS;
+            ok = wd.wait(BAR(CF::B_VFULL + vslot), (pv / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
+            if (ok) ok = wd.wait(BAR(CF::B_PFULL + (pv & 1)), (pv >> 1) & 1, ROLE_MMA, CF::B_PFULL + (pv & 1));
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(0, vslot, pv > 0, pv & 1);  // o += P_{it-1} V_{it-1}
+            mma_commit_elect(BAR(CF::B_VEMPTY + vslot));
+          }
         }
-        if (ok) mma_commit_elect(BAR(CF::B_VEMPTY + vslot));
+        if (ok && sch.n_it > 0) {
+          const int pv = sch.n_it - 1, vslot = pv % CF::VS;
+          ok = wd.wait(BAR(CF::B_VFULL + vslot), (pv / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
+          if (ok) ok = wd.wait(BAR(CF::B_PFULL + (pv & 1)), (pv >> 1) & 1, ROLE_MMA, CF::B_PFULL + (pv & 1));
+          if (ok) {
+            tc_fence_after();
+            issue_pv(0, vslot, pv > 0, pv & 1);
+            mma_commit_elect(BAR(CF::B_OFULL));
+            mma_commit_elect(BAR(CF::B_VEMPTY + vslot));
+          }
+        }
+      } else {
+        for (int it = 0; ok && it < sch.n_it; ++it) {
+          const int kslot = it % CF::KS;
+          const int vprev = (it + CF::VS - 1) % CF::VS;
+          ok = wd.wait(BAR(CF::B_KFULL + kslot), (it / CF::KS) & 1, ROLE_MMA, CF::B_KFULL + kslot);
+          ETA_TRACE(20);
+          if (ok && it > 0)
+            ok = wd.wait(BAR(CF::B_VFULL + vprev), ((it - 1) / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vprev);
+          if (!ok) break;
+          tc_fence_after();
+  #pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            if (it < sch.first_it(q)) continue;
+            ETA_TRACE(21);
+            if (it > sch.first_it(q)) {
+              ok = wait_pv_inputs(q);
+              if (!ok) break;
+              ETA_TRACE(22 + q);
+              tc_fence_after();
+              issue_pv(q, vprev, it - 1 > sch.first_it(q), q);  // o_q += P_q V_{it-1}
+            }
+            issue_s(q, kslot, q);  // S_q = Q_q K_it^T
+            mma_commit_elect(BAR(CF::B_SFULL + q));
+            ETA_TRACE(24 + q);
+          }
+          if (!ok) break;
+          mma_commit_elect(BAR(CF::B_KEMPTY + kslot));
+          if (it > 0) mma_commit_elect(BAR(CF::B_VEMPTY + vprev));
+        }
+        if (ok && sch.n_it > 0) {
+          const int last = sch.n_it - 1;
+          const int vslot = last % CF::VS;
+          ok = wd.wait(BAR(CF::B_VFULL + vslot), (last / CF::VS) & 1, ROLE_MMA, CF::B_VFULL + vslot);
+          if (ok) tc_fence_after();
+  #pragma unroll
+          for (int q = 0; q < NQ; ++q) {
+            if (!ok || sch.first_it(q) >= sch.n_it) continue;
+            ok = wait_pv_inputs(q);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(q, vslot, last > sch.first_it(q), q);
+            mma_commit_elect(BAR(CF::B_OFULL + q));
+          }
+          if (ok) mma_commit_elect(BAR(CF::B_VEMPTY + vslot));
+        }
       }
       // Nothing may still be in flight on the tensor cores when tensor memory is freed.
       mma_commit_elect(BAR(CF::B_DRAIN));
