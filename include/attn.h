@@ -125,7 +125,11 @@ ATTN_API int attn_fwd(const void *Q, const void *K, const void *V, int mode, con
  *         (DENSE and KEY together are rejected: add the vector into C instead; SHARED needs
  *         DENSE)
  *   C     fp32 [BH][Nq][Nk] with ATTN_BIAS_DENSE ([Nq][Nk] with ATTN_BIAS_SHARED), else NULL
- *   ckey  fp32 [BH][Nk] with ATTN_BIAS_KEY, else NULL; 4-byte aligned; finite or -inf
+ *   ckey  fp32 [BH][Nk] with ATTN_BIAS_KEY, else NULL; 4-byte aligned; finite or -inf.
+ *         At d = 64, d_v = 128 (one key range) the bias enters the score product as
+ *         c_j / scale in two bf16 parts, carried to about 2^-17 relative; finite values
+ *         need |c_j| < 3.3e38 * scale there (4.1e37 at scale 1/8), as they need
+ *         |c_j| < 2.3e38 on the other paths, which scale them by log2(e).
  *   Nq    >= 0 (0: no-op); Nk >= 1 when Nq >= 1
  *   O     [BH][Nq][d_v];  LSE fp32 [BH][Nq] or NULL
  * The causal mask aligns the last query with the last key: query i may see keys
