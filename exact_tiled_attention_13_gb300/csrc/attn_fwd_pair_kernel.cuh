@@ -1,5 +1,6 @@
-// Exact attention forward pass on CTA pairs, for sm_103a: no bias term or a dense bias read
-// through TMA, with or without the causal mask, d = 64 or 128, d_v = 128.
+// Exact attention forward pass on CTA pairs, for sm_103a: no bias term, a dense bias read
+// through TMA, or (d = 64) a per-key bias, with or without the causal mask, d = 64 or 128,
+// d_v = 128.
 //
 // The recurrence is the one in "Compilers and kernels", section "FlashAttention rewrites
 // the algorithm around IO" (b_t, m_t, alpha_t, l_t, o_t, O_i = o_T / l_T), evaluated over
@@ -31,6 +32,12 @@
 // warpgroup alone), filled by two lanes of the V copy warp; the rings take the room of the
 // deeper K/V rings and of the second Q buffer.
 //
+// A per-key bias c_j is not added by the softmax (that add and the row maximum it then
+// needs would lengthen the hand-off between the warpgroups) but folded into the S product:
+// each K slot holds a second 128-byte atom whose logical columns 0 and 1 are c_j / scale as
+// bf16 high and low parts for this CTA's 64 keys, written by the Q/K copy warp, and a
+// constant tile of ones is the query side of one more 16-wide step of the contraction.
+//
 // Warp roles (16 warps in each CTA):
 //   softmax, warps 0-7: two warpgroups that take the key tiles in turn (tiles are numbered
 //     across units; even tiles in the first warpgroup, odd ones in the second); thread =
@@ -52,7 +59,8 @@
 //   Q/K load (warp 9) and V load (warp 10, lane 0; lanes 1-2 the bias rings) of both CTAs:
 //     TMA copies of this CTA's halves; completion is signalled on the even CTA's full
 //     barriers, whose expected byte count covers both halves, so an MMA warp waits once per
-//     tile.
+//     tile. With a per-key bias the whole Q/K warp runs its loop and writes each K slot's
+//     bias columns; each CTA's writers add one arrival to the even CTA's K-full barrier.
 // Every wait is an mbarrier wait bounded in time, as in attn_fwd_kernel.cuh (no named
 // barriers: a warp that gave up cannot leave another waiting forever).
 #pragma once
