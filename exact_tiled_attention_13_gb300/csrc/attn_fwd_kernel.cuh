@@ -12,7 +12,9 @@
 // so one tile's softmax overlaps the other tile's matrix products; NQ = 1 with a
 // dense bias, whose time is the bias bytes, and for d_v = 128 without a bias, where
 // this kernel runs only split launches: those cover a few query tiles, and the 32 KB
-// of the second Q slot deepen the K/V rings instead). Warp roles (12 or 8 warps):
+// of the second Q slot deepen the K/V rings instead). With one query tile, tensor memory
+// holds two S buffers that the key tiles take in turn: S(t) is computed ahead of
+// P(t-1) V, while the softmax still works on tile t-1. Warp roles (12 or 8 warps):
 //   softmax warpgroup q (warps 4q..4q+3): thread = query row = tensor-memory lane.
 //     Reads its row of S from tensor memory, masks, takes the tile max b_t, the new
 //     exponent reference and alpha_t, writes P as bf16 back over S, rescales its row of o
