@@ -115,3 +115,27 @@ def test_key_bias_heads_with_no_allowed_key():
                                               c["scale"])
         assert np.all(O[0] == 0.0) and np.all(L[0] == -np.inf)
         compare(O, L, O_ref, L_ref, label=f"padded heads d{d} dv{dv}")
+
+
+@pytest.mark.parametrize("BH,Nq,Nk,mode", [(1, 1, 700, KEY), (5, 64, 256, CAUSAL | KEY)],
+                         ids=["one-query", "causal-short"])
+def test_key_bias_pair_without_lse(BH, Nq, Nk, mode):
+    """Per-key bias on the CTA-pair path (d = 64, d_v = 128) with LSE = NULL: O alone is
+    written, and it equals the oracle's."""
+    import torch
+
+    import exact_tiled_attention_13_gb300 as eta
+
+    c = synth.random_case_ex(4700 + Nq + Nk, BH, Nq, Nk, 64, 128, mode, 1.0, 0.3)
+
+    def bits(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+
+    O = torch.full((BH, Nq, 128), float("nan"), device="cuda")
+    eta.attn_fwd_ex(bits(c["Q"]), bits(c["K"]), bits(c["V"]), mode, None,
+                    torch.from_numpy(c["ckey"]).cuda(), c["scale"], O, None)
+    torch.cuda.synchronize()
+    code, word = eta.attn_device_status(None)
+    assert code == eta.ATTN_OK, f"watchdog {word:#x}"
+    O_ref, L_ref, _ = oracle.attention_ex(c["Q"], c["K"], c["V"], mode, None, c["ckey"], c["scale"])
+    compare(O.cpu().numpy().astype(np.float64), L_ref, O_ref, L_ref, label=f"no LSE {BH}x{Nq}x{Nk}")
